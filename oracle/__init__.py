@@ -1,0 +1,154 @@
+"""Python wrapper of the fp64 CPU oracle for jagged GDPA.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``.  The library path never imports it.
+
+The oracle is plain C (``oracle.c``), compiled here with gcc into
+``oracle/_build/liboracle.so``.  It takes the bf16 inputs decoded exactly to
+float64 and returns float64 outputs.  Definitions and the readings of the
+pages are in the header comment of ``oracle.c``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT = os.path.join(_HERE, "_build", "liboracle.so")
+
+ACT_CODE = {"gelu": 0, "silu": 1, "softmax": 2, "identity": 3}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (-O2, OpenMP, no fast-math) into _build/."""
+    if not force and os.path.exists(_OUT) and os.path.getmtime(_OUT) >= os.path.getmtime(_SRC):
+        return _OUT
+    os.makedirs(os.path.dirname(_OUT), exist_ok=True)
+    tmp = _OUT + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-fPIC", "-shared", "-fopenmp",
+                    "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, _OUT)
+    return _OUT
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+        lib.oracle_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32,
+                                   P, i32, i32, P, P]
+        lib.oracle_fwd.restype = ctypes.c_int
+        lib.oracle_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32,
+                                   P, i32, i32, P, P, P, P]
+        lib.oracle_bwd.restype = ctypes.c_int
+        lib.oracle_act_eval.argtypes = [i32, P, i64, P, P]
+        lib.oracle_act_eval.restype = ctypes.c_int
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        t = t.detach().to("cpu").to(torch.float64).numpy()
+    return np.ascontiguousarray(t, dtype=np.float64)
+
+
+def _i32(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        t = t.detach().to("cpu").numpy()
+    return np.ascontiguousarray(t, dtype=np.int32)
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def act(name: str, x) -> tuple[np.ndarray, np.ndarray]:
+    """act(x) and act'(x) in fp64 for 'gelu', 'silu' or 'identity'."""
+    x = _f64(x).ravel()
+    y = np.empty_like(x)
+    dy = np.empty_like(x)
+    if _load().oracle_act_eval(ACT_CODE[name], _ptr(x), x.size, _ptr(y), _ptr(dy)):
+        raise ValueError(f"oracle has no element-wise activation {name!r}")
+    return y, dy
+
+
+def _units(units: Optional[Sequence[int]]):
+    if units is None:
+        return None, 0
+    u = np.ascontiguousarray(units, dtype=np.int32)
+    return u, int(u.size)
+
+
+def fwd(q, k, v, q_offsets, kv_offsets, heads: int, head_dim: int, act: str, scale: float,
+        bias=None, causal: bool = False, units: Optional[Sequence[int]] = None,
+        threads: int = 0):
+    """O (float64 [total_q, H, d]) and LSE (float64 [H, total_q]).
+
+    ``units`` restricts the work to (segment, head) units b*H + h; rows of
+    other units are returned as NaN.
+    """
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    bf = None if bias is None else _f64(bias)
+    bias_len = 0 if bf is None else int(bf.shape[1])
+    total_q = int(qo[-1])
+    out = np.full((total_q, heads, head_dim), np.nan)
+    lse = np.full((heads, total_q), np.nan)
+    u, nu = _units(units)
+    rc = _load().oracle_fwd(_ptr(qf), _ptr(kf), _ptr(vf), _ptr(qo), _ptr(ko), len(qo) - 1,
+                            heads, head_dim, ACT_CODE[act], float(scale), _ptr(bf), bias_len,
+                            int(bool(causal)), _ptr(u), nu, int(threads), _ptr(out), _ptr(lse))
+    if rc:
+        raise ValueError("oracle_fwd rejected its arguments")
+    return out, lse
+
+
+def bwd(q, k, v, dout, q_offsets, kv_offsets, heads: int, head_dim: int, act: str,
+        scale: float, bias=None, causal: bool = False,
+        units: Optional[Sequence[int]] = None, threads: int = 0):
+    """dQ, dK, dV (float64, layouts of q/k/v) and dbias (float64 [H, T] or None)."""
+    qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(dout)
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    bf = None if bias is None else _f64(bias)
+    bias_len = 0 if bf is None else int(bf.shape[1])
+    dq = np.full(qf.shape, np.nan)
+    dk = np.full(kf.shape, np.nan)
+    dv = np.full(vf.shape, np.nan)
+    dbias = None if bf is None else np.zeros_like(bf)
+    u, nu = _units(units)
+    rc = _load().oracle_bwd(_ptr(qf), _ptr(kf), _ptr(vf), _ptr(dof), _ptr(qo), _ptr(ko),
+                            len(qo) - 1, heads, head_dim, ACT_CODE[act], float(scale), _ptr(bf),
+                            bias_len, int(bool(causal)), _ptr(u), nu, int(threads),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias))
+    if rc:
+        raise ValueError("oracle_bwd rejected its arguments")
+    return dq, dk, dv, dbias
+
+
+def fwd_inputs(x, units=None, threads: int = 0):
+    """``fwd`` on a ``workloads.Inputs`` bundle."""
+    return fwd(x.q, x.k, x.v, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, x.act, x.scale,
+               bias=x.bias, causal=x.causal, units=units, threads=threads)
+
+
+def bwd_inputs(x, units=None, threads: int = 0):
+    """``bwd`` on a ``workloads.Inputs`` bundle."""
+    return bwd(x.q, x.k, x.v, x.dout, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, x.act,
+               x.scale, bias=x.bias, causal=x.causal, units=units, threads=threads)

@@ -1,0 +1,322 @@
+/*
+ * Plain fp64 CPU oracle for jagged Generalized Dot-Product Attention (GDPA).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library path includes, links or
+ * calls this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no header, helper, table or constant with the
+ * CUDA library: the activation codes below are re-declared here on purpose.
+ *
+ * What it computes (the plain definition, evaluated pair by pair):
+ *
+ *   For every segment b and head h, with Lq = q_off[b+1]-q_off[b] and
+ *   Lkv = kv_off[b+1]-kv_off[b], segment-local indices i < Lq, j < Lkv, and
+ *   valid(i,j) = (j < Lkv) and (not causal or j <= i):
+ *
+ *     x_ij = s * <q_i, k_j> + bias[h][clamp(i-j, -R, R) + R]   (bias optional,
+ *                                                               R = (T-1)/2)
+ *     GELU / SiLU : O_i = sum_{valid j} act(x_ij) v_j           (no normalisation)
+ *     SOFTMAX     : O_i = sum_{valid j} exp(x_ij - LSE_i) v_j,
+ *                   LSE_i = log sum_{valid j} exp(x_ij)
+ *
+ * Sources.  "GEM Training: How Meta Doubled the Efficiency of Its ..." (page
+ * globalainews.in), section "What to watch": the attention modules are two
+ * matrix multiplications with an element-wise activation in between, softmax
+ * replaced by GELU or SiLU; section "What happened": JFA runs flash attention
+ * directly on jagged tensors with custom attention biases, asymmetric
+ * query/key-value lengths and a backward pass.  "Meta redesigns AI training
+ * infrastructure ..." (aiuniverse.news), section "Custom Kernels and 5D
+ * Parallelism ...": GDPA with GELU/SiLU activations.  The pages print no
+ * formula; the readings taken where they are silent are:
+ *   - no 1/L or row-sum normalisation in GELU/SiLU mode;
+ *   - GELU is the exact erf form x*Phi(x);
+ *   - the bias is a per-head table of T = 2R+1 entries indexed by
+ *     clamp(i-j, -R, R)+R with segment-local i, j, added after scaling;
+ *   - the scale multiplies q.k only;
+ *   - causal masking is top-left aligned (j <= i);
+ *   - a row with no valid key gives O_i = 0 (and LSE_i = -inf in softmax mode).
+ *
+ * The backward pass is the analytic gradient of L = sum O * dO:
+ *   dP_ij = <dO_i, v_j>
+ *   GELU / SiLU : dS_ij = dP_ij act'(x_ij),        dV_j += act(x_ij) dO_i
+ *   SOFTMAX     : P_ij = exp(x_ij - LSE_i), D_i = <dO_i, O_i>,
+ *                 dS_ij = P_ij (dP_ij - D_i),       dV_j += P_ij dO_i
+ *   dQ_i += s dS_ij k_j,  dK_j += s dS_ij q_i,  dbias[h][clamp(i-j)+R] += dS_ij
+ *
+ * Layouts: q, out, dout, dq are [total_q][H][d]; k, v, dk, dv are
+ * [total_kv][H][d]; lse is [H][total_q]; bias and dbias are [H][T].
+ * All floating point is double.  OpenMP parallelises over (segment, head)
+ * units only; every unit runs the same sequential loops.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_GELU = 0, ORACLE_SILU = 1, ORACLE_SOFTMAX = 2, ORACLE_IDENTITY = 3 };
+
+/* Standard normal density and distribution function. */
+static double phi_pdf(double x) { return exp(-0.5 * x * x) / sqrt(2.0 * M_PI); }
+static double phi_cdf(double x) { return 0.5 * (1.0 + erf(x / sqrt(2.0))); }
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* act(x) and act'(x) for the element-wise modes (not softmax). */
+static void act_eval(int act, double x, double* y, double* dy) {
+    switch (act) {
+    case ORACLE_GELU: {            /* GELU(x) = x Phi(x), GELU'(x) = Phi(x) + x phi(x) */
+        double c = phi_cdf(x);
+        *y = x * c;
+        *dy = c + x * phi_pdf(x);
+        break;
+    }
+    case ORACLE_SILU: {            /* SiLU(x) = x sigma(x), SiLU' = sigma (1 + x (1 - sigma)) */
+        double sg = sigmoid(x);
+        *y = x * sg;
+        *dy = sg * (1.0 + x * (1.0 - sg));
+        break;
+    }
+    default:                       /* identity: test mode for the associativity check */
+        *y = x;
+        *dy = 1.0;
+        break;
+    }
+}
+
+int oracle_act_eval(int32_t act, const double* x, int64_t n, double* y, double* dy) {
+    if (act != ORACLE_GELU && act != ORACLE_SILU && act != ORACLE_IDENTITY) return 1;
+    for (int64_t t = 0; t < n; ++t) act_eval(act, x[t], &y[t], &dy[t]);
+    return 0;
+}
+
+typedef struct {
+    const double *q, *k, *v, *dout, *bias;
+    const int32_t *q_off, *kv_off;
+    int32_t batch, heads, d, act, bias_len, causal;
+    double scale;
+} problem;
+
+static int valid_pair(const problem* p, int64_t i, int64_t j, int64_t lkv) {
+    if (j >= lkv) return 0;
+    if (p->causal && j > i) return 0;
+    return 1;
+}
+
+/* Index into the bias table of head h for local (i, j). */
+static int64_t bias_index(const problem* p, int64_t i, int64_t j) {
+    int64_t r = (p->bias_len - 1) / 2;
+    int64_t rel = i - j;
+    if (rel < -r) rel = -r;
+    if (rel > r) rel = r;
+    return rel + r;
+}
+
+/* x_ij = s <q_i, k_j> + bias. */
+static double logit(const problem* p, int32_t b, int32_t h, int64_t i, int64_t j) {
+    const int64_t hd = (int64_t)p->heads * p->d;
+    const double* qi = p->q + ((int64_t)p->q_off[b] + i) * hd + (int64_t)h * p->d;
+    const double* kj = p->k + ((int64_t)p->kv_off[b] + j) * hd + (int64_t)h * p->d;
+    double dot = 0.0;
+    for (int32_t c = 0; c < p->d; ++c) dot += qi[c] * kj[c];
+    double x = p->scale * dot;
+    if (p->bias_len > 0) x += p->bias[(int64_t)h * p->bias_len + bias_index(p, i, j)];
+    return x;
+}
+
+/* Forward of one (segment, head) unit: O rows and LSE of that unit. */
+static void fwd_unit(const problem* p, int32_t b, int32_t h, double* out, double* lse,
+                     int64_t total_q) {
+    const int64_t lq = p->q_off[b + 1] - p->q_off[b];
+    const int64_t lkv = p->kv_off[b + 1] - p->kv_off[b];
+    const int64_t hd = (int64_t)p->heads * p->d;
+    double* x = (double*)malloc(sizeof(double) * (size_t)(lkv > 0 ? lkv : 1));
+    for (int64_t i = 0; i < lq; ++i) {
+        double* oi = out + ((int64_t)p->q_off[b] + i) * hd + (int64_t)h * p->d;
+        for (int32_t c = 0; c < p->d; ++c) oi[c] = 0.0;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < lkv; ++j) {
+            if (!valid_pair(p, i, j, lkv)) continue;
+            x[j] = logit(p, b, h, i, j);
+            if (x[j] > m) m = x[j];
+        }
+        double l = 0.0;
+        if (p->act == ORACLE_SOFTMAX) {
+            for (int64_t j = 0; j < lkv; ++j)
+                if (valid_pair(p, i, j, lkv)) l += exp(x[j] - m);
+        }
+        for (int64_t j = 0; j < lkv; ++j) {
+            if (!valid_pair(p, i, j, lkv)) continue;
+            double w, dw;
+            if (p->act == ORACLE_SOFTMAX) w = exp(x[j] - m) / l;
+            else act_eval(p->act, x[j], &w, &dw);
+            const double* vj = p->v + ((int64_t)p->kv_off[b] + j) * hd + (int64_t)h * p->d;
+            for (int32_t c = 0; c < p->d; ++c) oi[c] += w * vj[c];
+        }
+        if (lse) lse[(int64_t)h * total_q + p->q_off[b] + i] = (l > 0.0) ? m + log(l) : -INFINITY;
+    }
+    free(x);
+}
+
+/* Backward of one unit.  dq/dk/dv rows of the unit are overwritten; the
+ * unit's dbias contribution is written to dbias_unit[T] (zeroed here). */
+static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double* dk,
+                     double* dv, double* dbias_unit) {
+    const int64_t lq = p->q_off[b + 1] - p->q_off[b];
+    const int64_t lkv = p->kv_off[b + 1] - p->kv_off[b];
+    const int32_t d = p->d;
+    const int64_t hd = (int64_t)p->heads * d;
+    const int64_t q0 = p->q_off[b], k0 = p->kv_off[b];
+    if (dbias_unit) memset(dbias_unit, 0, sizeof(double) * (size_t)p->bias_len);
+    for (int64_t i = 0; i < lq; ++i) {
+        double* dqi = dq + (q0 + i) * hd + (int64_t)h * d;
+        for (int32_t c = 0; c < d; ++c) dqi[c] = 0.0;
+    }
+    for (int64_t j = 0; j < lkv; ++j) {
+        double* dkj = dk + (k0 + j) * hd + (int64_t)h * d;
+        double* dvj = dv + (k0 + j) * hd + (int64_t)h * d;
+        for (int32_t c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+    }
+    /* Softmax mode needs O_i and LSE_i of this unit: recompute them here. */
+    double* o = NULL;
+    double* lse = NULL;
+    if (p->act == ORACLE_SOFTMAX && lq > 0) {
+        /* A private single-unit problem whose output rows start at 0. */
+        int32_t qoff2[2] = {0, (int32_t)lq};
+        int32_t koff2[2] = {0, (int32_t)lkv};
+        problem sub = *p;
+        sub.q = p->q + q0 * hd;
+        sub.k = p->k + k0 * hd;
+        sub.v = p->v + k0 * hd;
+        sub.q_off = qoff2;
+        sub.kv_off = koff2;
+        sub.batch = 1;
+        o = (double*)calloc((size_t)(lq * hd), sizeof(double));
+        lse = (double*)calloc((size_t)(lq * p->heads), sizeof(double));
+        fwd_unit(&sub, 0, h, o, lse, lq);
+    }
+    for (int64_t i = 0; i < lq; ++i) {
+        const double* qi = p->q + (q0 + i) * hd + (int64_t)h * d;
+        const double* doi = p->dout + (q0 + i) * hd + (int64_t)h * d;
+        double* dqi = dq + (q0 + i) * hd + (int64_t)h * d;
+        double di = 0.0, lse_i = 0.0;
+        if (o) {
+            const double* oi = o + i * hd + (int64_t)h * d;
+            for (int32_t c = 0; c < d; ++c) di += doi[c] * oi[c];
+            lse_i = lse[(int64_t)h * lq + i];
+        }
+        for (int64_t j = 0; j < lkv; ++j) {
+            if (!valid_pair(p, i, j, lkv)) continue;
+            const double* kj = p->k + (k0 + j) * hd + (int64_t)h * d;
+            const double* vj = p->v + (k0 + j) * hd + (int64_t)h * d;
+            double* dkj = dk + (k0 + j) * hd + (int64_t)h * d;
+            double* dvj = dv + (k0 + j) * hd + (int64_t)h * d;
+            double x = logit(p, b, h, i, j);
+            double dp = 0.0;
+            for (int32_t c = 0; c < d; ++c) dp += doi[c] * vj[c];
+            double pij, ds;
+            if (p->act == ORACLE_SOFTMAX) {
+                pij = exp(x - lse_i);
+                ds = pij * (dp - di);
+            } else {
+                double da;
+                act_eval(p->act, x, &pij, &da);
+                ds = dp * da;
+            }
+            for (int32_t c = 0; c < d; ++c) {
+                dvj[c] += pij * doi[c];
+                dqi[c] += p->scale * ds * kj[c];
+                dkj[c] += p->scale * ds * qi[c];
+            }
+            if (dbias_unit) dbias_unit[bias_index(p, i, j)] += ds;
+        }
+    }
+    free(o);
+    free(lse);
+}
+
+static int check_problem(const problem* p) {
+    if (p->batch < 0 || p->heads < 1 || p->d < 1) return 1;
+    if (p->act < ORACLE_GELU || p->act > ORACLE_IDENTITY) return 1;
+    if (p->bias_len < 0 || (p->bias_len > 0 && (p->bias_len % 2) == 0)) return 1;
+    if (p->bias_len > 0 && !p->bias) return 1;
+    if (p->batch > 0 && (p->q_off[0] != 0 || p->kv_off[0] != 0)) return 1;
+    for (int32_t b = 0; b < p->batch; ++b)
+        if (p->q_off[b + 1] < p->q_off[b] || p->kv_off[b + 1] < p->kv_off[b]) return 1;
+    return 0;
+}
+
+static void set_threads(int32_t threads) {
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#else
+    (void)threads;
+#endif
+}
+
+/*
+ * Forward.  units/n_units select (segment, head) units as b*H + h; units ==
+ * NULL means all of them.  Only the selected units' rows of out and lse are
+ * written.  lse may be NULL.  Returns 0, or 1 on invalid arguments.
+ */
+int oracle_fwd(const double* q, const double* k, const double* v,
+               const int32_t* q_off, const int32_t* kv_off, int32_t batch,
+               int32_t heads, int32_t d, int32_t act, double scale,
+               const double* bias, int32_t bias_len, int32_t causal,
+               const int32_t* units, int32_t n_units, int32_t threads,
+               double* out, double* lse) {
+    problem p = {q, k, v, NULL, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, scale};
+    if (check_problem(&p)) return 1;
+    const int64_t total_q = batch > 0 ? q_off[batch] : 0;
+    const int32_t n = units ? n_units : batch * heads;
+    set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t u = 0; u < n; ++u) {
+        int32_t id = units ? units[u] : u;
+        fwd_unit(&p, id / heads, id % heads, out, lse, total_q);
+    }
+    return 0;
+}
+
+/*
+ * Backward.  Overwrites the selected units' rows of dq, dk, dv; dbias (may be
+ * NULL) receives the sum over the selected units, reduced in unit order.
+ */
+int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
+               const int32_t* q_off, const int32_t* kv_off, int32_t batch,
+               int32_t heads, int32_t d, int32_t act, double scale,
+               const double* bias, int32_t bias_len, int32_t causal,
+               const int32_t* units, int32_t n_units, int32_t threads,
+               double* dq, double* dk, double* dv, double* dbias) {
+    problem p = {q, k, v, dout, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, scale};
+    if (check_problem(&p)) return 1;
+    const int32_t n = units ? n_units : batch * heads;
+    const int32_t t = bias_len > 0 ? bias_len : 1;
+    double* part = (dbias && bias_len > 0)
+                       ? (double*)calloc((size_t)n * (size_t)t, sizeof(double)) : NULL;
+    set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t u = 0; u < n; ++u) {
+        int32_t id = units ? units[u] : u;
+        bwd_unit(&p, id / heads, id % heads, dq, dk, dv, part ? part + (int64_t)u * t : NULL);
+    }
+    if (part) {
+        memset(dbias, 0, sizeof(double) * (size_t)heads * (size_t)bias_len);
+        for (int32_t u = 0; u < n; ++u) {
+            int32_t id = units ? units[u] : u;
+            int32_t h = id % heads;
+            for (int32_t e = 0; e < bias_len; ++e)
+                dbias[(int64_t)h * bias_len + e] += part[(int64_t)u * t + e];
+        }
+        free(part);
+    }
+    return 0;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
