@@ -1,0 +1,172 @@
+/*
+ * jgdpa.h - C ABI of libjgdpa.so: jagged Generalized Dot-Product Attention
+ * (GDPA) forward and backward on one GB300 GPU (sm_103a).
+ *
+ * What is computed.  For every segment b and head h, with segment-local query
+ * rows i < Lq_b and key/value rows j < Lkv_b, and valid(i,j) = (not causal or
+ * j <= i):
+ *
+ *     x_ij = scale * <q_i, k_j> + bias[h][clamp(i - j, -R, R) + R]
+ *     GELU / SiLU mode:  O_i = sum_{valid j} act(x_ij) * v_j   (no normalisation)
+ *     SOFTMAX mode:      O_i = sum_{valid j} softmax_j(x_ij) * v_j,
+ *                        LSE_i = log sum_{valid j} exp(x_ij)
+ *
+ * Sources: "GEM Training: How Meta Doubled the Efficiency of Its ..."
+ * (globalainews.in), section "What to watch" -- self-attention, PMA and
+ * cross-attention are two matrix multiplications with an element-wise
+ * activation (GELU or SiLU) in place of softmax, unified in one GDPA kernel;
+ * section "What happened" -- Jagged Flash Attention works directly on jagged
+ * tensors with custom attention biases, asymmetric query/key-value lengths and
+ * a backward pass.  "Meta redesigns AI training infrastructure to solve
+ * trillion-parameter ad recommendation bottlenecks" (aiuniverse.news),
+ * sections "Eliminating Compute Waste in Asymmetric Workloads" and "Custom
+ * Kernels and 5D Parallelism for Trillion-Parameter Scale" -- the jagged
+ * masking, the software tile scheduler and the split-dQ backward.
+ *
+ * The pages print no formula; where they are silent this library reads them
+ * as follows: no normalisation in GELU/SiLU mode; GELU means x*Phi(x) (the
+ * device evaluates an approximation of it); the bias is a per-head table of
+ * bias_len = 2R+1 entries indexed by clamp(i-j, -R, R)+R with segment-local
+ * i, j and is added after scaling; causal masking is top-left aligned
+ * (j <= i); a query row with no valid key gets O_i = 0 (and LSE_i = -inf).
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates and frees nothing and keeps no per-call state.
+ *  - Calls are asynchronous and ordered on `stream`; they return before the
+ *    kernels run.  The stream must belong to the current device.
+ *  - Q, K, V, O and their gradients are bf16, packed "THD": [total][H][d],
+ *    row-major, with no padding between segments.  The base pointers must be
+ *    16-byte aligned.  Segment b owns query rows q_offsets[b] ..
+ *    q_offsets[b+1]-1 and key/value rows kv_offsets[b] .. kv_offsets[b+1]-1.
+ *  - Offsets are int32 [batch+1] device arrays with offsets[0] = 0,
+ *    non-decreasing, and offsets[batch] equal to total_q (total_kv).
+ *  - Outputs are overwritten, never accumulated; rows of segments with no keys
+ *    (or no queries, for dK/dV) are written as zeros.
+ *  - head_dim is 32, 64 or 128; heads >= 1; bias_len is 0 or odd (<= 4095).
+ *  - Errors that the host can see are returned before anything is launched.
+ *    Errors that only the device can see (bad offsets, an internal wait that
+ *    timed out) are recorded in the workspace status word, turn the remaining
+ *    kernels into no-ops, and are read back with jgdpa_read_device_status().
+ *  - `workspace` is caller-owned device scratch of at least
+ *    jgdpa_workspace_bytes(...) bytes, 256-byte aligned; its contents need no
+ *    initialisation and are clobbered by every call.  Two calls that overlap
+ *    in time must not share a workspace.
+ */
+#ifndef JGDPA_H
+#define JGDPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define JGDPA_API __attribute__((visibility("default")))
+#else
+#define JGDPA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* jgdpa_stream_t;  /* a cudaStream_t (NULL = legacy default stream) */
+
+typedef enum {
+    JGDPA_ACT_GELU = 0,     /* act(x) = x * Phi(x) */
+    JGDPA_ACT_SILU = 1,     /* act(x) = x * sigmoid(x) */
+    JGDPA_ACT_SOFTMAX = 2   /* Jagged Flash Attention: softmax over the valid keys */
+} jgdpa_act;
+
+typedef enum {
+    JGDPA_OK = 0,
+    JGDPA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, bad enum, even bias_len */
+    JGDPA_ERR_UNSUPPORTED = 2,        /* head_dim not in {32, 64, 128}, sizes beyond int32 rows */
+    JGDPA_ERR_MISALIGNED = 3,         /* a tensor or the workspace is not suitably aligned */
+    JGDPA_ERR_WORKSPACE_TOO_SMALL = 4,
+    JGDPA_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
+    JGDPA_ERR_BAD_OFFSETS = 6,        /* device-detected: offsets not monotone / wrong ends */
+    JGDPA_ERR_DEVICE_TIMEOUT = 7      /* device-detected: an internal wait gave up */
+} jgdpa_status;
+
+/*
+ * Bytes of device workspace that jgdpa_fwd (for_backward = 0) or jgdpa_bwd
+ * (for_backward = 1) needs for these sizes.  Depends only on the arguments
+ * and on the number of SMs of the current device.  Returns 0 if the arguments
+ * are invalid.
+ */
+JGDPA_API size_t jgdpa_workspace_bytes(int32_t batch, int64_t total_q, int64_t total_kv,
+                             int32_t heads, int32_t head_dim, jgdpa_act act,
+                             int32_t bias_len, int32_t for_backward);
+
+/*
+ * Forward pass.
+ *   q        bf16 [total_q][heads][head_dim]
+ *   k, v     bf16 [total_kv][heads][head_dim]
+ *   scale    the factor s on <q_i, k_j> (typically 1/sqrt(head_dim))
+ *   bias_table  fp32 [heads][bias_len], or NULL with bias_len = 0
+ *   causal   0 or 1 (top-left aligned: key j is visible to query i iff j <= i)
+ *   out      bf16 [total_q][heads][head_dim], written
+ *   lse      fp32 [heads][total_q], natural-log log-sum-exp of each row;
+ *            required in SOFTMAX mode (needed by jgdpa_bwd), must be NULL
+ *            otherwise
+ * Work runs in a persistent kernel over (segment, head, pair of 128-row query
+ * tiles) units ordered longest first by a scheduling kernel (the software tile
+ * scheduler of the GDPA kernel redesign, "Custom Kernels and 5D Parallelism
+ * ...", aiuniverse.news).
+ */
+JGDPA_API jgdpa_status jgdpa_fwd(const void* q, const void* k, const void* v,
+                       const int32_t* q_offsets, const int32_t* kv_offsets,
+                       int32_t batch, int64_t total_q, int64_t total_kv,
+                       int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
+                       const float* bias_table, int32_t bias_len, int32_t causal,
+                       void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, jgdpa_stream_t stream);
+
+/*
+ * Backward pass: gradients of L = sum(O * dout) with respect to q, k, v and
+ * the bias table.
+ *   out, lse   the forward's O and LSE; read in SOFTMAX mode only (may be NULL
+ *              otherwise)
+ *   dout       bf16 [total_q][heads][head_dim]
+ *   dq         bf16 [total_q][heads][head_dim], written
+ *   dk, dv     bf16 [total_kv][heads][head_dim], written
+ *   dbias      fp32 [heads][bias_len], written; NULL to skip (must be NULL
+ *              when bias_table is NULL)
+ * dK/dV come from a KV-major pass and dQ from a separate Q-major pass, so
+ * every output tile has exactly one writer and no atomics touch dQ, dK or dV
+ * (the split-dQ, atomics-free backward of "Eliminating Compute Waste in
+ * Asymmetric Workloads", aiuniverse.news).
+ */
+JGDPA_API jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v,
+                       const void* out, const float* lse, const void* dout,
+                       const int32_t* q_offsets, const int32_t* kv_offsets,
+                       int32_t batch, int64_t total_q, int64_t total_kv,
+                       int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
+                       const float* bias_table, int32_t bias_len, int32_t causal,
+                       void* dq, void* dk, void* dv, float* dbias,
+                       void* workspace, size_t workspace_bytes, jgdpa_stream_t stream);
+
+/*
+ * Reads the device status word of `workspace` (synchronises `stream`) and
+ * returns JGDPA_OK, a device-detected error, or JGDPA_ERR_CUDA.
+ */
+JGDPA_API jgdpa_status jgdpa_read_device_status(const void* workspace, jgdpa_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+JGDPA_API const char* jgdpa_status_string(jgdpa_status s);
+
+/*
+ * Test hook: evaluates the device's own activation functions, exactly as the
+ * forward and backward kernels use them, on n fp32 inputs.  act is GELU or
+ * SiLU; y[i] = act(x[i]) and dy[i] = act'(x[i]) (dy may be NULL).  `path`
+ * selects the evaluation route: 0 = the special-function-unit route (hardware
+ * tanh), 1 = the ALU-only polynomial route.  x, y, dy are device pointers.
+ */
+JGDPA_API jgdpa_status jgdpa_eval_activation(jgdpa_act act, int32_t path, const float* x, int64_t n,
+                                   float* y, float* dy, jgdpa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JGDPA_H */

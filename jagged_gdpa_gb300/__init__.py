@@ -1,0 +1,18 @@
+"""jagged_gdpa_gb300: jagged Generalized Dot-Product Attention on GB300 (sm_103a).
+
+The computation lives in libjgdpa.so (C ABI in include/jgdpa.h, CUDA kernels
+under csrc/).  This package only builds and binds it.
+"""
+
+from ._lib import (  # noqa: F401
+    ACT,
+    EXPORTS,
+    JgdpaError,
+    jgdpa_bwd,
+    jgdpa_eval_activation,
+    jgdpa_fwd,
+    jgdpa_read_device_status,
+    jgdpa_status_string,
+    jgdpa_workspace_bytes,
+    load,
+)

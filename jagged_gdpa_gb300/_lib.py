@@ -1,0 +1,164 @@
+"""ctypes binding of libjgdpa.so (include/jgdpa.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  Tensors are torch tensors on the current CUDA device;
+torch supplies device memory and the stream.  If the library is missing the
+import fails loudly -- there is no fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libjgdpa.so")
+
+ACT = {"gelu": 0, "silu": 1, "softmax": 2}
+STATUS = {
+    0: "JGDPA_OK", 1: "JGDPA_ERR_INVALID_ARGUMENT", 2: "JGDPA_ERR_UNSUPPORTED",
+    3: "JGDPA_ERR_MISALIGNED", 4: "JGDPA_ERR_WORKSPACE_TOO_SMALL", 5: "JGDPA_ERR_CUDA",
+    6: "JGDPA_ERR_BAD_OFFSETS", 7: "JGDPA_ERR_DEVICE_TIMEOUT",
+}
+EXPORTS = ("jgdpa_workspace_bytes", "jgdpa_fwd", "jgdpa_bwd", "jgdpa_read_device_status",
+           "jgdpa_status_string", "jgdpa_eval_activation")
+
+
+class JgdpaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libjgdpa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with jagged_gdpa_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.jgdpa_workspace_bytes.argtypes = [i32, i64, i64, i32, i32, ctypes.c_int, i32, i32]
+    lib.jgdpa_workspace_bytes.restype = sz
+    lib.jgdpa_fwd.argtypes = [P, P, P, P, P, i32, i64, i64, i32, i32, ctypes.c_int, f32, P, i32, i32,
+                              P, P, P, sz, P]
+    lib.jgdpa_fwd.restype = ctypes.c_int
+    lib.jgdpa_bwd.argtypes = [P, P, P, P, P, P, P, P, i32, i64, i64, i32, i32, ctypes.c_int, f32, P, i32,
+                              i32, P, P, P, P, P, sz, P]
+    lib.jgdpa_bwd.restype = ctypes.c_int
+    lib.jgdpa_read_device_status.argtypes = [P, P]
+    lib.jgdpa_read_device_status.restype = ctypes.c_int
+    lib.jgdpa_status_string.argtypes = [ctypes.c_int]
+    lib.jgdpa_status_string.restype = ctypes.c_char_p
+    lib.jgdpa_eval_activation.argtypes = [ctypes.c_int, i32, P, i64, P, P, P]
+    lib.jgdpa_eval_activation.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libjgdpa must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libjgdpa must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise JgdpaError(rc, where)
+
+
+def _act(act) -> int:
+    return ACT[act] if isinstance(act, str) else int(act)
+
+
+def jgdpa_status_string(code: int) -> str:
+    return load().jgdpa_status_string(int(code)).decode()
+
+
+def jgdpa_workspace_bytes(batch: int, total_q: int, total_kv: int, heads: int, head_dim: int, act,
+                          bias_len: int = 0, for_backward: bool = False) -> int:
+    return int(load().jgdpa_workspace_bytes(batch, total_q, total_kv, heads, head_dim, _act(act),
+                                            bias_len, int(bool(for_backward))))
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+    if workspace is not None:
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def jgdpa_fwd(q, k, v, q_offsets, kv_offsets, act, scale: float, bias_table=None, causal: bool = False,
+              out=None, lse=None, workspace=None, stream=None):
+    """Forward pass; returns (out, lse) with lse None unless act == 'softmax'."""
+    lib = load()
+    total_q, heads, d = q.shape
+    total_kv = k.shape[0]
+    batch = q_offsets.numel() - 1
+    a = _act(act)
+    bias_len = 0 if bias_table is None else int(bias_table.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and a == ACT["softmax"]:
+        lse = torch.empty((heads, total_q), dtype=torch.float32, device=q.device)
+    nbytes = jgdpa_workspace_bytes(batch, total_q, total_kv, heads, d, a, bias_len, False)
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.jgdpa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(kv_offsets), batch, total_q,
+                       total_kv, heads, d, a, float(scale), _ptr(bias_table), bias_len, int(bool(causal)),
+                       _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jgdpa_fwd")
+    return out, lse
+
+
+def jgdpa_bwd(q, k, v, out, lse, dout, q_offsets, kv_offsets, act, scale: float, bias_table=None,
+              causal: bool = False, dq=None, dk=None, dv=None, dbias=None, want_dbias: bool = True,
+              workspace=None, stream=None):
+    """Backward pass; returns (dq, dk, dv, dbias) with dbias None without a bias table."""
+    lib = load()
+    total_q, heads, d = q.shape
+    total_kv = k.shape[0]
+    batch = q_offsets.numel() - 1
+    a = _act(act)
+    bias_len = 0 if bias_table is None else int(bias_table.shape[1])
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dbias is None and bias_len and want_dbias:
+        dbias = torch.empty((heads, bias_len), dtype=torch.float32, device=q.device)
+    nbytes = jgdpa_workspace_bytes(batch, total_q, total_kv, heads, d, a, bias_len, True)
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.jgdpa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(q_offsets),
+                       _ptr(kv_offsets), batch, total_q, total_kv, heads, d, a, float(scale),
+                       _ptr(bias_table), bias_len, int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
+                       _ptr(dbias), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jgdpa_bwd")
+    return dq, dk, dv, dbias
+
+
+def jgdpa_read_device_status(workspace, stream=None) -> int:
+    return int(load().jgdpa_read_device_status(_ptr(workspace), _stream(stream)))
+
+
+def jgdpa_eval_activation(act, x, path: int = 0, stream=None):
+    """Device act(x), act'(x) for fp32 x (test hook); path 0 = SFU route, 1 = ALU route."""
+    y = torch.empty_like(x)
+    dy = torch.empty_like(x)
+    rc = load().jgdpa_eval_activation(_act(act), int(path), _ptr(x), x.numel(), _ptr(y), _ptr(dy),
+                                      _stream(stream))
+    _check(rc, "jgdpa_eval_activation")
+    return y, dy

@@ -1,0 +1,157 @@
+// Device activations of the GDPA kernels: GELU and SiLU with their
+// derivatives, by two routes that give the same function up to rounding.
+//
+//  * SFU route: sigmoid(z) = 1/2 + tanh(z/2)/2 with the hardware tanh
+//    (tanh.approx.f32, one special-function-unit op per element).
+//  * ALU route: sigmoid(z) = 1/(1 + 2^(-z log2 e)) with 2^w from a polynomial
+//    after range reduction and 1/a from an integer seed plus two Newton
+//    steps -- FMA/integer pipes only, no special-function unit.
+//
+// The GDPA kernel redesign replaces the activation's special-function-unit
+// work by an ALU-only polynomial to remove SFU contention ("Meta redesigns
+// AI training infrastructure ...", aiuniverse.news, section "Custom Kernels
+// and 5D Parallelism for Trillion-Parameter Scale": a 6th-order Taylor
+// expansion).  The pages give neither the expanded function nor the range
+// reduction; here GELU is evaluated as x * sigmoid(a x + b x^3) and the
+// kernels send a fixed share of each tile through the ALU route and the rest
+// through the SFU route, so that neither pipe is the bottleneck.
+//
+// Constants come from fit_constants.py (next to this file):
+//   a, b      minimise max |x sigmoid(a x + b x^3) - x Phi(x)| on [-16, 16]
+//             (2.71e-4; the classic tanh-form constants give 4.73e-4)
+//   P0..P3    degree-3 minimax fit of 2^f on [-1/2, 1/2] (rel. err 1.1e-4)
+//   kRcpSeed  integer seed for 1/a (rel. err 5.1e-2 before the Newton steps)
+#pragma once
+
+#include <cstdint>
+
+namespace jg {
+
+constexpr float kGeluA = 1.60031416f;
+constexpr float kGeluB = 0.0694017869f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kExpP0 = 0.999941753f;
+constexpr float kExpP1 = 0.693257044f;
+constexpr float kExpP2 = 0.242413568f;
+constexpr float kExpP3 = 0.055092146f;
+constexpr int kRcpSeed = 0x7EF311C2;
+
+__device__ __forceinline__ float tanh_sfu(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^w for w in [-64, 64]: w = n + f with integer n and |f| <= 1/2, 2^f from
+// the polynomial, 2^n added to the exponent field.
+__device__ __forceinline__ float exp2_alu(float w) {
+  const float kRound = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer
+  const float t = __fadd_rn(w, kRound);
+  const float n = __fsub_rn(t, kRound);
+  const float f = __fsub_rn(w, n);
+  float p = __fmaf_rn(kExpP3, f, kExpP2);
+  p = __fmaf_rn(p, f, kExpP1);
+  p = __fmaf_rn(p, f, kExpP0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+// 1/a for a >= 1 (finite): seed by integer subtraction, then two Newton steps.
+__device__ __forceinline__ float rcp_alu(float a) {
+  float y = __int_as_float(kRcpSeed - __float_as_int(a));
+  float e = __fmaf_rn(-a, y, 1.0f);
+  y = __fmaf_rn(y, e, y);
+  e = __fmaf_rn(-a, y, 1.0f);
+  return __fmaf_rn(y, e, y);
+}
+
+// sigmoid(z) and 2^(-z log2 e) by the ALU route; z given as w = -z log2 e.
+__device__ __forceinline__ float sigmoid_alu_w(float w, float& e) {
+  w = fminf(fmaxf(w, -64.0f), 64.0f);
+  e = exp2_alu(w);
+  return rcp_alu(1.0f + e);
+}
+
+// ----------------------------------------------------------------- GELU
+__device__ __forceinline__ float gelu_sfu(float x) {
+  const float x2 = x * x;
+  const float u = x * __fmaf_rn(0.5f * kGeluB, x2, 0.5f * kGeluA);
+  const float t = tanh_sfu(u);
+  const float hx = 0.5f * x;
+  return __fmaf_rn(hx, t, hx);
+}
+__device__ __forceinline__ float gelu_sfu_d(float x, float& dy) {
+  const float x2 = x * x;
+  const float u = x * __fmaf_rn(0.5f * kGeluB, x2, 0.5f * kGeluA);
+  const float t = tanh_sfu(u);
+  const float hx = 0.5f * x;
+  // d/dx [x s(k(x))] = s + x s (1-s) k',  s = (1+t)/2,  s(1-s) = (1-t^2)/4
+  const float q = __fmaf_rn(-t, t, 1.0f);
+  const float s = __fmaf_rn(0.5f, t, 0.5f);
+  const float kp = __fmaf_rn(0.5f * 3.0f * kGeluB, x2, 0.5f * kGeluA);  // k'/2
+  dy = __fmaf_rn(hx * q, kp, s);
+  return __fmaf_rn(hx, t, hx);
+}
+__device__ __forceinline__ float gelu_alu(float x) {
+  const float x2 = x * x;
+  const float w = x * __fmaf_rn(-kGeluB * kLog2e, x2, -kGeluA * kLog2e);
+  float e;
+  const float s = sigmoid_alu_w(w, e);
+  return x * s;
+}
+__device__ __forceinline__ float gelu_alu_d(float x, float& dy) {
+  const float x2 = x * x;
+  const float w = x * __fmaf_rn(-kGeluB * kLog2e, x2, -kGeluA * kLog2e);
+  float e;
+  const float s = sigmoid_alu_w(w, e);
+  // s (1 - s) = e s^2
+  const float kp = __fmaf_rn(3.0f * kGeluB, x2, kGeluA);
+  dy = s * __fmaf_rn(x * e * s, kp, 1.0f);
+  return x * s;
+}
+
+// ----------------------------------------------------------------- SiLU
+__device__ __forceinline__ float silu_sfu(float x) {
+  const float hx = 0.5f * x;
+  const float t = tanh_sfu(hx);
+  return __fmaf_rn(hx, t, hx);
+}
+__device__ __forceinline__ float silu_sfu_d(float x, float& dy) {
+  const float hx = 0.5f * x;
+  const float t = tanh_sfu(hx);
+  // s + x s (1-s) = (1+t)/2 + x (1-t^2)/4
+  const float q = __fmaf_rn(-t, t, 1.0f);
+  const float s = __fmaf_rn(0.5f, t, 0.5f);
+  dy = __fmaf_rn(0.25f * x, q, s);
+  return __fmaf_rn(hx, t, hx);
+}
+__device__ __forceinline__ float silu_alu(float x) {
+  float e;
+  const float s = sigmoid_alu_w(-kLog2e * x, e);
+  return x * s;
+}
+__device__ __forceinline__ float silu_alu_d(float x, float& dy) {
+  float e;
+  const float s = sigmoid_alu_w(-kLog2e * x, e);
+  dy = s * __fmaf_rn(x * e, s, 1.0f);
+  return x * s;
+}
+
+// Dispatch on (act, route) at compile time.  ACT: 0 = GELU, 1 = SiLU.
+template <int ACT, bool ALU>
+__device__ __forceinline__ float act_val(float x) {
+  if constexpr (ACT == 0) return ALU ? gelu_alu(x) : gelu_sfu(x);
+  else return ALU ? silu_alu(x) : silu_sfu(x);
+}
+template <int ACT, bool ALU>
+__device__ __forceinline__ float act_val_d(float x, float& dy) {
+  if constexpr (ACT == 0) return ALU ? gelu_alu_d(x, dy) : gelu_sfu_d(x, dy);
+  else return ALU ? silu_alu_d(x, dy) : silu_sfu_d(x, dy);
+}
+
+}  // namespace jg

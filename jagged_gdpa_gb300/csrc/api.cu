@@ -1,0 +1,387 @@
+// Host side of libjgdpa.so: argument validation, workspace layout, TMA tensor
+// maps and kernel launches behind the C ABI declared in include/jgdpa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/jgdpa.h"
+#include "act.cuh"
+#include "common.cuh"
+
+namespace jg {
+cudaError_t launch_fwd(const FwdParams& p, int head_dim, int act, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_pass(const BwdParams& p, int head_dim, int act, bool kv_major, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_softmax_delta(const void* out, const void* dout, float* delta, int64_t total_q, int heads,
+                                 int head_dim, const int* status, cudaStream_t stream);
+cudaError_t launch_dbias_reduce(const float* part, float* dbias, int n_parts, int n, cudaStream_t stream);
+cudaError_t launch_sched(const SchedParams& p, cudaStream_t stream);
+}  // namespace jg
+
+namespace {
+
+using jg::kTile;
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// ----------------------------------------------------------- device facts
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cache[128] = {0};
+  if (dev < 0 || dev >= 128) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn encode_fn() {
+  static std::once_flag once;
+  static EncodeFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a packed [rows][heads][d] bf16 tensor; box = 128 rows x 1 head
+// x min(d, 64) columns, swizzled to match the MMA operand layout.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int heads, int d) {
+  std::memset(m, 0, sizeof(*m));
+  EncodeFn enc = encode_fn();
+  if (!enc || rows <= 0) return false;
+  const int box_cols = d < 64 ? d : 64;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), 1, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = box_cols * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- workspace
+struct Layout {
+  size_t header = 0;      // status word + unit counters
+  size_t item_base = 0;   // scheduler scratch, 2 lists x (batch + 1)
+  size_t units0 = 0;      // fwd units, or dkdv units
+  size_t units1 = 0;      // dq units (bwd)
+  size_t delta = 0;       // softmax bwd: [H][total_q]
+  size_t dbias = 0;       // bwd with dbias: [grid][H][T]
+  size_t total = 0;
+  int max0 = 0, max1 = 0;
+  int grid = 0;
+};
+
+int64_t max_units(int64_t total, int64_t batch, int rows_per_unit, int heads) {
+  return (total / rows_per_unit + batch) * heads;
+}
+
+bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads, int32_t act, int32_t bias_len,
+                bool bwd, Layout* L) {
+  const int sms = sm_count();
+  if (sms <= 0) return false;
+  int64_t m0, m1 = 0;
+  if (!bwd) {
+    m0 = max_units(total_q, batch, 2 * kTile, heads);
+  } else {
+    m0 = max_units(total_kv, batch, kTile, heads);
+    m1 = max_units(total_q, batch, kTile, heads);
+  }
+  if (m0 > INT32_MAX / 2 || m1 > INT32_MAX / 2) return false;
+  L->max0 = static_cast<int>(m0);
+  L->max1 = static_cast<int>(m1);
+  L->grid = sms;
+  size_t off = 0;
+  L->header = off;
+  off += up(64 * sizeof(int));
+  L->item_base = off;
+  off += up(2 * (static_cast<size_t>(batch) + 1) * sizeof(int32_t));
+  L->units0 = off;
+  off += up(static_cast<size_t>(m0) * sizeof(jg::Unit));
+  L->units1 = off;
+  off += up(static_cast<size_t>(m1) * sizeof(jg::Unit));
+  L->delta = off;
+  if (bwd && act == JGDPA_ACT_SOFTMAX) off += up(static_cast<size_t>(heads) * total_q * sizeof(float));
+  L->dbias = off;
+  if (bwd && bias_len > 0) off += up(static_cast<size_t>(sms) * heads * bias_len * sizeof(float));
+  L->total = off;
+  return true;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+jgdpa_status check_common(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim,
+                          int32_t act, float scale, const float* bias_table, int32_t bias_len, int32_t causal,
+                          const int32_t* q_offsets, const int32_t* kv_offsets) {
+  if (batch < 0 || total_q < 0 || total_kv < 0 || heads < 1) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (act < JGDPA_ACT_GELU || act > JGDPA_ACT_SOFTMAX) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (causal != 0 && causal != 1) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(scale)) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (bias_len < 0 || (bias_len > 0 && (bias_len % 2 == 0 || bias_table == nullptr)) ||
+      (bias_len == 0 && bias_table != nullptr))
+    return JGDPA_ERR_INVALID_ARGUMENT;
+  if (bias_len > jg::kMaxBiasLen) return JGDPA_ERR_UNSUPPORTED;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return JGDPA_ERR_UNSUPPORTED;
+  if (total_q > INT32_MAX || total_kv > INT32_MAX || heads > 65535) return JGDPA_ERR_UNSUPPORTED;
+  if (batch > 0 && (q_offsets == nullptr || kv_offsets == nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (batch == 0 && (total_q != 0 || total_kv != 0)) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_offsets, 4) || !aligned(kv_offsets, 4) || !aligned(bias_table, 4)) return JGDPA_ERR_MISALIGNED;
+  return JGDPA_OK;
+}
+
+#define JG_CUDA(x)                              \
+  do {                                          \
+    if ((x) != cudaSuccess) return JGDPA_ERR_CUDA; \
+  } while (0)
+
+__global__ void fill_f32_kernel(float* p, int64_t n, float v) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = v;
+}
+
+cudaError_t fill_f32(float* p, int64_t n, float v, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  fill_f32_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(p, n, v);
+  return cudaGetLastError();
+}
+
+__global__ void eval_act_kernel(int act, int path, const float* x, int64_t n, float* y, float* dy) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float v = x[i];
+  float a, d;
+  if (act == 0) a = path ? jg::act_val_d<0, true>(v, d) : jg::act_val_d<0, false>(v, d);
+  else a = path ? jg::act_val_d<1, true>(v, d) : jg::act_val_d<1, false>(v, d);
+  y[i] = a;
+  if (dy) dy[i] = d;
+}
+
+jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batch, int32_t heads,
+                          int64_t total_q, int64_t total_kv, int32_t causal, uint8_t* ws, const Layout& L,
+                          bool bwd, cudaStream_t stream) {
+  jg::SchedParams sp{};
+  sp.q_off = q_off;
+  sp.kv_off = kv_off;
+  sp.batch = batch;
+  sp.heads = heads;
+  sp.total_q = total_q;
+  sp.total_kv = total_kv;
+  sp.causal = causal;
+  int* hdr = reinterpret_cast<int*>(ws + L.header);
+  sp.status = hdr;
+  sp.item_base = reinterpret_cast<int32_t*>(ws + L.item_base);
+  sp.list[0].kind = bwd ? jg::kUnitsKv : jg::kUnitsFwd;
+  sp.list[0].max_units = L.max0;
+  sp.list[0].n_units = hdr + 1;
+  sp.list[0].units = reinterpret_cast<jg::Unit*>(ws + L.units0);
+  sp.n_lists = bwd ? 2 : 1;
+  if (bwd) {
+    sp.list[1].kind = jg::kUnitsQ;
+    sp.list[1].max_units = L.max1;
+    sp.list[1].n_units = hdr + 2;
+    sp.list[1].units = reinterpret_cast<jg::Unit*>(ws + L.units1);
+  }
+  JG_CUDA(jg::launch_sched(sp, stream));
+  JG_CUDA(cudaGetLastError());
+  return JGDPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t jgdpa_workspace_bytes(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim,
+                             jgdpa_act act, int32_t bias_len, int32_t for_backward) {
+  if (batch < 0 || total_q < 0 || total_kv < 0 || heads < 1 || bias_len < 0) return 0;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return 0;
+  Layout L;
+  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, for_backward != 0, &L)) return 0;
+  return L.total;
+}
+
+jgdpa_status jgdpa_fwd(const void* q, const void* k, const void* v, const int32_t* q_offsets,
+                       const int32_t* kv_offsets, int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
+                       int32_t head_dim, jgdpa_act act, float scale, const float* bias_table, int32_t bias_len,
+                       int32_t causal, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       jgdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  jgdpa_status st = check_common(batch, total_q, total_kv, heads, head_dim, act, scale, bias_table, bias_len,
+                                 causal, q_offsets, kv_offsets);
+  if (st != JGDPA_OK) return st;
+  if ((act == JGDPA_ACT_SOFTMAX) != (lse != nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (total_q > 0 && (q == nullptr || out == nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (total_kv > 0 && (k == nullptr || v == nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return JGDPA_ERR_MISALIGNED;
+  Layout L;
+  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, false, &L)) return JGDPA_ERR_CUDA;
+  if (workspace == nullptr || workspace_bytes < L.total) return JGDPA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, kAlign)) return JGDPA_ERR_MISALIGNED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  JG_CUDA(cudaMemsetAsync(ws + L.header, 0, 64 * sizeof(int), stream));
+  if (batch == 0 || total_q == 0) return JGDPA_OK;
+  if (total_kv == 0) {  // no keys anywhere: O = 0, LSE = -inf
+    JG_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(total_q) * heads * head_dim * 2, stream));
+    if (lse) JG_CUDA(fill_f32(lse, total_q * heads, -INFINITY, stream));
+    return JGDPA_OK;
+  }
+  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, ws, L, false, stream);
+  if (st != JGDPA_OK) return st;
+
+  jg::FwdParams p{};
+  if (!make_map(&p.tm_q, q, total_q, heads, head_dim) || !make_map(&p.tm_k, k, total_kv, heads, head_dim) ||
+      !make_map(&p.tm_v, v, total_kv, heads, head_dim))
+    return JGDPA_ERR_CUDA;
+  int* hdr = reinterpret_cast<int*>(ws + L.header);
+  p.q_off = q_offsets;
+  p.kv_off = kv_offsets;
+  p.units = reinterpret_cast<const jg::Unit*>(ws + L.units0);
+  p.n_units = hdr + 1;
+  p.status = hdr;
+  p.bias = bias_table;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.total_q = total_q;
+  p.heads = heads;
+  p.bias_len = bias_len;
+  p.causal = causal;
+  p.scale = act == JGDPA_ACT_SOFTMAX ? scale * jg::kLog2e : scale;
+  const int grid = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max0)));
+  JG_CUDA(jg::launch_fwd(p, head_dim, act, grid, stream));
+  return JGDPA_OK;
+}
+
+jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                       const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
+                       int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
+                       float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq, void* dk,
+                       void* dv, float* dbias, void* workspace, size_t workspace_bytes, jgdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  jgdpa_status st = check_common(batch, total_q, total_kv, heads, head_dim, act, scale, bias_table, bias_len,
+                                 causal, q_offsets, kv_offsets);
+  if (st != JGDPA_OK) return st;
+  if (dbias != nullptr && bias_len == 0) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (total_q > 0 && (q == nullptr || dout == nullptr || dq == nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
+  if (total_kv > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr))
+    return JGDPA_ERR_INVALID_ARGUMENT;
+  if (act == JGDPA_ACT_SOFTMAX && total_q > 0 && (out == nullptr || lse == nullptr))
+    return JGDPA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(dbias, 4))
+    return JGDPA_ERR_MISALIGNED;
+  Layout L;
+  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, true, &L)) return JGDPA_ERR_CUDA;
+  if (workspace == nullptr || workspace_bytes < L.total) return JGDPA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, kAlign)) return JGDPA_ERR_MISALIGNED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  JG_CUDA(cudaMemsetAsync(ws + L.header, 0, 64 * sizeof(int), stream));
+  if (dbias) JG_CUDA(cudaMemsetAsync(dbias, 0, static_cast<size_t>(heads) * bias_len * sizeof(float), stream));
+  if (batch == 0) return JGDPA_OK;
+  const size_t row_bytes = static_cast<size_t>(heads) * head_dim * 2;
+  if (total_q == 0 || total_kv == 0) {  // no valid pair anywhere: all gradients are zero
+    if (total_q) JG_CUDA(cudaMemsetAsync(dq, 0, total_q * row_bytes, stream));
+    if (total_kv) {
+      JG_CUDA(cudaMemsetAsync(dk, 0, total_kv * row_bytes, stream));
+      JG_CUDA(cudaMemsetAsync(dv, 0, total_kv * row_bytes, stream));
+    }
+    return JGDPA_OK;
+  }
+  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, ws, L, true, stream);
+  if (st != JGDPA_OK) return st;
+
+  jg::BwdParams p{};
+  if (!make_map(&p.tm_q, q, total_q, heads, head_dim) || !make_map(&p.tm_k, k, total_kv, heads, head_dim) ||
+      !make_map(&p.tm_v, v, total_kv, heads, head_dim) || !make_map(&p.tm_do, dout, total_q, heads, head_dim))
+    return JGDPA_ERR_CUDA;
+  int* hdr = reinterpret_cast<int*>(ws + L.header);
+  p.q_off = q_offsets;
+  p.kv_off = kv_offsets;
+  p.status = hdr;
+  p.bias = bias_table;
+  p.lse = lse;
+  p.delta = act == JGDPA_ACT_SOFTMAX ? reinterpret_cast<float*>(ws + L.delta) : nullptr;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.total_q = total_q;
+  p.heads = heads;
+  p.bias_len = bias_len;
+  p.causal = causal;
+  p.scale = scale;
+  if (act == JGDPA_ACT_SOFTMAX)
+    JG_CUDA(jg::launch_softmax_delta(out, dout, const_cast<float*>(p.delta), total_q, heads, head_dim, hdr,
+                                     stream));
+  const int grid_kv = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max0)));
+  const int grid_q = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max1)));
+  float* part = dbias ? reinterpret_cast<float*>(ws + L.dbias) : nullptr;
+  if (part) JG_CUDA(cudaMemsetAsync(part, 0, static_cast<size_t>(grid_kv) * heads * bias_len * sizeof(float), stream));
+  p.dbias_part = part;
+  p.units = reinterpret_cast<const jg::Unit*>(ws + L.units0);
+  p.n_units = hdr + 1;
+  JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, true, grid_kv, stream));
+  p.dbias_part = nullptr;
+  p.units = reinterpret_cast<const jg::Unit*>(ws + L.units1);
+  p.n_units = hdr + 2;
+  JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
+  if (part) JG_CUDA(jg::launch_dbias_reduce(part, dbias, grid_kv, heads * bias_len, stream));
+  return JGDPA_OK;
+}
+
+jgdpa_status jgdpa_read_device_status(const void* workspace, jgdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (workspace == nullptr) return JGDPA_ERR_INVALID_ARGUMENT;
+  int s = 0;
+  if (cudaMemcpyAsync(&s, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return JGDPA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return JGDPA_ERR_CUDA;
+  return static_cast<jgdpa_status>(s);
+}
+
+const char* jgdpa_status_string(jgdpa_status s) {
+  switch (s) {
+    case JGDPA_OK: return "ok";
+    case JGDPA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case JGDPA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case JGDPA_ERR_MISALIGNED: return "misaligned pointer";
+    case JGDPA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case JGDPA_ERR_CUDA: return "CUDA error";
+    case JGDPA_ERR_BAD_OFFSETS: return "bad offsets (device-detected)";
+    case JGDPA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+jgdpa_status jgdpa_eval_activation(jgdpa_act act, int32_t path, const float* x, int64_t n, float* y, float* dy,
+                                   jgdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if ((act != JGDPA_ACT_GELU && act != JGDPA_ACT_SILU) || (path != 0 && path != 1) || n < 0)
+    return JGDPA_ERR_INVALID_ARGUMENT;
+  if (n == 0) return JGDPA_OK;
+  if (x == nullptr || y == nullptr) return JGDPA_ERR_INVALID_ARGUMENT;
+  eval_act_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(act, path, x, n, y, dy);
+  JG_CUDA(cudaGetLastError());
+  return JGDPA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,124 @@
+// Parameters and small helpers shared by the GDPA kernels and their launcher.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace jg {
+
+constexpr int kTile = 128;          // rows per Q / K / V tile (= MMA M and N)
+constexpr int kMaxBiasLen = 4095;   // largest accepted bias table (2R + 1)
+constexpr int kCostBuckets = 4096;  // scheduler's counting-sort buckets
+
+// Kinds of work lists built by the scheduler.
+enum UnitKind : int {
+  kUnitsFwd = 0,   // (segment, head, pair of 128-row query tiles)
+  kUnitsKv = 1,    // (segment, head, 128-row key/value tile): dK, dV
+  kUnitsQ = 2,     // (segment, head, 128-row query tile): dQ
+};
+
+// One work unit: x = segment, y = head, z = tile (or tile pair) index, w = cost.
+using Unit = int4;
+
+struct SchedList {
+  int kind;
+  int max_units;
+  int* n_units;   // device counter written by the scheduler
+  Unit* units;    // device list, longest first
+};
+
+struct SchedParams {
+  const int32_t* q_off;
+  const int32_t* kv_off;
+  int32_t batch;
+  int32_t heads;
+  int64_t total_q;
+  int64_t total_kv;
+  int32_t causal;
+  int* status;
+  int32_t* item_base;   // scratch [batch + 1] per list
+  SchedList list[2];
+  int n_lists;
+};
+
+// Lengths and tile counts of one segment.
+struct Seg {
+  int q0, lq, k0, lkv;
+};
+
+__device__ __forceinline__ Seg load_seg(const int32_t* q_off, const int32_t* kv_off, int b) {
+  Seg s;
+  s.q0 = __ldg(q_off + b);
+  s.lq = __ldg(q_off + b + 1) - s.q0;
+  s.k0 = __ldg(kv_off + b);
+  s.lkv = __ldg(kv_off + b + 1) - s.k0;
+  return s;
+}
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Number of key/value tiles that query tile t (128 rows) must visit.  With
+// top-left causal masking, query row i sees keys j <= i, so tile t needs kv
+// tiles 0..t.
+__device__ __forceinline__ int kv_tiles_for_q_tile(int t, int lkv, int causal) {
+  const int n = ceil_div(lkv, kTile);
+  return causal ? min(t + 1, n) : n;
+}
+// Number of query tiles that key/value tile kt meets (same masking rule).
+__device__ __forceinline__ int q_tiles_for_kv_tile(int kt, int lq, int causal) {
+  const int n = ceil_div(lq, kTile);
+  return causal ? max(0, n - kt) : n;
+}
+__device__ __forceinline__ int first_q_tile_for_kv_tile(int kt, int causal) { return causal ? kt : 0; }
+
+// Index of the i-th unit processed by CTA c of G (serpentine over rounds, so
+// that each round's longest units are spread evenly).
+__device__ __forceinline__ int unit_index(int round, int c, int g) {
+  return round * g + ((round & 1) ? (g - 1 - c) : c);
+}
+
+struct FwdParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  const int32_t* q_off;
+  const int32_t* kv_off;
+  const Unit* units;
+  const int* n_units;
+  int* status;
+  const float* bias;      // [H][bias_len] or nullptr
+  __nv_bfloat16* out;     // [total_q][H][D]
+  float* lse;             // [H][total_q] (softmax) or nullptr
+  int64_t total_q;
+  int32_t heads;
+  int32_t bias_len;
+  int32_t causal;
+  float scale;            // s (GELU/SiLU) or s * log2(e) (softmax)
+};
+
+struct BwdParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const int32_t* q_off;
+  const int32_t* kv_off;
+  const Unit* units;
+  const int* n_units;
+  int* status;
+  const float* bias;       // [H][bias_len] or nullptr
+  const float* lse;        // [H][total_q] (softmax)
+  const float* delta;      // [H][total_q] rowsum(dO * O) (softmax)
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* dbias_part;       // [gridDim.x][H][bias_len] per-CTA partial sums, or nullptr
+  int64_t total_q;
+  int32_t heads;
+  int32_t bias_len;
+  int32_t causal;
+  float scale;             // s
+};
+
+}  // namespace jg

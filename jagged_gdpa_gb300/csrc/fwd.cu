@@ -1,0 +1,531 @@
+// Forward jagged GDPA kernel for sm_103a.
+//
+// A persistent CTA (one per SM) walks the scheduler's unit list.  A unit is a
+// (segment b, head h, pair of 128-row query tiles); the two query tiles share
+// every key/value tile of the segment.  Warp roles:
+//   warp 0      TMA producer: Q tiles into two slots, K/V tiles into a ring
+//   warp 1      MMA issuer (one thread): S = Q K^T and O += P V with tcgen05,
+//               accumulators in Tensor Memory; also owns the TMEM allocation
+//   warps 4-7   activation warpgroup of query slot 0
+//   warps 8-11  activation warpgroup of query slot 1
+// The two slots ping-pong: while one warpgroup turns S into P the tensor core
+// works on the other slot, so activation and MMA overlap.
+//
+// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D),
+// O1 [256+D, 256+2D).  P (bf16) is written over the first 64 columns of its
+// S and consumed from TMEM by the second MMA.
+//
+// GELU/SiLU mode has no normalisation and no online rescaling: O accumulates
+// in TMEM over every key/value tile and is stored once (the "softmax
+// correction stage elimination" of the GDPA redesign, aiuniverse.news,
+// section "Custom Kernels and 5D Parallelism ...").  Softmax mode (Jagged
+// Flash Attention) keeps a running row maximum in base 2 and rescales O in
+// TMEM only when the maximum grows by more than 2^8.
+//
+// Masking follows the jagged "subtraction scheme" ("Eliminating Compute Waste
+// in Asymmetric Workloads", aiuniverse.news): per tile and row the number of
+// valid columns n = min(Lkv - j0, causal ? i - j0 + 1 : 128) is computed once,
+// and only tiles where n < 128 compare column indices against it.
+#include "act.cuh"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace jg {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kBlockCols = D < 64 ? D : 64;      // bf16 columns per swizzle row
+  static constexpr int kRowBytes = kBlockCols * 2;        // 64 or 128 bytes
+  static constexpr int kBlockBytes = kTile * kRowBytes;   // one column block of a tile
+  static constexpr int kNumBlocks = D / kBlockCols;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr uint32_t kSwizzle = kRowBytes == 128 ? 2u : 4u;  // 128-byte / 64-byte
+  static constexpr int kSBO = 8 * kRowBytes;              // stride between 8-row groups
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+  static constexpr int kTmemCols = 512;
+};
+
+struct FwdBars {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t drain;
+  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Per-unit geometry shared by every role.
+struct FwdUnit {
+  int b, h, pair;
+  Seg seg;
+  int nkv_s[2];   // key/value tiles for each query slot (0 = slot idle)
+  int rows_s[2];  // valid query rows in each slot's tile (<= 0: no tile)
+  int nkv;        // max of nkv_s
+};
+
+__device__ __forceinline__ FwdUnit fwd_unit(const FwdParams& p, int idx) {
+  FwdUnit u;
+  const Unit w = p.units[idx];
+  u.b = w.x;
+  u.h = w.y;
+  u.pair = w.z;
+  u.seg = load_seg(p.q_off, p.kv_off, u.b);
+  u.nkv = 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int t = 2 * u.pair + s;
+    u.rows_s[s] = u.seg.lq - t * kTile;
+    u.nkv_s[s] = u.rows_s[s] > 0 ? kv_tiles_for_q_tile(t, u.seg.lkv, p.causal) : 0;
+    u.nkv = max(u.nkv, u.nkv_s[s]);
+  }
+  return u;
+}
+
+// --------------------------------------------------------------- producer
+template <int D>
+__device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, int n_units, Fail fail) {
+  using C = FwdCfg<D>;
+  uint32_t q_it[2] = {0, 0};
+  uint32_t kv_it = 0;
+  bool ok = true;
+  for (int r = 0;; ++r) {
+    const int idx = unit_index(r, blockIdx.x, gridDim.x);
+    if (idx >= n_units) break;
+    const FwdUnit u = fwd_unit(p, idx);
+    if (u.nkv == 0) continue;
+    for (int s = 0; s < 2 && ok; ++s) {
+      if (u.nkv_s[s] == 0) continue;
+      ok = mbar_wait(&bars->q_empty[s], (q_it[s] & 1) ^ 1, fail);
+      if (!ok) break;
+      mbar_arrive_tx(&bars->q_full[s], C::kTileBytes);
+      uint8_t* dst = smem + C::kQOff + s * C::kTileBytes;
+      const int row = u.seg.q0 + (2 * u.pair + s) * kTile;
+#pragma unroll
+      for (int cb = 0; cb < C::kNumBlocks; ++cb)
+        tma_load_3d(dst + cb * C::kBlockBytes, &p.tm_q, &bars->q_full[s], cb * C::kBlockCols, u.h, row);
+      ++q_it[s];
+    }
+    for (int kt = 0; kt < u.nkv && ok; ++kt) {
+      const int st = kv_it % C::kStages;
+      ok = mbar_wait(&bars->kv_empty[st], ((kv_it / C::kStages) & 1) ^ 1, fail);
+      if (!ok) break;
+      const int row = u.seg.k0 + kt * kTile;
+      mbar_arrive_tx(&bars->k_full[st], C::kTileBytes);
+      uint8_t* kd = smem + C::kKOff + st * C::kTileBytes;
+#pragma unroll
+      for (int cb = 0; cb < C::kNumBlocks; ++cb)
+        tma_load_3d(kd + cb * C::kBlockBytes, &p.tm_k, &bars->k_full[st], cb * C::kBlockCols, u.h, row);
+      mbar_arrive_tx(&bars->v_full[st], C::kTileBytes);
+      uint8_t* vd = smem + C::kVOff + st * C::kTileBytes;
+#pragma unroll
+      for (int cb = 0; cb < C::kNumBlocks; ++cb)
+        tma_load_3d(vd + cb * C::kBlockBytes, &p.tm_v, &bars->v_full[st], cb * C::kBlockCols, u.h, row);
+      ++kv_it;
+    }
+    if (!ok) break;
+  }
+  if (!ok) {
+    // Let copies already issued land before the CTA exits.
+    for (int s = 0; s < 2; ++s)
+      if (q_it[s]) mbar_wait_drain(&bars->q_full[s], (q_it[s] - 1) & 1);
+    for (uint32_t i = kv_it > C::kStages ? kv_it - C::kStages : 0; i < kv_it; ++i) {
+      mbar_wait_drain(&bars->k_full[i % C::kStages], (i / C::kStages) & 1);
+      mbar_wait_drain(&bars->v_full[i % C::kStages], (i / C::kStages) & 1);
+    }
+  }
+}
+
+// ------------------------------------------------------------- MMA issuer
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+  using C = FwdCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(kTile, kTile, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk * 16 / C::kBlockCols) * C::kBlockBytes + (kk * 16 % C::kBlockCols) * 2;
+    const uint64_t a = sdesc(q_addr + off, 16, C::kSBO, C::kSwizzle);
+    const uint64_t b = sdesc(k_addr + off, 16, C::kSBO, C::kSwizzle);
+    mma_ss(tmem_s, a, b, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate) {
+  using C = FwdCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(kTile, D, 0, 1);  // B (= V) is MN-major
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk) {
+    const uint64_t b = sdesc(v_addr + kk * 16 * C::kRowBytes, C::kBlockBytes, C::kSBO, C::kSwizzle);
+    mma_ts(tmem_o, tmem_p + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem, int n_units, Fail fail) {
+  using C = FwdCfg<D>;
+  const uint32_t q_addr[2] = {smem_u32(smem + C::kQOff), smem_u32(smem + C::kQOff + C::kTileBytes)};
+  const uint32_t k_base = smem_u32(smem + C::kKOff);
+  const uint32_t v_base = smem_u32(smem + C::kVOff);
+  const uint32_t t_s[2] = {tmem, tmem + 128};
+  const uint32_t t_o[2] = {tmem + 256, tmem + 256 + D};
+  uint32_t q_it[2] = {0, 0}, p_it[2] = {0, 0}, o_it[2] = {0, 0};
+  uint32_t kv_it = 0;
+  bool ok = true;
+
+  for (int r = 0; ok; ++r) {
+    const int idx = unit_index(r, blockIdx.x, gridDim.x);
+    if (idx >= n_units) break;
+    const FwdUnit u = fwd_unit(p, idx);
+    if (u.nkv == 0) continue;
+    for (int s = 0; s < 2 && ok; ++s) {
+      if (u.nkv_s[s] == 0) continue;
+      ok = mbar_wait(&bars->q_full[s], q_it[s] & 1, fail);
+      ++q_it[s];
+    }
+    if (!ok) break;
+    // S(0) for both slots
+    {
+      const int st = kv_it % C::kStages;
+      if (!(ok = mbar_wait(&bars->k_full[st], (kv_it / C::kStages) & 1, fail))) break;
+      tc_fence_after();
+      for (int s = 0; s < 2; ++s) {
+        if (u.nkv_s[s] == 0) continue;
+        issue_qk<D>(t_s[s], q_addr[s], k_base + st * C::kTileBytes);
+        mma_commit(&bars->s_full[s]);
+        if (u.nkv_s[s] == 1) mma_commit(&bars->q_empty[s]);
+      }
+    }
+    for (int kt = 0; kt < u.nkv && ok; ++kt) {
+      const uint32_t it = kv_it + kt;
+      const int st = it % C::kStages;
+      const uint32_t v_addr = v_base + st * C::kTileBytes;
+      if (!(ok = mbar_wait(&bars->v_full[st], (it / C::kStages) & 1, fail))) break;
+      const bool more = kt + 1 < u.nkv;
+      const int st1 = (it + 1) % C::kStages;
+      // slot 0: O0 += P0 V, then S0 of the next tile
+      if (kt < u.nkv_s[0]) {
+        if (kt == 0) {
+          if (!(ok = mbar_wait(&bars->o_empty[0], (o_it[0] & 1) ^ 1, fail))) break;
+          ++o_it[0];
+        }
+        if (!(ok = mbar_wait(&bars->p_full[0], p_it[0] & 1, fail))) break;
+        ++p_it[0];
+        tc_fence_after();
+        issue_pv<D>(t_o[0], t_s[0], v_addr, kt > 0);
+        if (kt == u.nkv_s[0] - 1) mma_commit(&bars->o_full[0]);
+      }
+      if (more) {
+        if (!(ok = mbar_wait(&bars->k_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
+        tc_fence_after();
+        if (kt + 1 < u.nkv_s[0]) {
+          issue_qk<D>(t_s[0], q_addr[0], k_base + st1 * C::kTileBytes);
+          mma_commit(&bars->s_full[0]);
+          if (kt + 1 == u.nkv_s[0] - 1) mma_commit(&bars->q_empty[0]);
+        }
+      }
+      // slot 1: O1 += P1 V, release the stage, then S1 of the next tile
+      if (kt < u.nkv_s[1]) {
+        if (kt == 0) {
+          if (!(ok = mbar_wait(&bars->o_empty[1], (o_it[1] & 1) ^ 1, fail))) break;
+          ++o_it[1];
+        }
+        if (!(ok = mbar_wait(&bars->p_full[1], p_it[1] & 1, fail))) break;
+        ++p_it[1];
+        tc_fence_after();
+        issue_pv<D>(t_o[1], t_s[1], v_addr, kt > 0);
+        if (kt == u.nkv_s[1] - 1) mma_commit(&bars->o_full[1]);
+      }
+      mma_commit(&bars->kv_empty[st]);
+      if (more && kt + 1 < u.nkv_s[1]) {
+        issue_qk<D>(t_s[1], q_addr[1], k_base + st1 * C::kTileBytes);
+        mma_commit(&bars->s_full[1]);
+        if (kt + 1 == u.nkv_s[1] - 1) mma_commit(&bars->q_empty[1]);
+      }
+    }
+    kv_it += u.nkv;
+  }
+  // Make sure every MMA issued so far has finished before TMEM is released.
+  mma_commit(&bars->drain);
+  mbar_wait_drain(&bars->drain, 0);
+}
+
+// ------------------------------------------------------ activation warps
+// Bias of one element: table index clamp(rel, -R, R) + R = clamp(base - c, 0, 2R)
+// with base = i - j0 + R for the thread's row i and the tile's first key j0.
+struct BiasTile {
+  int mode;      // 0 none, 1 constant, 2 per element
+  float value;   // mode 1
+  int base;      // mode 2
+  int top;       // 2R
+  const float* row;  // this head's table
+};
+
+__device__ __forceinline__ BiasTile bias_tile(const FwdParams& p, int h, int i0, int r, int j0) {
+  BiasTile t;
+  t.mode = 0;
+  t.value = 0.f;
+  t.base = 0;
+  t.top = p.bias_len - 1;
+  t.row = nullptr;
+  if (p.bias_len == 0) return t;
+  const int R = (p.bias_len - 1) / 2;
+  const int delta = i0 - j0;  // rel = delta + r - c, r, c in [0, 128)
+  t.row = p.bias + static_cast<int64_t>(h) * p.bias_len;
+  if (delta - (kTile - 1) >= R) {
+    t.mode = 1;
+    t.value = __ldg(t.row + 2 * R);
+  } else if (delta + (kTile - 1) <= -R) {
+    t.mode = 1;
+    t.value = __ldg(t.row);
+  } else {
+    t.mode = 2;
+    t.base = delta + r + R;
+  }
+  return t;
+}
+
+__device__ __forceinline__ float bias_at(const BiasTile& t, int c) {
+  if (t.mode == 0) return 0.f;
+  if (t.mode == 1) return t.value;
+  return ld_nc_f32(t.row + min(max(t.base - c, 0), t.top));
+}
+
+template <int D, int ACT>
+__device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int slot, int n_units, Fail fail) {
+  constexpr bool kSoftmax = ACT == 2;
+  const int warp = threadIdx.x >> 5;
+  const int quad = warp & 3;
+  const int r = quad * 32 + (threadIdx.x & 31);  // row of the tile owned by this thread
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t t_s = tmem + lane_off + 128 * slot;
+  const uint32_t t_o = tmem + lane_off + 256 + D * slot;
+  uint32_t s_it = 0, o_it = 0;
+  const int H = p.heads;
+
+  for (int rr = 0;; ++rr) {
+    const int idx = unit_index(rr, blockIdx.x, gridDim.x);
+    if (idx >= n_units) break;
+    const FwdUnit u = fwd_unit(p, idx);
+    const int rows = u.rows_s[slot];
+    if (rows <= 0) continue;
+    const int t = 2 * u.pair + slot;
+    const bool row_ok = r < rows;
+    const int64_t grow = static_cast<int64_t>(u.seg.q0) + t * kTile + r;
+    __nv_bfloat16* out_row = p.out + (grow * H + u.h) * D;
+    const int nkv = u.nkv_s[slot];
+    if (nkv == 0) {  // no keys: O = 0, LSE = -inf
+      if (row_ok) {
+#pragma unroll
+        for (int c = 0; c < D; c += 8) st_global_v4(out_row + c, 0u, 0u, 0u, 0u);
+        if (kSoftmax && p.lse) p.lse[static_cast<int64_t>(u.h) * p.total_q + grow] = -INFINITY;
+      }
+      continue;
+    }
+    float m_run = -INFINITY, l_run = 0.f;  // softmax state (base 2)
+    bool ok = true;
+    for (int kt = 0; kt < nkv; ++kt) {
+      if (!(ok = mbar_wait(&bars->s_full[slot], s_it & 1, fail))) break;
+      ++s_it;
+      tc_fence_after();
+      const int j0 = kt * kTile;
+      int nvalid = min(kTile, u.seg.lkv - j0);
+      if (p.causal) nvalid = min(nvalid, t * kTile + r - j0 + 1);
+      const bool tile_masked = (u.seg.lkv - j0 < kTile) || (p.causal && kt == t);
+      const BiasTile bt = bias_tile(p, u.h, t * kTile, r, j0);
+
+      if constexpr (!kSoftmax) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t a[32], b[32];
+          tmem_ld32(t_s + half * 64, a);
+          tmem_ld32(t_s + half * 64 + 32, b);
+          tmem_ld_wait2(a, b);
+          uint32_t pk[32];
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2) {
+            float v2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int cl = 2 * c2 + e;  // column within the half
+              const int c = half * 64 + cl;
+              const uint32_t raw = cl < 32 ? a[cl] : b[cl - 32];
+              float x = __fmaf_rn(__uint_as_float(raw), p.scale, bias_at(bt, c));
+              if (tile_masked && c >= nvalid) x = 0.f;  // act(0) = 0
+              // one chunk of 32 columns out of four goes through the ALU route
+              v2[e] = (half == 1 && cl >= 32) ? act_val<ACT, true>(x) : act_val<ACT, false>(x);
+            }
+            pk[c2] = pack_bf16(v2[0], v2[1]);
+          }
+          tmem_st32(t_s + half * 32, pk);
+        }
+      } else {
+        uint32_t a[32], b[32], c3[32], d4[32];
+        tmem_ld32(t_s, a);
+        tmem_ld32(t_s + 32, b);
+        tmem_ld_wait2(a, b);
+        tmem_ld32(t_s + 64, c3);
+        tmem_ld32(t_s + 96, d4);
+        tmem_ld_wait2(c3, d4);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          uint32_t& raw = c < 32 ? a[c] : c < 64 ? b[c - 32] : c < 96 ? c3[c - 64] : d4[c - 96];
+          float x = __fmaf_rn(__uint_as_float(raw), p.scale, kLog2e * bias_at(bt, c));
+          if (tile_masked && c >= nvalid) x = -INFINITY;
+          raw = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+        // Rescale only when the maximum grows by more than 8 (a factor 256).
+        const bool grow_max = mx > m_run + 8.0f;
+        const float m_new = grow_max ? mx : m_run;
+        const float factor = grow_max ? ex2_sfu(m_run - m_new) : 1.0f;  // ex2(-inf) = 0 on the first tile
+        l_run *= factor;
+        m_run = m_new;
+        float lsum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t(&src)[32] = q == 0 ? a : q == 1 ? b : q == 2 ? c3 : d4;
+          uint32_t pk[16];
+#pragma unroll
+          for (int c2 = 0; c2 < 16; ++c2) {
+            const float p0 = ex2_sfu(__uint_as_float(src[2 * c2]) - m_run);
+            const float p1 = ex2_sfu(__uint_as_float(src[2 * c2 + 1]) - m_run);
+            lsum += p0 + p1;
+            pk[c2] = pack_bf16(p0, p1);
+          }
+          tmem_st16(t_s + 16 * q, pk);  // P columns [16q, 16q+16) lie in S columns already read
+        }
+        l_run += lsum;
+        // O holds every earlier tile's P V (complete: it was issued before this
+        // tile's S), so it can be rescaled in place before P is released.
+        if (kt > 0 && __any_sync(0xffffffffu, grow_max)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c0, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+            tmem_st32(t_o + c0, o);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[slot]);
+    }
+    if (!ok) break;
+    // epilogue: O (TMEM) -> bf16 -> global, rows < Lq only
+    if (!mbar_wait(&bars->o_full[slot], o_it & 1, fail)) break;
+    ++o_it;
+    tc_fence_after();
+    const float inv_l = kSoftmax ? 1.0f / l_run : 1.0f;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t o[32];
+      tmem_ld32(t_o + c0, o);
+      tmem_ld_wait(o);
+      if (row_ok) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * inv_l, __uint_as_float(o[c + 2 * e + 1]) * inv_l);
+          st_global_v4(out_row + c0 + c, w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&bars->o_empty[slot]);
+    if (kSoftmax && row_ok && p.lse)
+      p.lse[static_cast<int64_t>(u.h) * p.total_q + grow] = (m_run + __log2f(l_run)) * kLn2;
+  }
+}
+
+// ----------------------------------------------------------------- kernel
+template <int D, int ACT>
+__global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::kBarOff);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->o_full[s], 1);
+      mbar_init(&bars->o_empty[s], 128);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int n_units = *p.n_units;
+  if (*reinterpret_cast<volatile int*>(p.status) != kOk) n_units = 0;
+  Fail fail{&bars->abort, p.status};
+
+  if (warp == 0) {
+    if (lane == 0) fwd_producer<D>(p, smem, bars, n_units, fail);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) fwd_mma<D>(p, smem, bars, tmem, n_units, fail);
+    __syncwarp();
+  } else if (warp >= 4) {
+    fwd_act<D, ACT>(p, bars, tmem, (warp - 4) >> 2, n_units, fail);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ launch
+template <int D, int ACT>
+static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = gdpa_fwd_kernel<D, ACT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 384, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int head_dim, int act, int grid, cudaStream_t stream) {
+#define JG_FWD_CASE(DD)                                              \
+  if (head_dim == DD) {                                              \
+    if (act == 0) return launch_fwd_t<DD, 0>(p, grid, stream);       \
+    if (act == 1) return launch_fwd_t<DD, 1>(p, grid, stream);       \
+    return launch_fwd_t<DD, 2>(p, grid, stream);                     \
+  }
+  JG_FWD_CASE(128)
+  JG_FWD_CASE(64)
+  JG_FWD_CASE(32)
+#undef JG_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace jg

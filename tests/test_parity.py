@@ -1,0 +1,140 @@
+"""GPU parity: libjgdpa.so (through the C ABI) against the fp64 CPU oracle.
+
+Bar (per output tensor): max|gpu - oracle| <= 2e-2 * max|oracle|; offsets
+and lengths are integers and must be reproduced exactly.  Small cases run the
+oracle on everything; the five named workloads run at full size on the GPU
+and the oracle recomputes a sample of (segment, head) units, whose rows are
+compared (each unit is independent of the others).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests._util import assert_close, oracle_bwd, oracle_fwd, sample_units, unit_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def jg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import jagged_gdpa_gb300 as m
+    return m
+
+
+def run_fwd(jg, x):
+    d = x.to("cuda")
+    out, lse = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale,
+                            bias_table=d.bias, causal=x.causal)
+    torch.cuda.synchronize()
+    return out.cpu(), (None if lse is None else lse.cpu())
+
+
+def run_bwd(jg, x, out=None, lse=None):
+    d = x.to("cuda")
+    if x.act == "softmax":
+        out, lse = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale,
+                                bias_table=d.bias, causal=x.causal)
+    dq, dk, dv, db = jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act,
+                                  x.scale, bias_table=d.bias, causal=x.causal)
+    torch.cuda.synchronize()
+    return dq.cpu(), dk.cpu(), dv.cpu(), (None if db is None else db.cpu())
+
+
+def check_fwd_full(jg, x, tag=""):
+    out, lse = run_fwd(jg, x)
+    ref, rlse = oracle_fwd(x)
+    assert_close(f"O {tag}", out, ref)
+    if x.act == "softmax":
+        valid = np.isfinite(rlse)
+        assert np.array_equal(np.isfinite(lse.numpy()), valid), f"LSE -inf pattern {tag}"
+        assert_close(f"LSE {tag}", lse.numpy()[valid], rlse[valid])
+
+
+def check_bwd_full(jg, x, tag=""):
+    dq, dk, dv, db = run_bwd(jg, x)
+    rq, rk, rv, rb = oracle_bwd(x)
+    assert_close(f"dQ {tag}", dq, rq)
+    assert_close(f"dK {tag}", dk, rk)
+    assert_close(f"dV {tag}", dv, rv)
+    if rb is not None:
+        assert_close(f"dbias {tag}", db, rb)
+
+
+# ---------------------------------------------------------------- small cases
+SMALL = []
+for d in (32, 64, 128):
+    for act in ("gelu", "silu", "softmax"):
+        for bias_len in (0, 257):
+            for causal in (False, True):
+                SMALL.append((d, act, bias_len, causal))
+
+
+@pytest.mark.parametrize("d,act,bias_len,causal", SMALL)
+def test_forward_small(jg, d, act, bias_len, causal):
+    # several tiles and ragged tails: lengths up to ~3 tiles, some empty segments
+    x = workloads.random_case(1000 + d + bias_len + int(causal), batch=5, heads=2, head_dim=d, act=act,
+                              lq_range=(1, 300), lkv_range=(1, 300), causal=causal, bias_len=bias_len)
+    check_fwd_full(jg, x, f"d={d} {act} bias={bias_len} causal={causal}")
+
+
+@pytest.mark.parametrize("d,act,bias_len,causal", SMALL)
+def test_backward_small(jg, d, act, bias_len, causal):
+    x = workloads.random_case(2000 + d + bias_len + int(causal), batch=4, heads=2, head_dim=d, act=act,
+                              lq_range=(1, 300), lkv_range=(1, 300), causal=causal, bias_len=bias_len)
+    check_bwd_full(jg, x, f"d={d} {act} bias={bias_len} causal={causal}")
+
+
+@pytest.mark.parametrize("act", ["gelu", "softmax"])
+def test_edge_lengths(jg, act):
+    """Empty segments, length 1, multiples of 128 and +-1 around them."""
+    lq = [0, 1, 127, 128, 129, 255, 256, 257, 3, 0, 384]
+    lkv = [5, 1, 128, 127, 129, 256, 0, 257, 0, 7, 385]
+    rng = np.random.default_rng(9)
+    x = workloads.make_inputs(lq, lkv, 3, 64, act, causal=False, bias_len=7, rng=rng)
+    check_fwd_full(jg, x, "edge fwd")
+    check_bwd_full(jg, x, "edge bwd")
+    x = workloads.make_inputs(lq, lkv, 3, 64, act, causal=True, bias_len=0, rng=rng)
+    check_fwd_full(jg, x, "edge fwd causal")
+    check_bwd_full(jg, x, "edge bwd causal")
+
+
+def test_workload_1_tiny_full(jg):
+    x = workloads.workload_inputs(1)
+    check_fwd_full(jg, x, "w1")
+    check_bwd_full(jg, x, "w1")
+
+
+# ------------------------------------------------------ full-size workloads
+def check_sampled(jg, x, units_fwd, units_bwd, tag):
+    out, lse = run_fwd(jg, x)
+    ref, rlse = oracle_fwd(x, units=units_fwd)
+    rows, heads = unit_rows(x, units_fwd, "q")
+    assert_close(f"O {tag}", out.float().numpy()[rows, heads], ref[rows, heads])
+    if x.act == "softmax":
+        assert_close(f"LSE {tag}", lse.numpy()[heads, rows], rlse[heads, rows])
+    dq, dk, dv, db = run_bwd(jg, x)
+    rq, rk, rv, _ = oracle_bwd(x, units=units_bwd)
+    rows, heads = unit_rows(x, units_bwd, "q")
+    assert_close(f"dQ {tag}", dq.float().numpy()[rows, heads], rq[rows, heads])
+    rows, heads = unit_rows(x, units_bwd, "kv")
+    assert_close(f"dK {tag}", dk.float().numpy()[rows, heads], rk[rows, heads])
+    assert_close(f"dV {tag}", dv.float().numpy()[rows, heads], rv[rows, heads])
+    for t in (out, dq, dk, dv):
+        assert torch.isfinite(t.float()).all(), f"non-finite output {tag}"
+
+
+@pytest.mark.parametrize("idx,n_random,max_pairs_fwd,max_pairs_bwd", [
+    (2, 6, None, None),
+    (3, 6, None, None),
+    (4, 6, None, None),
+    (5, 4, None, 3e7),
+])
+def test_full_size_workloads_sampled(jg, idx, n_random, max_pairs_fwd, max_pairs_bwd):
+    x = workloads.workload_inputs(idx)
+    uf = sample_units(x, n_random, seed=idx, max_pairs=max_pairs_fwd)
+    ub = sample_units(x, n_random, seed=100 + idx, max_pairs=max_pairs_bwd)
+    check_sampled(jg, x, uf, ub, f"w{idx}")
