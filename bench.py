@@ -1,0 +1,440 @@
+"""Benchmark: jagged GDPA forward + backward on the long-tail workload.
+
+One step is one pass of the whole hot path over one batch: the forward
+(scheduler + forward kernel) and the backward (scheduler, dK/dV pass, dQ pass,
+dbias reduction), through the C ABI of libjgdpa.so.  The workload is the
+long-tail jagged GDPA batch (B=64 segments, H=8, d=128, lengths
+round(LogNormal(ln 1500, 1)) clamped to [100, 16384], GELU, 257-entry
+relative-position bias; seed 4), synthetic data.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Metric: TFLOPS counted over valid (i, j) pairs only: forward 4*pairs*d,
+backward 10*pairs*d, summed over heads; value = whole-job FLOPs / time.
+With N > 1 (torchrun), every rank runs an independent replica on its own GPU
+(the units are independent; there is no exchange step), and the value is the
+FLOPs of all ranks over the slowest rank's time ("weak" scaling).
+
+--impl reference times the fp64 CPU oracle on the host cores over a bounded
+sample of the same workload (some of its segment-head units) in the same
+metric, as the reported CPU baseline.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = 5
+METRIC = "jagged GDPA fwd/bwd TFLOPS over valid pairs; % of GB300 BF16 tensor peak"
+
+
+def valid_pairs(lq, lkv, causal: bool) -> int:
+    """Number of (i, j) pairs with j < Lkv (and j <= i when causal), per head."""
+    lq = np.asarray(lq, dtype=np.int64)
+    lkv = np.asarray(lkv, dtype=np.int64)
+    if not causal:
+        return int(np.sum(lq * lkv))
+    m = np.minimum(lq, lkv)
+    # rows i < m see i+1 keys; rows i >= m see all Lkv keys
+    return int(np.sum(m * (m + 1) // 2 + (lq - m) * lkv))
+
+
+def flops(x) -> tuple[float, float]:
+    p = valid_pairs(x.lq, x.lkv, x.causal) * x.heads
+    return 4.0 * p * x.head_dim, 10.0 * p * x.head_dim
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["bf16_tflops"], d["bf16_tflops_sustained"], d["hbm_gbs"], "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.f is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def subset(x, n: int):
+    """The first n segments of a workload (smaller case for profiler captures)."""
+    import dataclasses
+
+    import workloads
+    qo, ko = x.q_offsets.numpy(), x.kv_offsets.numpy()
+    return dataclasses.replace(
+        x, q=x.q[: qo[n]].contiguous(), k=x.k[: ko[n]].contiguous(), v=x.v[: ko[n]].contiguous(),
+        dout=x.dout[: qo[n]].contiguous(), q_offsets=workloads.offsets_from_lengths(x.lq[:n]),
+        kv_offsets=workloads.offsets_from_lengths(x.lkv[:n]), lq=x.lq[:n], lkv=x.lkv[:n])
+
+
+# ------------------------------------------------------------- CPU baseline
+def oracle_sample(x, budget_s: float, seed: int = 0):
+    """Times the fp64 oracle (fwd + bwd) on a sample of (segment, head) units
+    chosen to take roughly budget_s seconds; returns (TFLOPS, seconds, units,
+    threads)."""
+    import oracle
+    import workloads
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(x.batch)
+    d = x.head_dim
+    pairs = x.lq.astype(np.int64) * x.lkv.astype(np.int64)
+    threads = oracle.max_threads()
+
+    def run(segs):
+        # the sampled segments only, one random head each (units b'*H + h)
+        sub = workloads.select_segments(x, segs)
+        units = [i * x.heads + int(rng.integers(0, x.heads)) for i in range(len(segs))]
+        t0 = time.perf_counter()
+        oracle.fwd_inputs(sub, units=units, threads=threads)
+        oracle.bwd_inputs(sub, units=units, threads=threads)
+        return time.perf_counter() - t0
+
+    # calibrate: the smallest segment on one core
+    small = int(order[np.argmin(pairs[order])])
+    rate = max(int(pairs[small]), 1) / max(run([small]), 1e-6)  # pairs/s on one core
+    target = budget_s * rate * threads
+    cap = max(target / (2 * threads), pairs[small])  # one unit runs on one core
+    segs, tot = [], 0
+    for b in order:
+        if pairs[b] > cap or (tot + pairs[b] > target and segs):
+            continue
+        segs.append(int(b))
+        tot += int(pairs[b])
+        if tot >= target:
+            break
+    dt = run(segs)
+    fl = 14.0 * tot * d
+    return fl / dt / 1e12, dt, segs, tot, threads
+
+
+# --------------------------------------------------------------- native arm
+def run_native(args, world, rank, local):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import jagged_gdpa_gb300 as jg
+    import workloads
+
+    x = workloads.workload_inputs(WORKLOAD)
+    if args.segments:
+        x = subset(x, args.segments)
+    f_fwd, f_bwd = flops(x)
+    dev = torch.device("cuda", local)
+    d = x.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    total_q, heads, hd = x.q.shape
+    total_kv = x.k.shape[0]
+    bias_len = x.bias_len
+    out = torch.empty_like(d.q)
+    dq, dk, dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
+    dbias = torch.empty((heads, bias_len), dtype=torch.float32, device=dev)
+    ws_f = torch.empty(jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, False),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, True),
+                       dtype=torch.uint8, device=dev)
+
+    def fwd():
+        jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
+                     causal=x.causal, out=out, workspace=ws_f)
+
+    def bwd():
+        jg.jgdpa_bwd(d.q, d.k, d.v, out, None, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
+                     bias_table=d.bias, causal=x.causal, dq=dq, dk=dk, dv=dv, dbias=dbias, workspace=ws_b)
+
+    launches_per_step = 2 + 4  # (sched, fwd) + (sched, dK/dV, dQ, dbias reduce)
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if jg.jgdpa_read_device_status(ws_f) or jg.jgdpa_read_device_status(ws_b):
+        raise RuntimeError("device status error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with Clocks(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            fwd()
+            ev[s][1].record(stream)
+            bwd()
+            ev[s][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = clk.summary()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_fwd = [e[0].elapsed_time(e[1]) for e in ev]
+    ms_bwd = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_step = max_over_ranks(world, ms_total / args.steps)
+    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device, step,
+    # results -> pinned host
+    host_in = {k: getattr(x, k).pin_memory() for k in ("q", "k", "v", "dout", "q_offsets", "kv_offsets", "bias")}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in
+                (("out", out), ("dq", dq), ("dk", dk), ("dv", dv), ("dbias", dbias))}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        o, _ = jg.jgdpa_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["q_offsets"], dev_in["kv_offsets"],
+                            x.act, x.scale, bias_table=dev_in["bias"], causal=x.causal, out=out, workspace=ws_f)
+        jg.jgdpa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, None, dev_in["dout"], dev_in["q_offsets"],
+                     dev_in["kv_offsets"], x.act, x.scale, bias_table=dev_in["bias"], causal=x.causal, dq=dq,
+                     dk=dk, dv=dv, dbias=dbias, workspace=ws_b)
+        for k, t in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv), ("dbias", dbias)):
+            host_out[k].copy_(t, non_blocking=True)
+
+    ms_e2e = float("nan")
+    if not args.no_e2e:
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
+        barrier(world)
+
+    bf16_burst, bf16_sust, hbm, peak_kind = peaks()
+    # dominant kernel: the backward passes share one call; the forward kernel
+    # is timed alone (its call adds only the small scheduling kernel)
+    fwd_ms = statistics.mean(ms_fwd)
+    bwd_ms = statistics.mean(ms_bwd)
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "long-tail jagged GDPA fwd+bwd: B=64, H=8, d=128, L~round(LogNormal(ln 1500, 1)) "
+                        "clamped [100, 16384], GELU, rel-pos bias 257, seed 4",
+            "batch_segments": x.batch,
+            "total_tokens": int(total_q),
+            "valid_pairs_x_heads": int(valid_pairs(x.lq, x.lkv, x.causal) * heads),
+            "fwd_tflop_per_step": f_fwd / 1e12,
+            "bwd_tflop_per_step": f_bwd / 1e12,
+            "l2": "inputs larger than L2 (1.2 GB of Q/K/V/dO per step vs 129 MB L2); no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "fwd_ms": round(fwd_ms, 4),
+        "bwd_ms": round(bwd_ms, 4),
+        "fwd_tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
+        "bwd_tflops": round(f_bwd / (bwd_ms * 1e-3) / 1e12, 2),
+        "roofline": {
+            "kernel": "gdpa_fwd_kernel (timed with CUDA events around jgdpa_fwd; includes the ~10 us "
+                      "scheduling kernel)",
+            "bound": "tensor",
+            "achieved": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
+            "peak": bf16_sust,
+            "unit": "TFLOP/s",
+            "frac": round(f_fwd / (fwd_ms * 1e-3) / 1e12 / bf16_sust, 4),
+            "peak_kind": f"{peak_kind} bf16 sustained",
+            "traffic": None,
+        },
+        "e2e": {
+            "value": round(world * (f_fwd + f_bwd) / (ms_e2e * 1e-3) / 1e12, 2),
+            "unit": "TFLOPS",
+            "ms_per_step": round(ms_e2e, 4),
+            "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h),
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, dt, units, tot, threads = oracle_sample(x, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = {
+            "value": round(tf, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"{len(units)} (segment, head) units of the same workload, {tot} valid pairs, "
+                      f"fwd+bwd in fp64, {dt:.1f} s wall",
+        }
+    return result
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: rank 0 only, bounded sample per step."""
+    if rank != 0:
+        return None
+    import oracle
+    import workloads
+    oracle.build()
+    x = workloads.workload_inputs(WORKLOAD)
+    budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(x, budget_s=budget, seed=1)
+    vals, secs, tot_pairs, n_units = [], 0.0, 0, 0
+    for s in range(args.steps):
+        tf, dt, units, tot, threads = oracle_sample(x, budget_s=budget, seed=2 + s)
+        vals.append(tf)
+        secs += dt
+        tot_pairs += tot
+        n_units += len(units)
+    value = 14.0 * tot_pairs * x.head_dim / secs / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "long-tail jagged GDPA fwd+bwd (B=64, H=8, d=128, GELU, bias 257, seed 4); "
+                               "each step a bounded sample of its (segment, head) units"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_units} units, {tot_pairs} valid pairs over {args.steps} steps"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) timing")
+    ap.add_argument("--segments", type=int, default=0, help="use only the first N segments (profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    world, rank, local = dist_setup()
+    res = run_native(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

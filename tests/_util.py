@@ -72,3 +72,31 @@ def oracle_fwd(x, units=None):
 
 def oracle_bwd(x, units=None):
     return oracle.bwd_inputs(x, units=units)
+
+
+def sampled_oracle(x, units, backward: bool):
+    """Oracle results for the (segment, head) units b*H + h of a large batch,
+    computed on a compact copy holding only those segments.  Returns a list of
+    (b, h, q_rows, kv_rows, results) where q_rows / kv_rows index the full
+    batch and results are the oracle arrays restricted to that unit's rows."""
+    import workloads
+    segs = [u // x.heads for u in units]
+    sub = workloads.select_segments(x, segs)
+    sub_units = [i * x.heads + (u % x.heads) for i, u in enumerate(units)]
+    res = oracle.bwd_inputs(sub, units=sub_units) if backward else oracle.fwd_inputs(sub, units=sub_units)
+    qo, ko = x.q_offsets.numpy(), x.kv_offsets.numpy()
+    sqo, sko = sub.q_offsets.numpy(), sub.kv_offsets.numpy()
+    out = []
+    for i, u in enumerate(units):
+        b, h = divmod(u, x.heads)
+        q_rows = np.arange(qo[b], qo[b + 1])
+        kv_rows = np.arange(ko[b], ko[b + 1])
+        sq = slice(sqo[i], sqo[i + 1])
+        sk = slice(sko[i], sko[i + 1])
+        if backward:
+            dq, dk, dv, _ = res
+            out.append((b, h, q_rows, kv_rows, (dq[sq, h], dk[sk, h], dv[sk, h])))
+        else:
+            o, lse = res
+            out.append((b, h, q_rows, kv_rows, (o[sq, h], lse[h, sq])))
+    return out

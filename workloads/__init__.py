@@ -164,6 +164,23 @@ def make_inputs(lq, lkv, heads: int, head_dim: int, act: str, causal: bool = Fal
                   heads=h, head_dim=d, act=act, causal=causal, scale=scale, q_seed=q_seed)
 
 
+def select_segments(x: Inputs, segs) -> Inputs:
+    """A compact Inputs holding only the listed segments (in the given order),
+    with their rows copied and the offsets rebuilt; used to run the oracle on a
+    sample of a large batch."""
+    segs = [int(b) for b in segs]
+    qo, ko = x.q_offsets.numpy(), x.kv_offsets.numpy()
+    qi = np.concatenate([np.arange(qo[b], qo[b + 1]) for b in segs]) if segs else np.zeros(0, np.int64)
+    ki = np.concatenate([np.arange(ko[b], ko[b + 1]) for b in segs]) if segs else np.zeros(0, np.int64)
+    qi = torch.from_numpy(qi.astype(np.int64))
+    ki = torch.from_numpy(ki.astype(np.int64))
+    lq, lkv = x.lq[segs], x.lkv[segs]
+    return dataclasses.replace(
+        x, q=x.q[qi].contiguous(), k=x.k[ki].contiguous(), v=x.v[ki].contiguous(),
+        dout=x.dout[qi].contiguous(), q_offsets=offsets_from_lengths(lq),
+        kv_offsets=offsets_from_lengths(lkv), lq=lq, lkv=lkv)
+
+
 def workload_inputs(index: int) -> Inputs:
     """The full-size inputs of workload ``index`` (1..5)."""
     w = WORKLOADS[index]
