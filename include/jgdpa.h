@@ -147,6 +147,40 @@ JGDPA_API jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v,
                        void* workspace, size_t workspace_bytes, jgdpa_stream_t stream);
 
 /*
+ * Forward pass without a caller-provided workspace: the same computation and
+ * arguments as jgdpa_fwd minus (workspace, workspace_bytes).  There is no
+ * counterpart on the pages; this entry point exists for callers that cannot
+ * allocate device memory at call time -- for example a plugin interface that
+ * hands over only input and output buffers, or a process whose device memory
+ * is already fully reserved by another allocator, so that a cudaMalloc would
+ * fail or force a synchronising reclaim.  The caller still owns and passes
+ * every input and output.
+ *
+ * Scratch comes from a fixed array of JGDPA_NOALLOC_SCRATCH_BYTES (4 MiB)
+ * compiled into the library; every GPU that loads the library holds that
+ * array until the process exits.  Sizes whose scratch would not fit (about
+ * 260,000 units of (segment, head, pair of 128-row query tiles)) are rejected
+ * with JGDPA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  No call allocates or frees memory.  All calls
+ * on a device share the one array and it keeps the previous call's contents
+ * (the parts that must start at zero are cleared on the stream by each call):
+ * calls that overlap in time on the GPU -- on different streams, or from
+ * different host threads -- race on it and must be serialised by the caller.
+ * Device-detected errors (bad offsets) leave the outputs unwritten and are not
+ * reported by this entry point; use jgdpa_fwd to read them back.
+ */
+#define JGDPA_NOALLOC_SCRATCH_BYTES (4u << 20)
+JGDPA_API jgdpa_status jgdpa_fwd_noalloc(const void* q, const void* k, const void* v,
+                       const int32_t* q_offsets, const int32_t* kv_offsets,
+                       int32_t batch, int64_t total_q, int64_t total_kv,
+                       int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
+                       const float* bias_table, int32_t bias_len, int32_t causal,
+                       void* out, float* lse, jgdpa_stream_t stream);
+
+/*
  * Reads the device status word of `workspace` (synchronises `stream`) and
  * returns JGDPA_OK, a device-detected error, or JGDPA_ERR_CUDA.
  */

@@ -24,7 +24,7 @@ STATUS = {
     6: "JGDPA_ERR_BAD_OFFSETS", 7: "JGDPA_ERR_DEVICE_TIMEOUT",
 }
 EXPORTS = ("jgdpa_workspace_bytes", "jgdpa_fwd", "jgdpa_bwd", "jgdpa_read_device_status",
-           "jgdpa_status_string", "jgdpa_eval_activation")
+           "jgdpa_status_string", "jgdpa_eval_activation", "jgdpa_fwd_noalloc")
 
 
 class JgdpaError(RuntimeError):
@@ -59,6 +59,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.jgdpa_status_string.restype = ctypes.c_char_p
     lib.jgdpa_eval_activation.argtypes = [ctypes.c_int, i32, P, i64, P, P, P]
     lib.jgdpa_eval_activation.restype = ctypes.c_int
+    lib.jgdpa_fwd_noalloc.argtypes = [P, P, P, P, P, i32, i64, i64, i32, i32, ctypes.c_int, f32, P, i32, i32,
+                                      P, P, P]
+    lib.jgdpa_fwd_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -148,6 +151,28 @@ def jgdpa_bwd(q, k, v, out, lse, dout, q_offsets, kv_offsets, act, scale: float,
                        _ptr(dbias), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "jgdpa_bwd")
     return dq, dk, dv, dbias
+
+
+def jgdpa_fwd_noalloc(q, k, v, q_offsets, kv_offsets, act, scale: float, bias_table=None,
+                      causal: bool = False, out=None, lse=None, stream=None):
+    """Forward pass using the library's built-in scratch (no workspace
+    argument; for callers that cannot allocate device memory at call time).
+    out / lse must be passed by such callers; they are created here only for
+    convenience when omitted.  Returns (out, lse)."""
+    lib = load()
+    total_q, heads, d = q.shape
+    a = _act(act)
+    bias_len = 0 if bias_table is None else int(bias_table.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and a == ACT["softmax"]:
+        lse = torch.empty((heads, total_q), dtype=torch.float32, device=q.device)
+    rc = lib.jgdpa_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(kv_offsets),
+                               q_offsets.numel() - 1, total_q, k.shape[0], heads, d, a, float(scale),
+                               _ptr(bias_table), bias_len, int(bool(causal)), _ptr(out), _ptr(lse),
+                               _stream(stream))
+    _check(rc, "jgdpa_fwd_noalloc")
+    return out, lse
 
 
 def jgdpa_read_device_status(workspace, stream=None) -> int:

@@ -385,3 +385,48 @@ jgdpa_status jgdpa_eval_activation(jgdpa_act act, int32_t path, const float* x, 
 }
 
 }  // extern "C"
+
+// --------------------------------------------------------------------------
+// Forward without a caller workspace: scratch lives in a fixed device array.
+namespace {
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[JGDPA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[128] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.  (In host code the array's name is
+// only a host-side stand-in and must never reach a kernel.)
+jgdpa_status noalloc_scratch(void** addr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return JGDPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return JGDPA_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return JGDPA_OK;
+}
+
+}  // namespace
+
+extern "C" jgdpa_status jgdpa_fwd_noalloc(const void* q, const void* k, const void* v, const int32_t* q_offsets,
+                                          const int32_t* kv_offsets, int32_t batch, int64_t total_q,
+                                          int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
+                                          float scale, const float* bias_table, int32_t bias_len, int32_t causal,
+                                          void* out, float* lse, jgdpa_stream_t stream) {
+  jgdpa_status st = check_common(batch, total_q, total_kv, heads, head_dim, act, scale, bias_table, bias_len,
+                                 causal, q_offsets, kv_offsets);
+  if (st != JGDPA_OK) return st;
+  Layout L;
+  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, false, &L)) return JGDPA_ERR_CUDA;
+  if (L.total > JGDPA_NOALLOC_SCRATCH_BYTES) return JGDPA_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != JGDPA_OK) return st;
+  return jgdpa_fwd(q, k, v, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act, scale,
+                   bias_table, bias_len, causal, out, lse, scratch, JGDPA_NOALLOC_SCRATCH_BYTES, stream);
+}
