@@ -142,6 +142,112 @@ __device__ __forceinline__ float silu_alu_d(float x, float& dy) {
   return x * s;
 }
 
+// ------------------------------------------------- packed (two-lane) forms
+// Both take hx = x / 2 for two elements (the kernels fold the 1/2 into the
+// scale and bias), so GELU(x) = hx + hx tanh(u) with
+// u = (a x + b x^3) / 2 = hx (a + 4 b hx^2), and SiLU(x) = hx + hx tanh(hx).
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+__device__ __forceinline__ float2 tanh2_sfu(float2 u) { return make_float2(tanh_sfu(u.x), tanh_sfu(u.y)); }
+
+// 2^w for two lanes, w already in [-64, 64].
+__device__ __forceinline__ float2 exp2_alu2(float2 w) {
+  const float kRound = 12582912.0f;
+  const float2 t = __fadd2_rn(w, f2(kRound));
+  const float2 n = __fadd2_rn(t, f2(-kRound));
+  const float2 f = __fadd2_rn(w, make_float2(-n.x, -n.y));
+  float2 p = __ffma2_rn(f2(kExpP3), f, f2(kExpP2));
+  p = __ffma2_rn(p, f, f2(kExpP1));
+  p = __ffma2_rn(p, f, f2(kExpP0));
+  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
+// 1 / a for two lanes (a >= 1).
+__device__ __forceinline__ float2 rcp_alu2(float2 a) {
+  float2 y = make_float2(__int_as_float(kRcpSeed - __float_as_int(a.x)),
+                         __int_as_float(kRcpSeed - __float_as_int(a.y)));
+  const float2 na = make_float2(-a.x, -a.y);
+  float2 e = __ffma2_rn(na, y, f2(1.0f));
+  y = __ffma2_rn(y, e, y);
+  e = __ffma2_rn(na, y, f2(1.0f));
+  return __ffma2_rn(y, e, y);
+}
+// sigmoid(z) with w = -z log2 e given; also returns e = 2^w.
+__device__ __forceinline__ float2 sigmoid_alu2_w(float2 w, float2& e) {
+  w = make_float2(fminf(fmaxf(w.x, -64.0f), 64.0f), fminf(fmaxf(w.y, -64.0f), 64.0f));
+  e = exp2_alu2(w);
+  return rcp_alu2(__fadd2_rn(e, f2(1.0f)));
+}
+
+template <int ACT>
+__device__ __forceinline__ float2 act2_sfu(float2 hx) {
+  float2 u = hx;
+  if constexpr (ACT == 0) u = __fmul2_rn(hx, __ffma2_rn(__fmul2_rn(hx, hx), f2(4.0f * kGeluB), f2(kGeluA)));
+  return __ffma2_rn(hx, tanh2_sfu(u), hx);
+}
+template <int ACT>
+__device__ __forceinline__ float2 act2_alu(float2 hx) {
+  // w = -2 u log2 e  (GELU),  w = -2 hx log2 e  (SiLU);  y = 2 hx sigmoid
+  float2 w;
+  if constexpr (ACT == 0)
+    w = __fmul2_rn(hx, __ffma2_rn(__fmul2_rn(hx, hx), f2(-8.0f * kGeluB * kLog2e), f2(-2.0f * kGeluA * kLog2e)));
+  else
+    w = __fmul2_rn(hx, f2(-2.0f * kLog2e));
+  float2 e;
+  const float2 s = sigmoid_alu2_w(w, e);
+  const float2 hs = __fmul2_rn(hx, s);
+  return __fadd2_rn(hs, hs);
+}
+template <int ACT, bool ALU>
+__device__ __forceinline__ float2 act2(float2 hx) {
+  if constexpr (ALU) return act2_alu<ACT>(hx);
+  else return act2_sfu<ACT>(hx);
+}
+
+// act(x) and act'(x) for two lanes from hx = x / 2 (SFU route).
+//   GELU: act' = s + x s (1 - s) k'(x), s = (1 + t) / 2, s (1 - s) = (1 - t^2) / 4,
+//         k'(x) / 2 = a / 2 + 6 b hx^2  ->  act' = s + hx (1 - t^2) k'/2
+//   SiLU: act' = s + x s (1 - s) = s + hx (1 - t^2) / 2
+template <int ACT>
+__device__ __forceinline__ float2 act2_d_sfu(float2 hx, float2& dy) {
+  const float2 h2 = __fmul2_rn(hx, hx);
+  float2 u = hx;
+  if constexpr (ACT == 0) u = __fmul2_rn(hx, __ffma2_rn(h2, f2(4.0f * kGeluB), f2(kGeluA)));
+  const float2 t = tanh2_sfu(u);
+  const float2 q = __ffma2_rn(make_float2(-t.x, -t.y), t, f2(1.0f));
+  const float2 s = __ffma2_rn(t, f2(0.5f), f2(0.5f));
+  float2 kp;
+  if constexpr (ACT == 0) kp = __ffma2_rn(h2, f2(6.0f * kGeluB), f2(0.5f * kGeluA));
+  else kp = f2(0.5f);
+  dy = __ffma2_rn(__fmul2_rn(hx, q), kp, s);
+  return __ffma2_rn(hx, t, hx);
+}
+// ALU route: with s = sigmoid(k), s (1 - s) = e s^2 (e = 2^(-k log2 e)):
+//   GELU: act' = s (1 + x e s k'(x)),  SiLU: act' = s (1 + x e s)
+template <int ACT>
+__device__ __forceinline__ float2 act2_d_alu(float2 hx, float2& dy) {
+  const float2 h2 = __fmul2_rn(hx, hx);
+  float2 w;
+  if constexpr (ACT == 0)
+    w = __fmul2_rn(hx, __ffma2_rn(h2, f2(-8.0f * kGeluB * kLog2e), f2(-2.0f * kGeluA * kLog2e)));
+  else
+    w = __fmul2_rn(hx, f2(-2.0f * kLog2e));
+  float2 e;
+  const float2 s = sigmoid_alu2_w(w, e);
+  const float2 x = __fadd2_rn(hx, hx);
+  float2 kp;
+  if constexpr (ACT == 0) kp = __ffma2_rn(h2, f2(12.0f * kGeluB), f2(kGeluA));  // k'(x) = a + 3 b x^2
+  else kp = f2(1.0f);
+  const float2 xes = __fmul2_rn(__fmul2_rn(x, e), s);
+  dy = __fmul2_rn(s, __ffma2_rn(xes, kp, f2(1.0f)));
+  return __fmul2_rn(x, s);
+}
+template <int ACT, bool ALU>
+__device__ __forceinline__ float2 act2_d(float2 hx, float2& dy) {
+  if constexpr (ALU) return act2_d_alu<ACT>(hx, dy);
+  else return act2_d_sfu<ACT>(hx, dy);
+}
+
 // Dispatch on (act, route) at compile time.  ACT: 0 = GELU, 1 = SiLU.
 template <int ACT, bool ALU>
 __device__ __forceinline__ float act_val(float x) {

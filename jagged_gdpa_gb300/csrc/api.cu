@@ -166,15 +166,33 @@ cudaError_t fill_f32(float* p, int64_t n, float v, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Evaluates the kernels' packed activation routines (act2: forward value,
+// act2_d: backward derivative) on two elements per thread, from hx = x / 2
+// exactly as the kernels form it.
+template <int ACT, bool ALU>
+__device__ void eval_act_pair(const float* x, int64_t i, int64_t n, float* y, float* dy) {
+  const float2 hx = make_float2(0.5f * x[i], i + 1 < n ? 0.5f * x[i + 1] : 0.f);
+  const float2 a = jg::act2<ACT, ALU>(hx);
+  float2 d;
+  (void)jg::act2_d<ACT, ALU>(hx, d);
+  y[i] = a.x;
+  if (dy) dy[i] = d.x;
+  if (i + 1 < n) {
+    y[i + 1] = a.y;
+    if (dy) dy[i + 1] = d.y;
+  }
+}
+
 __global__ void eval_act_kernel(int act, int path, const float* x, int64_t n, float* y, float* dy) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t i = 2 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
   if (i >= n) return;
-  const float v = x[i];
-  float a, d;
-  if (act == 0) a = path ? jg::act_val_d<0, true>(v, d) : jg::act_val_d<0, false>(v, d);
-  else a = path ? jg::act_val_d<1, true>(v, d) : jg::act_val_d<1, false>(v, d);
-  y[i] = a;
-  if (dy) dy[i] = d;
+  if (act == 0) {
+    if (path) eval_act_pair<0, true>(x, i, n, y, dy);
+    else eval_act_pair<0, false>(x, i, n, y, dy);
+  } else {
+    if (path) eval_act_pair<1, true>(x, i, n, y, dy);
+    else eval_act_pair<1, false>(x, i, n, y, dy);
+  }
 }
 
 jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batch, int32_t heads,
@@ -379,7 +397,7 @@ jgdpa_status jgdpa_eval_activation(jgdpa_act act, int32_t path, const float* x, 
     return JGDPA_ERR_INVALID_ARGUMENT;
   if (n == 0) return JGDPA_OK;
   if (x == nullptr || y == nullptr) return JGDPA_ERR_INVALID_ARGUMENT;
-  eval_act_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(act, path, x, n, y, dy);
+  eval_act_kernel<<<static_cast<unsigned>((n + 511) / 512), 256, 0, stream>>>(act, path, x, n, y, dy);
   JG_CUDA(cudaGetLastError());
   return JGDPA_OK;
 }

@@ -5,22 +5,28 @@
 // atomics-free backward of "Eliminating Compute Waste in Asymmetric
 // Workloads", aiuniverse.news):
 //
-//   dkdv pass, unit = (segment, head, 128-row key/value tile j0):
+//   dkdv pass, unit = (segment, head, 128-row key/value tile):
 //     for every query tile that meets it:
 //       S^T = K Q^T, dP^T = V dO^T                       (tcgen05, TMEM)
-//       P^T = act(x)^T, dS^T = dP^T act'(x)^T            (activation warps)
+//       phase A: P^T = act(x)^T, act'(x) kept in registers
+//       phase B: dS^T = dP^T act'(x)^T, dbias partials
 //       (softmax: P = exp(x - LSE_i), dS = P (dP - D_i))
-//       dV += P^T dO, dK += dS^T Q                       (tcgen05, TMEM)
-//     dK *= s; store dK, dV; dbias partial sums of dS
+//       dV += P^T dO (after phase A), dK += dS^T Q (after phase B)
+//     dK *= s; store dK, dV
 //   dq pass, unit = (segment, head, 128-row query tile):
-//     for every key/value tile: S = Q K^T, dP = dO V^T, dS, dQ += dS K
+//     for every key/value tile: S = Q K^T (double-buffered), dP = dO V^T,
+//       phase A: act'(x); phase B: dS = dP act'(x); dQ += dS K
 //     dQ *= s; store
 //
+// Phase A runs while the tensor core computes dP; phase B runs while it
+// computes dV (dkdv) or the next tile's S (dq), so the activation work hides
+// behind the MMAs.
+//
 // TMEM (512 columns): dkdv uses S^T [0,128), dP^T [128,256), dV [256,256+D),
-// dK [256+D, 256+2D); dq uses S [0,128), dP [128,256), dQ [256,256+D).  Two
-// activation warpgroups split the 128 columns of a tile; each writes its
-// bf16 P / dS over S / dP columns that it has already read, and the MMA picks
-// the operand columns per 16-wide K step.
+// dK [256+D, 256+2D); dq uses S0 [0,128), dP [128,256), dQ [256,256+D),
+// S1 [384,512).  Two activation warpgroups split the 128 columns of a tile;
+// each writes its bf16 P / dS over S / dP columns that it has already read,
+// and the MMA picks the operand columns per 16-wide K step.
 #include "act.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
@@ -47,7 +53,7 @@ struct BwdCfg {
 
 struct BwdBars {
   uint64_t res_full, res_empty;
-  uint64_t s_full, p_full, acc_full, acc_empty;
+  uint64_t s_full[2], dp_full, p_full, ds_full, acc_full, acc_empty;
   uint64_t drain;
   uint64_t grp[2];
   uint64_t st_full[4], st_empty[4];
@@ -171,48 +177,42 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
 }
 
 // ---------------------------------------------------------------- MMA issuer
-template <int D, bool KV_MAJOR>
-__device__ void bwd_mma(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units, Fail fail) {
+// dkdv, per query tile: S^T, dP^T, [P^T ready] dV, [dS^T ready] dK.
+template <int D>
+__device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
+                           Fail fail) {
   using C = BwdCfg<D>;
-  const uint32_t res0 = smem_u32(smem + C::kResOff);
-  const uint32_t res1 = res0 + C::kTileBytes;
+  const uint32_t k_t = smem_u32(smem + C::kResOff), v_t = k_t + C::kTileBytes;
   const uint32_t str_base = smem_u32(smem + C::kStreamOff);
   uint32_t res_it = 0, st_it = 0, p_it = 0, acc_it = 0;
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
     if (idx >= n_units) break;
-    const BwdUnit u = bwd_unit<KV_MAJOR>(p, idx);
+    const BwdUnit u = bwd_unit<true>(p, idx);
     if (u.count == 0) continue;
     if (!(ok = mbar_wait(&bars->res_full, res_it & 1, fail))) break;
     ++res_it;
     for (int i = 0; i < u.count; ++i) {
       const int st = st_it % C::kStages;
-      const uint32_t s0 = str_base + st * 2 * C::kTileBytes;
-      const uint32_t s1 = s0 + C::kTileBytes;
+      const uint32_t q_t = str_base + st * 2 * C::kTileBytes, do_t = q_t + C::kTileBytes;
       if (!(ok = mbar_wait(&bars->st_full[st], (st_it / C::kStages) & 1, fail))) break;
       tc_fence_after();
-      if constexpr (KV_MAJOR) {
-        mma_tile_nt<D>(tmem, res0, s0);        // S^T  = K  Q^T
-        mma_tile_nt<D>(tmem + 128, res1, s1);  // dP^T = V  dO^T
-      } else {
-        mma_tile_nt<D>(tmem, res0, s0);        // S  = Q  K^T
-        mma_tile_nt<D>(tmem + 128, res1, s1);  // dP = dO V^T
-      }
-      mma_commit(&bars->s_full);
+      mma_tile_nt<D>(tmem, k_t, q_t);  // S^T  = K  Q^T
+      mma_commit(&bars->s_full[0]);
+      mma_tile_nt<D>(tmem + 128, v_t, do_t);  // dP^T = V  dO^T
+      mma_commit(&bars->dp_full);
       if (i == 0) {
         if (!(ok = mbar_wait(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
         ++acc_it;
       }
       if (!(ok = mbar_wait(&bars->p_full, p_it & 1, fail))) break;
+      tc_fence_after();
+      mma_tile_tn<D>(tmem + 256, tmem + 0, tmem + 64, do_t, i > 0);  // dV += P^T dO
+      if (!(ok = mbar_wait(&bars->ds_full, p_it & 1, fail))) break;
       ++p_it;
       tc_fence_after();
-      if constexpr (KV_MAJOR) {
-        mma_tile_tn<D>(tmem + 256, tmem + 0, tmem + 64, s1, i > 0);          // dV += P^T  dO
-        mma_tile_tn<D>(tmem + 256 + D, tmem + 128, tmem + 192, s0, i > 0);   // dK += dS^T Q
-      } else {
-        mma_tile_tn<D>(tmem + 256, tmem + 0, tmem + 64, s0, i > 0);          // dQ += dS K
-      }
+      mma_tile_tn<D>(tmem + 256 + D, tmem + 128, tmem + 192, q_t, i > 0);  // dK += dS^T Q
       mma_commit(&bars->st_empty[st]);
       ++st_it;
       if (i == u.count - 1) {
@@ -225,10 +225,106 @@ __device__ void bwd_mma(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
   mbar_wait_drain(&bars->drain, 0);
 }
 
+// dq, per key tile i (S buffers alternate): dP(i), S(i+1), [dS(i) ready] dQ.
+template <int D>
+__device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
+                          Fail fail) {
+  using C = BwdCfg<D>;
+  const uint32_t q_t = smem_u32(smem + C::kResOff), do_t = q_t + C::kTileBytes;
+  const uint32_t str_base = smem_u32(smem + C::kStreamOff);
+  const uint32_t t_s[2] = {tmem, tmem + 384};
+  uint32_t res_it = 0, st_it = 0, ds_it = 0, acc_it = 0, s_cnt = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = unit_index(r, blockIdx.x, gridDim.x);
+    if (idx >= n_units) break;
+    const BwdUnit u = bwd_unit<false>(p, idx);
+    if (u.count == 0) continue;
+    if (!(ok = mbar_wait(&bars->res_full, res_it & 1, fail))) break;
+    ++res_it;
+    {  // S of the first key tile
+      const int st = st_it % C::kStages;
+      if (!(ok = mbar_wait(&bars->st_full[st], (st_it / C::kStages) & 1, fail))) break;
+      tc_fence_after();
+      mma_tile_nt<D>(t_s[s_cnt & 1], q_t, str_base + st * 2 * C::kTileBytes);
+      mma_commit(&bars->s_full[s_cnt & 1]);
+    }
+    for (int i = 0; i < u.count; ++i) {
+      const uint32_t it = st_it + i;
+      const int st = it % C::kStages;
+      const uint32_t k_t = str_base + st * 2 * C::kTileBytes, v_t = k_t + C::kTileBytes;
+      const uint32_t sb = (s_cnt + i) & 1;
+      mma_tile_nt<D>(tmem + 128, do_t, v_t);  // dP = dO V^T
+      mma_commit(&bars->dp_full);
+      if (i + 1 < u.count) {  // S of the next key tile into the other buffer
+        const int st1 = (it + 1) % C::kStages;
+        if (!(ok = mbar_wait(&bars->st_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
+        tc_fence_after();
+        mma_tile_nt<D>(t_s[sb ^ 1], q_t, str_base + st1 * 2 * C::kTileBytes);
+        mma_commit(&bars->s_full[sb ^ 1]);
+      }
+      if (i == 0) {
+        if (!(ok = mbar_wait(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
+        ++acc_it;
+      }
+      if (!(ok = mbar_wait(&bars->ds_full, ds_it & 1, fail))) break;
+      ++ds_it;
+      tc_fence_after();
+      mma_tile_tn<D>(tmem + 256, t_s[sb], t_s[sb] + 64, k_t, i > 0);  // dQ += dS K
+      mma_commit(&bars->st_empty[st]);
+    }
+    if (!ok) break;
+    st_it += u.count;
+    s_cnt += u.count;
+    mma_commit(&bars->acc_full);
+    mma_commit(&bars->res_empty);
+  }
+  mma_commit(&bars->drain);
+  mbar_wait_drain(&bars->drain, 0);
+}
+
 // --------------------------------------------------------- activation warps
-// Element of the bias table for relative position rel.
-__device__ __forceinline__ float bias_val(const float* row, int rel, int R) {
-  return ld_nc_f32(row + min(max(rel, -R), R) + R);
+// Geometry of one (own tile, partner tile) pair for the thread of row r.
+// KV-major: own row = key j, column c = query i; Q-major: own row = query i,
+// column c = key j.  rel = i - j = rel0 + sgn * c.  Valid columns are
+// lo <= c < hi (the subtraction scheme: both bounds computed once per tile).
+struct PairGeom {
+  int lo, hi;
+  int rel0, sgn;
+  bool masked;   // some column of some row of this warp is invalid
+  bool band;     // some |rel| < R in this tile (per-element bias)
+  bool upper;    // not band: every rel >= R (else every rel <= -R)
+  float bconst;  // the bias of every element when not band (0 without a table)
+};
+
+template <bool KV_MAJOR>
+__device__ __forceinline__ PairGeom pair_geom(const BwdParams& p, const BwdUnit& u, int pt, int r, bool row_ok,
+                                              const float* brow, int R) {
+  PairGeom g;
+  g.lo = 0;
+  if constexpr (KV_MAJOR) {
+    g.hi = min(kTile, u.seg.lq - pt * kTile);
+    if (p.causal && pt == u.tile) g.lo = r;               // i >= j  <=>  c >= r
+    g.rel0 = (pt - u.tile) * kTile - r;
+    g.sgn = 1;
+  } else {
+    g.hi = min(kTile, u.seg.lkv - pt * kTile);
+    if (p.causal && pt == u.tile) g.hi = min(g.hi, r + 1);  // j <= i  <=>  c <= r
+    g.rel0 = (u.tile - pt) * kTile + r;
+    g.sgn = -1;
+  }
+  if (!row_ok) g.hi = 0;
+  g.masked = __any_sync(0xffffffffu, g.lo > 0 || g.hi < kTile);
+  const int relmin = (KV_MAJOR ? (pt - u.tile) : (u.tile - pt)) * kTile - (kTile - 1);
+  const int relmax = relmin + 2 * (kTile - 1);
+  g.band = brow != nullptr && relmin < R && relmax > -R;
+  g.upper = relmin >= R;
+  g.bconst = brow == nullptr ? 0.f : (g.upper ? __ldg(brow + 2 * R) : __ldg(brow));
+  return g;
+}
+
+__device__ __forceinline__ float bias_lookup(const float* brow, int rel, int R) {
+  return ld_nc_f32(brow + min(max(rel, -R), R) + R);
 }
 
 template <int D, int ACT, bool KV_MAJOR>
@@ -241,13 +337,14 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
   const int r = quad * 32 + (threadIdx.x & 31);    // row of this unit's own tile
   const int act_tid = threadIdx.x - 128;           // 0..255 over both warpgroups
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-  const uint32_t t_s = tmem + lane_off + 64 * half;
   const uint32_t t_dp = tmem + lane_off + 128 + 64 * half;
   const int H = p.heads;
   const bool want_dbias = KV_MAJOR && p.dbias_part != nullptr;
   const int R = (p.bias_len - 1) / 2;
   float* sbias = reinterpret_cast<float*>(smem + C::kBiasOff);
-  uint32_t s_it = 0, acc_it = 0, grp_it = 0;
+  uint32_t s_it = 0, dp_it = 0, acc_it = 0, grp_it = 0;
+  const float hs = 0.5f * p.scale;                 // x / 2 = hs S + bias / 2
+  const float s2 = p.scale * kLog2e;               // softmax: x log2 e
 
   for (int rr = 0;; ++rr) {
     const int idx = unit_index(rr, blockIdx.x, gridDim.x);
@@ -285,111 +382,133 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
 
     bool ok = true;
     for (int i = 0; i < u.count; ++i) {
-      if (!(ok = mbar_wait(&bars->s_full, s_it & 1, fail))) break;
+      const int pt = u.first + i;  // partner tile
+      const PairGeom g = pair_geom<KV_MAJOR>(p, u, pt, r, row_ok, brow, R);
+      // S buffer of this tile: dkdv always columns 0; dq alternates 0 / 384
+      const uint32_t sbuf = KV_MAJOR ? 0u : ((s_it & 1) ? 384u : 0u);
+      const uint32_t t_s = tmem + lane_off + sbuf + 64 * half;
+      uint64_t* sfull = &bars->s_full[KV_MAJOR ? 0 : (s_it & 1)];
+      const uint32_t sphase = KV_MAJOR ? (s_it & 1) : ((s_it >> 1) & 1);
+      if (!(ok = mbar_wait(sfull, sphase, fail))) break;
       ++s_it;
       tc_fence_after();
-      const int pt = u.first + i;  // partner tile
-      // Geometry: own row index a = tile*128 + r, partner column b = pt*128 + c.
-      // rel = i_q - j_kv; valid pairs need j_kv <= i_q under causal masking.
-      int lo = 0, hi = kTile;
-      int rel0;  // rel at c = 0
-      if constexpr (KV_MAJOR) {
-        hi = min(kTile, u.seg.lq - pt * kTile);
-        if (p.causal && pt == u.tile) lo = r;                 // i >= j  <=>  c >= r
-        rel0 = (pt - u.tile) * kTile - r;                      // rel = rel0 + c
-      } else {
-        hi = min(kTile, u.seg.lkv - pt * kTile);
-        if (p.causal && pt == u.tile) hi = min(hi, r + 1);    // j <= i  <=>  c <= r
-        rel0 = (u.tile - pt) * kTile + r;                      // rel = rel0 - c
-      }
-      if (!row_ok) hi = 0;
-      const bool tile_masked = lo > 0 || hi < kTile;
-      const bool tile_masked_any = __any_sync(0xffffffffu, tile_masked);
-      // bias band: is any |rel| < R in this tile?
-      const int relmin = (KV_MAJOR ? (pt - u.tile) * kTile - (kTile - 1) : (u.tile - pt) * kTile - (kTile - 1));
-      const int relmax = relmin + 2 * (kTile - 1);
-      const bool has_bias = brow != nullptr;
-      const bool band = has_bias && relmin < R && relmax > -R;
-      const float bconst = has_bias ? (relmin >= R ? __ldg(brow + 2 * R) : __ldg(brow)) : 0.f;
 
-#pragma unroll 1
+      // ---- phase A: S -> (P, act'(x)) [softmax: P]; P^T to TMEM (dkdv)
+      float keep[64];  // act'(x) (GELU/SiLU) or P (softmax) per owned column
+#pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
-        const int cbase = 64 * half + 32 * chunk;  // first column (0..127) of this chunk
-        uint32_t sv[32], dpv[32];
+        const int cbase = 64 * half + 32 * chunk;
+        uint32_t sv[32];
         tmem_ld32(t_s + 32 * chunk, sv);
-        tmem_ld32(t_dp + 32 * chunk, dpv);
-        tmem_ld_wait2(sv, dpv);
-        float lse_c[32], del_c[32];
+        float lse_c[32];
         if constexpr (kSoftmax && KV_MAJOR) {
-          // statistics of the query rows that are this chunk's columns
           const int64_t q0 = static_cast<int64_t>(u.h) * p.total_q + u.seg.q0 + pt * kTile + cbase;
           const int lim = max(0, min(32, u.seg.lq - pt * kTile - cbase));
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            lse_c[e] = e < lim ? __ldg(p.lse + q0 + e) * kLog2e : 0.f;
-            del_c[e] = e < lim ? __ldg(p.delta + q0 + e) : 0.f;
-          }
+          for (int e = 0; e < 32; ++e) lse_c[e] = e < lim ? __ldg(p.lse + q0 + e) * kLog2e : 0.f;
         }
-        uint32_t pk_p[16], pk_ds[16];
-        float row_sum = 0.f;
+        tmem_ld_wait(sv);
+        uint32_t pk[16];
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2) {
-          float pv[2], dsv[2];
+          const int cl = 2 * e2, c = cbase + cl;
+          float2 bias = f2(g.bconst);
+          if (g.band)
+            bias = make_float2(bias_lookup(brow, g.rel0 + g.sgn * c, R),
+                               bias_lookup(brow, g.rel0 + g.sgn * (c + 1), R));
+          const float2 sval = make_float2(__uint_as_float(sv[cl]), __uint_as_float(sv[cl + 1]));
+          const bool v0 = !g.masked || (c >= g.lo && c < g.hi);
+          const bool v1 = !g.masked || (c + 1 >= g.lo && c + 1 < g.hi);
+          float2 pv, kv;
+          if constexpr (kSoftmax) {
+            const float2 x2 = __ffma2_rn(sval, f2(s2), __fmul2_rn(bias, f2(kLog2e)));
+            const float2 l2 = KV_MAJOR ? make_float2(lse_c[cl], lse_c[cl + 1]) : f2(lse2_row);
+            const float2 z = __fadd2_rn(x2, make_float2(-l2.x, -l2.y));
+            pv = make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
+            kv = pv;
+          } else {
+            const float2 hx = __ffma2_rn(sval, f2(hs), __fmul2_rn(bias, f2(0.5f)));
+            // one 16-column group of the 64 owned columns takes the ALU route
+            if (chunk == 1 && e2 >= 8) pv = act2_d<ACT, true>(hx, kv);
+            else pv = act2_d<ACT, false>(hx, kv);
+          }
+          if (!v0) {
+            pv.x = 0.f;
+            kv.x = 0.f;
+          }
+          if (!v1) {
+            pv.y = 0.f;
+            kv.y = 0.f;
+          }
+          keep[32 * chunk + cl] = kv.x;
+          keep[32 * chunk + cl + 1] = kv.y;
+          pk[e2] = pack_bf16(pv.x, pv.y);
+        }
+        if constexpr (KV_MAJOR) tmem_st16(t_s + 16 * chunk, pk);  // P^T over S^T columns already read
+      }
+      if constexpr (KV_MAJOR) {
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);
+      }
+
+      // ---- phase B: dP -> dS (bf16 into TMEM), dbias partial sums
+      if (!(ok = mbar_wait(&bars->dp_full, dp_it & 1, fail))) break;
+      ++dp_it;
+      tc_fence_after();
+      float row_sum = 0.f;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cl = 2 * e2 + e;
-            const int c = cbase + cl;
-            const int rel = KV_MAJOR ? rel0 + c : rel0 - c;
-            float bias = 0.f;
-            if (has_bias) bias = band ? bias_val(brow, rel, R) : bconst;
-            const float sval = __uint_as_float(sv[cl]);
-            float dp = __uint_as_float(dpv[cl]);
-            float pval, ds;
-            if constexpr (kSoftmax) {
-              const float x2 = __fmaf_rn(sval, p.scale * kLog2e, bias * kLog2e);
-              const float lse2 = KV_MAJOR ? lse_c[cl] : lse2_row;
-              const float dl = KV_MAJOR ? del_c[cl] : delta_row;
-              pval = ex2_sfu(x2 - lse2);
-              ds = pval * (dp - dl);
-            } else {
-              const float x = __fmaf_rn(sval, p.scale, bias);
-              float da;
-              pval = (chunk == 1 && e2 >= 8) ? act_val_d<ACT, true>(x, da) : act_val_d<ACT, false>(x, da);
-              ds = dp * da;
-            }
-            if (tile_masked_any && (c < lo || c >= hi)) {
-              pval = 0.f;
-              ds = 0.f;
-            }
-            pv[e] = pval;
-            dsv[e] = ds;
-            if (want_dbias) {
-              if (band) {
-                if (rel >= R) acc_hi += ds;
-                else if (rel <= -R) acc_lo += ds;
-                else atomicAdd(sbias + rel + R, ds);
-              } else {
-                row_sum += ds;
+      for (int chunk = 0; chunk < 2; ++chunk) {
+        const int cbase = 64 * half + 32 * chunk;
+        uint32_t dv[32];
+        tmem_ld32(t_dp + 32 * chunk, dv);
+        float del_c[32];
+        if constexpr (kSoftmax && KV_MAJOR) {
+          const int64_t q0 = static_cast<int64_t>(u.h) * p.total_q + u.seg.q0 + pt * kTile + cbase;
+          const int lim = max(0, min(32, u.seg.lq - pt * kTile - cbase));
+#pragma unroll
+          for (int e = 0; e < 32; ++e) del_c[e] = e < lim ? __ldg(p.delta + q0 + e) : 0.f;
+        }
+        tmem_ld_wait(dv);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e2 = 0; e2 < 16; ++e2) {
+          const int cl = 2 * e2, c = cbase + cl;
+          const float2 dp = make_float2(__uint_as_float(dv[cl]), __uint_as_float(dv[cl + 1]));
+          const float2 kv = make_float2(keep[32 * chunk + cl], keep[32 * chunk + cl + 1]);
+          float2 ds;
+          if constexpr (kSoftmax) {
+            const float2 dl = KV_MAJOR ? make_float2(del_c[cl], del_c[cl + 1]) : f2(delta_row);
+            ds = __fmul2_rn(kv, __fadd2_rn(dp, make_float2(-dl.x, -dl.y)));
+          } else {
+            ds = __fmul2_rn(dp, kv);
+          }
+          pk[e2] = pack_bf16(ds.x, ds.y);
+          if (want_dbias) {
+            if (g.band) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int rel = g.rel0 + (c + e);
+                const float v = e ? ds.y : ds.x;
+                if (rel >= R) acc_hi += v;
+                else if (rel <= -R) acc_lo += v;
+                else atomicAdd(sbias + rel + R, v);
               }
+            } else {
+              row_sum += ds.x + ds.y;
             }
           }
-          pk_p[e2] = pack_bf16(pv[0], pv[1]);
-          pk_ds[e2] = pack_bf16(dsv[0], dsv[1]);
         }
-        if (want_dbias && !band) {
-          if (relmin >= R) acc_hi += row_sum;
-          else acc_lo += row_sum;
-        }
-        if constexpr (KV_MAJOR) {
-          tmem_st16(t_s + 16 * chunk, pk_p);     // P^T over S^T columns already read
-          tmem_st16(t_dp + 16 * chunk, pk_ds);   // dS^T over dP^T columns already read
-        } else {
-          tmem_st16(t_s + 16 * chunk, pk_ds);    // dS over S columns already read
-        }
+        // dS^T over dP^T columns (dkdv) / dS over S columns (dq), already read
+        tmem_st16((KV_MAJOR ? t_dp : t_s) + 16 * chunk, pk);
+      }
+      if (want_dbias && !g.band) {
+        if (g.upper) acc_hi += row_sum;  // the whole tile clamps to one end of the table
+        else acc_lo += row_sum;
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive(&bars->ds_full);
     }
     if (!ok) break;
 
@@ -433,7 +552,8 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * p.scale, __uint_as_float(o[c + 2 * e + 1]) * p.scale);
+              w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * p.scale,
+                               __uint_as_float(o[c + 2 * e + 1]) * p.scale);
             st_global_v4(dst + c0 + c, w[0], w[1], w[2], w[3]);
           }
         }
@@ -481,8 +601,11 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     mbar_init(&bars->res_full, 1);
     mbar_init(&bars->res_empty, 1);
-    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 256);
     mbar_init(&bars->drain, 1);
@@ -514,7 +637,10 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
     if (lane == 0) bwd_producer<D, KV_MAJOR>(p, smem, bars, n_units, fail);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) bwd_mma<D, KV_MAJOR>(p, smem, bars, tmem, n_units, fail);
+    if (lane == 0) {
+      if constexpr (KV_MAJOR) bwd_mma_kv<D>(p, smem, bars, tmem, n_units, fail);
+      else bwd_mma_q<D>(p, smem, bars, tmem, n_units, fail);
+    }
     __syncwarp();
   } else if (warp >= 4) {
     bwd_act<D, ACT, KV_MAJOR>(p, smem, bars, tmem, n_units, fail);

@@ -32,6 +32,13 @@
 
 namespace jg {
 
+// Number of the four 32-column chunks of every S tile whose activation takes
+// the ALU route (the rest use the special-function unit).
+#ifndef JGDPA_FWD_ALU_CHUNKS
+#define JGDPA_FWD_ALU_CHUNKS 1
+#endif
+constexpr int kFwdAluChunks = JGDPA_FWD_ALU_CHUNKS;
+
 template <int D>
 struct FwdCfg {
   static constexpr int kBlockCols = D < 64 ? D : 64;      // bf16 columns per swizzle row
@@ -255,47 +262,146 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
 }
 
 // ------------------------------------------------------ activation warps
-// Bias of one element: table index clamp(rel, -R, R) + R = clamp(base - c, 0, 2R)
-// with base = i - j0 + R for the thread's row i and the tile's first key j0.
-struct BiasTile {
-  int mode;      // 0 none, 1 constant, 2 per element
-  float value;   // mode 1
-  int base;      // mode 2
-  int top;       // 2R
-  const float* row;  // this head's table
+// Per tile, the thread of row r (query i = i0 + r) and column c (key
+// j = j0 + c) has rel = i - j = (i0 - j0) + r - c and bias index
+// clamp(rel, -R, R) + R = clamp(base - c, 0, 2R) with base = i0 - j0 + r + R.
+// A tile whose rel range lies wholly at or beyond +-R uses one constant, so
+// only the few tiles near the diagonal look the table up per element.
+struct TileBias {
+  bool band;          // per-element lookups needed
+  float value;        // the constant otherwise (0 without a table)
+  int base;           // base for band tiles
+  int top;            // 2R
+  const float* row;   // this head's table
 };
 
-__device__ __forceinline__ BiasTile bias_tile(const FwdParams& p, int h, int i0, int r, int j0) {
-  BiasTile t;
-  t.mode = 0;
-  t.value = 0.f;
-  t.base = 0;
-  t.top = p.bias_len - 1;
-  t.row = nullptr;
+__device__ __forceinline__ TileBias tile_bias(const FwdParams& p, int h, int i0, int r, int j0) {
+  TileBias t{false, 0.f, 0, p.bias_len - 1, nullptr};
   if (p.bias_len == 0) return t;
   const int R = (p.bias_len - 1) / 2;
-  const int delta = i0 - j0;  // rel = delta + r - c, r, c in [0, 128)
+  const int delta = i0 - j0;
   t.row = p.bias + static_cast<int64_t>(h) * p.bias_len;
   if (delta - (kTile - 1) >= R) {
-    t.mode = 1;
     t.value = __ldg(t.row + 2 * R);
   } else if (delta + (kTile - 1) <= -R) {
-    t.mode = 1;
     t.value = __ldg(t.row);
   } else {
-    t.mode = 2;
+    t.band = true;
     t.base = delta + r + R;
   }
   return t;
 }
 
-__device__ __forceinline__ float bias_at(const BiasTile& t, int c) {
-  if (t.mode == 0) return 0.f;
-  if (t.mode == 1) return t.value;
-  return ld_nc_f32(t.row + min(max(t.base - c, 0), t.top));
+__device__ __forceinline__ float2 band_bias2(const TileBias& tb, int c, float mul) {
+  return make_float2(mul * ld_nc_f32(tb.row + min(max(tb.base - c, 0), tb.top)),
+                     mul * ld_nc_f32(tb.row + min(max(tb.base - c - 1, 0), tb.top)));
 }
 
-template <int D, int ACT>
+// S (fp32, TMEM) -> P = act(s S + bias) (bf16, over the same TMEM columns)
+// for one 128 x 128 tile, GELU / SiLU, two columns per packed instruction.
+// The last NALU of the four 32-column chunks take the ALU route.  MASKED:
+// columns >= nvalid (the subtraction-scheme count) get P = act(0) = 0.
+template <int ACT, int NALU, bool BAND, bool MASKED>
+__device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias& tb, int nvalid) {
+  const float hb = 0.5f * tb.value;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t a[32], b[32];
+    tmem_ld32(t_s + half * 64, a);
+    tmem_ld32(t_s + half * 64 + 32, b);
+    tmem_ld_wait2(a, b);
+    uint32_t pk[32];
+#pragma unroll
+    for (int c2 = 0; c2 < 32; ++c2) {
+      const int cl = 2 * c2, c = half * 64 + cl;
+      const float2 sv = cl < 32 ? make_float2(__uint_as_float(a[cl]), __uint_as_float(a[cl + 1]))
+                                : make_float2(__uint_as_float(b[cl - 32]), __uint_as_float(b[cl - 31]));
+      const float2 bias = BAND ? band_bias2(tb, c, 0.5f) : f2(hb);
+      float2 hx = __ffma2_rn(sv, f2(hs), bias);  // x / 2
+      if (MASKED) {
+        if (c >= nvalid) hx.x = 0.f;
+        if (c + 1 >= nvalid) hx.y = 0.f;
+      }
+      float2 y;
+      if (c >= kTile - 32 * NALU) y = act2<ACT, true>(hx);
+      else y = act2<ACT, false>(hx);
+      pk[c2] = pack_bf16(y.x, y.y);
+    }
+    tmem_st32(t_s + half * 32, pk);
+  }
+}
+
+// Softmax tile (base 2): x2 = (s S + bias) log2 e, row maximum, lazy rescale
+// of O (only when the maximum grows by more than 8, i.e. a factor 256),
+// P = 2^(x2 - m) over the S columns, running row sum.
+template <int D, bool BAND, bool MASKED>
+__device__ __forceinline__ void tile_softmax(uint32_t t_s, uint32_t t_o, float scale2, const TileBias& tb,
+                                             int nvalid, bool first, float& m_run, float& l_run) {
+  uint32_t a[32], b[32], c3[32], d4[32];
+  tmem_ld32(t_s, a);
+  tmem_ld32(t_s + 32, b);
+  tmem_ld_wait2(a, b);
+  tmem_ld32(t_s + 64, c3);
+  tmem_ld32(t_s + 96, d4);
+  tmem_ld_wait2(c3, d4);
+  const float b2 = kLog2e * tb.value;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    uint32_t& r0 = c < 32 ? a[c] : c < 64 ? b[c - 32] : c < 96 ? c3[c - 64] : d4[c - 96];
+    uint32_t& r1 = c < 32 ? a[c + 1] : c < 64 ? b[c - 31] : c < 96 ? c3[c - 63] : d4[c - 95];
+    const float2 bias = BAND ? band_bias2(tb, c, kLog2e) : f2(b2);
+    float2 x = __ffma2_rn(make_float2(__uint_as_float(r0), __uint_as_float(r1)), f2(scale2), bias);
+    if (MASKED) {
+      if (c >= nvalid) x.x = -INFINITY;
+      if (c + 1 >= nvalid) x.y = -INFINITY;
+    }
+    r0 = __float_as_uint(x.x);
+    r1 = __float_as_uint(x.y);
+    mx = fmaxf(mx, fmaxf(x.x, x.y));
+  }
+  const bool grow_max = mx > m_run + 8.0f;
+  const float m_new = grow_max ? mx : m_run;
+  const float factor = grow_max ? ex2_sfu(m_run - m_new) : 1.0f;  // ex2(-inf) = 0 on the first tile
+  l_run *= factor;
+  m_run = m_new;
+  float2 lsum = f2(0.f);
+  const float2 neg_m = f2(-m_run);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t(&src)[32] = q == 0 ? a : q == 1 ? b : q == 2 ? c3 : d4;
+    uint32_t pk[16];
+#pragma unroll
+    for (int c2 = 0; c2 < 16; ++c2) {
+      const float2 z =
+          __fadd2_rn(make_float2(__uint_as_float(src[2 * c2]), __uint_as_float(src[2 * c2 + 1])), neg_m);
+      const float2 pv = make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
+      lsum = __fadd2_rn(lsum, pv);
+      pk[c2] = pack_bf16(pv.x, pv.y);
+    }
+    tmem_st16(t_s + 16 * q, pk);  // P columns [16q, 16q+16) lie in S columns already read
+  }
+  l_run += lsum.x + lsum.y;
+  // O holds every earlier tile's P V (complete: it was issued before this
+  // tile's S), so it can be rescaled in place before P is released.
+  if (!first && __any_sync(0xffffffffu, grow_max)) {
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t o[32];
+      tmem_ld32(t_o + c0, o);
+      tmem_ld_wait(o);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2(factor));
+        o[i] = __float_as_uint(v.x);
+        o[i + 1] = __float_as_uint(v.y);
+      }
+      tmem_st32(t_o + c0, o);
+    }
+  }
+}
+
+template <int D, int ACT, int NALU>
 __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int slot, int n_units, Fail fail) {
   constexpr bool kSoftmax = ACT == 2;
   const int warp = threadIdx.x >> 5;
@@ -336,83 +442,24 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
       int nvalid = min(kTile, u.seg.lkv - j0);
       if (p.causal) nvalid = min(nvalid, t * kTile + r - j0 + 1);
       const bool tile_masked = (u.seg.lkv - j0 < kTile) || (p.causal && kt == t);
-      const BiasTile bt = bias_tile(p, u.h, t * kTile, r, j0);
-
+      const TileBias tb = tile_bias(p, u.h, t * kTile, r, j0);
       if constexpr (!kSoftmax) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t a[32], b[32];
-          tmem_ld32(t_s + half * 64, a);
-          tmem_ld32(t_s + half * 64 + 32, b);
-          tmem_ld_wait2(a, b);
-          uint32_t pk[32];
-#pragma unroll
-          for (int c2 = 0; c2 < 32; ++c2) {
-            float v2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int cl = 2 * c2 + e;  // column within the half
-              const int c = half * 64 + cl;
-              const uint32_t raw = cl < 32 ? a[cl] : b[cl - 32];
-              float x = __fmaf_rn(__uint_as_float(raw), p.scale, bias_at(bt, c));
-              if (tile_masked && c >= nvalid) x = 0.f;  // act(0) = 0
-              // one chunk of 32 columns out of four goes through the ALU route
-              v2[e] = (half == 1 && cl >= 32) ? act_val<ACT, true>(x) : act_val<ACT, false>(x);
-            }
-            pk[c2] = pack_bf16(v2[0], v2[1]);
-          }
-          tmem_st32(t_s + half * 32, pk);
+        const float hs = 0.5f * p.scale;
+        if (tb.band) {
+          if (tile_masked) tile_act<ACT, NALU, true, true>(t_s, hs, tb, nvalid);
+          else tile_act<ACT, NALU, true, false>(t_s, hs, tb, nvalid);
+        } else {
+          if (tile_masked) tile_act<ACT, NALU, false, true>(t_s, hs, tb, nvalid);
+          else tile_act<ACT, NALU, false, false>(t_s, hs, tb, nvalid);
         }
       } else {
-        uint32_t a[32], b[32], c3[32], d4[32];
-        tmem_ld32(t_s, a);
-        tmem_ld32(t_s + 32, b);
-        tmem_ld_wait2(a, b);
-        tmem_ld32(t_s + 64, c3);
-        tmem_ld32(t_s + 96, d4);
-        tmem_ld_wait2(c3, d4);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          uint32_t& raw = c < 32 ? a[c] : c < 64 ? b[c - 32] : c < 96 ? c3[c - 64] : d4[c - 96];
-          float x = __fmaf_rn(__uint_as_float(raw), p.scale, kLog2e * bias_at(bt, c));
-          if (tile_masked && c >= nvalid) x = -INFINITY;
-          raw = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-        // Rescale only when the maximum grows by more than 8 (a factor 256).
-        const bool grow_max = mx > m_run + 8.0f;
-        const float m_new = grow_max ? mx : m_run;
-        const float factor = grow_max ? ex2_sfu(m_run - m_new) : 1.0f;  // ex2(-inf) = 0 on the first tile
-        l_run *= factor;
-        m_run = m_new;
-        float lsum = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t(&src)[32] = q == 0 ? a : q == 1 ? b : q == 2 ? c3 : d4;
-          uint32_t pk[16];
-#pragma unroll
-          for (int c2 = 0; c2 < 16; ++c2) {
-            const float p0 = ex2_sfu(__uint_as_float(src[2 * c2]) - m_run);
-            const float p1 = ex2_sfu(__uint_as_float(src[2 * c2 + 1]) - m_run);
-            lsum += p0 + p1;
-            pk[c2] = pack_bf16(p0, p1);
-          }
-          tmem_st16(t_s + 16 * q, pk);  // P columns [16q, 16q+16) lie in S columns already read
-        }
-        l_run += lsum;
-        // O holds every earlier tile's P V (complete: it was issued before this
-        // tile's S), so it can be rescaled in place before P is released.
-        if (kt > 0 && __any_sync(0xffffffffu, grow_max)) {
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c0, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-            tmem_st32(t_o + c0, o);
-          }
+        const bool first = kt == 0;
+        if (tb.band) {
+          if (tile_masked) tile_softmax<D, true, true>(t_s, t_o, p.scale, tb, nvalid, first, m_run, l_run);
+          else tile_softmax<D, true, false>(t_s, t_o, p.scale, tb, nvalid, first, m_run, l_run);
+        } else {
+          if (tile_masked) tile_softmax<D, false, true>(t_s, t_o, p.scale, tb, nvalid, first, m_run, l_run);
+          else tile_softmax<D, false, false>(t_s, t_o, p.scale, tb, nvalid, first, m_run, l_run);
         }
       }
       tmem_st_wait();
@@ -449,7 +496,7 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
 }
 
 // ----------------------------------------------------------------- kernel
-template <int D, int ACT>
+template <int D, int ACT, int NALU>
 __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -495,7 +542,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
     if (lane == 0) fwd_mma<D>(p, smem, bars, tmem, n_units, fail);
     __syncwarp();
   } else if (warp >= 4) {
-    fwd_act<D, ACT>(p, bars, tmem, (warp - 4) >> 2, n_units, fail);
+    fwd_act<D, ACT, NALU>(p, bars, tmem, (warp - 4) >> 2, n_units, fail);
   }
   tc_fence_before();
   __syncthreads();
@@ -507,7 +554,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
 template <int D, int ACT>
 static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = gdpa_fwd_kernel<D, ACT>;
+  auto kern = gdpa_fwd_kernel<D, ACT, kFwdAluChunks>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, C::kSmemBytes, stream>>>(p);
