@@ -57,6 +57,30 @@ def flops(x) -> tuple[float, float]:
     return 4.0 * p * x.head_dim, 10.0 * p * x.head_dim
 
 
+def algorithmic_bytes(x) -> tuple[float, float]:
+    """Bytes that must cross HBM once: forward Q, K, V in and O out (+ LSE);
+    backward Q, K, V, dO in and dQ, dK, dV out (+ O, LSE and D for softmax,
+    + dbias)."""
+    tq, tkv = int(np.sum(x.lq)), int(np.sum(x.lkv))
+    row = 2 * x.heads * x.head_dim  # bytes of one bf16 row over all heads
+    softmax = x.act == "softmax"
+    fwd = (2 * tq + 2 * tkv) * row + (4 * x.heads * tq if softmax else 0)
+    bwd = (3 * tq + 4 * tkv) * row + ((tq * row + 12 * x.heads * tq) if softmax else 0) \
+        + 4 * x.heads * x.bias_len
+    return float(fwd), float(bwd)
+
+
+WORKLOAD_TEXT = {
+    1: "tiny jagged GDPA fwd+bwd: B=4, H=2, d=32, Lq~U[1,64], Lkv~U[1,48], SiLU, seed 0",
+    2: "JFA causal self-attention fwd+bwd: B=256, H=4, d=128, L~U[1,1024], softmax, seed 1",
+    3: "GDPA short-K/V cross-attention fwd+bwd: B=1024, H=4, d=128, Lq~U[1,2048], Lkv~U[32,128], GELU, "
+       "rel-pos bias 257, seed 2",
+    4: "PMA-style pooling fwd+bwd: B=512, H=8, d=64, Lq=16 shared seed queries, Lkv~U[1,4096], SiLU, seed 3",
+    5: "long-tail jagged GDPA fwd+bwd: B=64, H=8, d=128, L~round(LogNormal(ln 1500, 1)) clamped [100, 16384], "
+       "GELU, rel-pos bias 257, seed 4",
+}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -139,13 +163,22 @@ def barrier(world):
 
 
 def max_over_ranks(world, v: float) -> float:
+    """The maximum of v over all ranks (NCCL on GPUs, gloo on CPU)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(world: int, flop_per_rank: float, ms_per_step_local: float):
+    """Weak scaling: every rank runs its own batch; the job's step time is the
+    slowest rank's and the value counts the FLOPs of all ranks."""
+    ms = max_over_ranks(world, ms_per_step_local)
+    return ms, world * flop_per_rank / (ms * 1e-3) / 1e12
 
 
 def subset(x, n: int):
@@ -209,19 +242,22 @@ def run_native(args, world, rank, local):
     import jagged_gdpa_gb300 as jg
     import workloads
 
-    x = workloads.workload_inputs(WORKLOAD)
+    x = workloads.workload_inputs(args.workload)
     if args.segments:
         x = subset(x, args.segments)
     f_fwd, f_bwd = flops(x)
+    b_fwd, b_bwd = algorithmic_bytes(x)
     dev = torch.device("cuda", local)
     d = x.to(dev)
     stream = torch.cuda.current_stream(dev)
     total_q, heads, hd = x.q.shape
     total_kv = x.k.shape[0]
     bias_len = x.bias_len
+    softmax = x.act == "softmax"
     out = torch.empty_like(d.q)
+    lse = torch.empty((heads, total_q), dtype=torch.float32, device=dev) if softmax else None
     dq, dk, dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
-    dbias = torch.empty((heads, bias_len), dtype=torch.float32, device=dev)
+    dbias = torch.empty((heads, bias_len), dtype=torch.float32, device=dev) if bias_len else None
     ws_f = torch.empty(jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, False),
                        dtype=torch.uint8, device=dev)
     ws_b = torch.empty(jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, True),
@@ -229,13 +265,14 @@ def run_native(args, world, rank, local):
 
     def fwd():
         jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
-                     causal=x.causal, out=out, workspace=ws_f)
+                     causal=x.causal, out=out, lse=lse, workspace=ws_f)
 
     def bwd():
-        jg.jgdpa_bwd(d.q, d.k, d.v, out, None, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
+        jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
                      bias_table=d.bias, causal=x.causal, dq=dq, dk=dk, dv=dv, dbias=dbias, workspace=ws_b)
 
-    launches_per_step = 2 + 4  # (sched, fwd) + (sched, dK/dV, dQ, dbias reduce)
+    # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, dQ, [dbias reduce])
+    launches_per_step = 2 + 3 + int(softmax) + int(bias_len > 0)
     for _ in range(args.warmup):
         fwd()
         bwd()
@@ -263,27 +300,28 @@ def run_native(args, world, rank, local):
     ms_total = t_start.elapsed_time(t_end)
     ms_fwd = [e[0].elapsed_time(e[1]) for e in ev]
     ms_bwd = [e[1].elapsed_time(e[2]) for e in ev]
-    ms_step = max_over_ranks(world, ms_total / args.steps)
-    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    ms_step, value = aggregate(world, f_fwd + f_bwd, ms_total / args.steps)
 
     # end to end through the public API: pinned host inputs -> device, step,
     # results -> pinned host
-    host_in = {k: getattr(x, k).pin_memory() for k in ("q", "k", "v", "dout", "q_offsets", "kv_offsets", "bias")}
+    in_names = ["q", "k", "v", "dout", "q_offsets", "kv_offsets"] + (["bias"] if bias_len else [])
+    host_in = {k: getattr(x, k).pin_memory() for k in in_names}
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in
-                (("out", out), ("dq", dq), ("dk", dk), ("dv", dv), ("dbias", dbias))}
+    results = [("out", out), ("dq", dq), ("dk", dk), ("dv", dv)] + ([("dbias", dbias)] if bias_len else [])
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in results}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     def e2e_step():
         for k, v in host_in.items():
             dev_in[k].copy_(v, non_blocking=True)
-        o, _ = jg.jgdpa_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["q_offsets"], dev_in["kv_offsets"],
-                            x.act, x.scale, bias_table=dev_in["bias"], causal=x.causal, out=out, workspace=ws_f)
-        jg.jgdpa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, None, dev_in["dout"], dev_in["q_offsets"],
-                     dev_in["kv_offsets"], x.act, x.scale, bias_table=dev_in["bias"], causal=x.causal, dq=dq,
+        o, l2 = jg.jgdpa_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["q_offsets"], dev_in["kv_offsets"],
+                             x.act, x.scale, bias_table=dev_in.get("bias"), causal=x.causal, out=out, lse=lse,
+                             workspace=ws_f)
+        jg.jgdpa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, l2, dev_in["dout"], dev_in["q_offsets"],
+                     dev_in["kv_offsets"], x.act, x.scale, bias_table=dev_in.get("bias"), causal=x.causal, dq=dq,
                      dk=dk, dv=dv, dbias=dbias, workspace=ws_b)
-        for k, t in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv), ("dbias", dbias)):
+        for k, t in results:
             host_out[k].copy_(t, non_blocking=True)
 
     ms_e2e = float("nan")
@@ -321,16 +359,22 @@ def run_native(args, world, rank, local):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": "long-tail jagged GDPA fwd+bwd: B=64, H=8, d=128, L~round(LogNormal(ln 1500, 1)) "
-                        "clamped [100, 16384], GELU, rel-pos bias 257, seed 4",
+            "workload": WORKLOAD_TEXT[args.workload] + ("" if not args.segments else
+                                                        f" (first {args.segments} segments)"),
             "batch_segments": x.batch,
-            "total_tokens": int(total_q),
+            "total_q_tokens": int(total_q),
+            "total_kv_tokens": int(total_kv),
             "valid_pairs_x_heads": int(valid_pairs(x.lq, x.lkv, x.causal) * heads),
             "fwd_tflop_per_step": f_fwd / 1e12,
             "bwd_tflop_per_step": f_bwd / 1e12,
-            "l2": "inputs larger than L2 (1.2 GB of Q/K/V/dO per step vs 129 MB L2); no flush",
-            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "fwd_algorithmic_gb_per_step": b_fwd / 1e9,
+            "bwd_algorithmic_gb_per_step": b_bwd / 1e9,
+            "l2": (f"inputs larger than L2 ({(b_fwd + b_bwd) / 1e9:.2f} GB moved per step vs 129 MB L2); "
+                   "no flush") if b_fwd > 2.6e8 else "inputs smaller than 2x L2; numbers include L2 reuse",
+            "parallelism": f"independent batch per GPU x{world}" if world > 1 else "1 GPU",
         },
+        "fwd_gbs": round(b_fwd / (statistics.mean(ms_fwd) * 1e-3) / 1e9, 1),
+        "bwd_gbs": round(b_bwd / (statistics.mean(ms_bwd) * 1e-3) / 1e9, 1),
         "fwd_ms": round(fwd_ms, 4),
         "bwd_ms": round(bwd_ms, 4),
         "fwd_tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
@@ -373,7 +417,7 @@ def run_reference(args, world, rank):
     import oracle
     import workloads
     oracle.build()
-    x = workloads.workload_inputs(WORKLOAD)
+    x = workloads.workload_inputs(args.workload)
     budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(x, budget_s=budget, seed=1)
@@ -399,8 +443,8 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "long-tail jagged GDPA fwd+bwd (B=64, H=8, d=128, GELU, bias 257, seed 4); "
-                               "each step a bounded sample of its (segment, head) units"},
+        "config": {"workload": WORKLOAD_TEXT[args.workload] + "; each step a bounded sample of its "
+                                                             "(segment, head) units"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                          "sample": f"{n_units} units, {tot_pairs} valid pairs over {args.steps} steps"},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -417,6 +461,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) timing")
     ap.add_argument("--segments", type=int, default=0, help="use only the first N segments (profiling)")
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=sorted(WORKLOAD_TEXT),
+                    help="which of the five workloads (default: the long-tail one)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

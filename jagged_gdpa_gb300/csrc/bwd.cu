@@ -327,6 +327,92 @@ __device__ __forceinline__ float bias_lookup(const float* brow, int rel, int R) 
   return ld_nc_f32(brow + min(max(rel, -R), R) + R);
 }
 
+// Phase A on one 32-column chunk: x from S (+ bias), P (bf16, packed into pk)
+// and what phase B needs (act'(x), or P for softmax) into keep.  BAND and
+// MASKED are decided once per tile.  CHUNK 1's upper 16 columns take the ALU
+// route (GELU/SiLU).
+template <int ACT, bool KV_MAJOR, int CHUNK, bool BAND, bool MASKED>
+__device__ __forceinline__ void phase_a_chunk(const uint32_t (&sv)[32], const float (&lse_c)[32], float lse2_row,
+                                              const PairGeom& g, const float* brow, int R, int cbase, float hs,
+                                              float s2, float (&keep)[32], uint32_t (&pk)[16]) {
+  constexpr bool kSoftmax = ACT == 2;
+  const float hb = 0.5f * g.bconst;
+  const float b2 = kLog2e * g.bconst;
+#pragma unroll
+  for (int e2 = 0; e2 < 16; ++e2) {
+    const int cl = 2 * e2, c = cbase + cl;
+    const float2 sval = make_float2(__uint_as_float(sv[cl]), __uint_as_float(sv[cl + 1]));
+    float2 bias = f2(g.bconst);
+    if constexpr (BAND)
+      bias = make_float2(bias_lookup(brow, g.rel0 + g.sgn * c, R), bias_lookup(brow, g.rel0 + g.sgn * (c + 1), R));
+    float2 pv, kv;
+    if constexpr (kSoftmax) {
+      const float2 x2 = BAND ? __ffma2_rn(sval, f2(s2), __fmul2_rn(bias, f2(kLog2e))) : __ffma2_rn(sval, f2(s2), f2(b2));
+      const float2 l2 = KV_MAJOR ? make_float2(lse_c[cl], lse_c[cl + 1]) : f2(lse2_row);
+      const float2 z = __fadd2_rn(x2, make_float2(-l2.x, -l2.y));
+      pv = make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
+      kv = pv;
+    } else {
+      const float2 hx = BAND ? __ffma2_rn(sval, f2(hs), __fmul2_rn(bias, f2(0.5f))) : __ffma2_rn(sval, f2(hs), f2(hb));
+      if constexpr (CHUNK == 1) {
+        if (e2 >= 8) pv = act2_d<ACT, true>(hx, kv);
+        else pv = act2_d<ACT, false>(hx, kv);
+      } else {
+        pv = act2_d<ACT, false>(hx, kv);
+      }
+    }
+    if constexpr (MASKED) {
+      if (!(c >= g.lo && c < g.hi)) {
+        pv.x = 0.f;
+        kv.x = 0.f;
+      }
+      if (!(c + 1 >= g.lo && c + 1 < g.hi)) {
+        pv.y = 0.f;
+        kv.y = 0.f;
+      }
+    }
+    keep[cl] = kv.x;
+    keep[cl + 1] = kv.y;
+    pk[e2] = pack_bf16(pv.x, pv.y);
+  }
+}
+
+// Phase B on one 32-column chunk: dS = act'(x) dP (softmax: P (dP - D)),
+// packed into pk.  DBIAS: 0 none, 1 the tile clamps to one table end (sum
+// into row_sum), 2 per-element table entries (band tile).
+template <int ACT, bool KV_MAJOR, int DBIAS>
+__device__ __forceinline__ void phase_b_chunk(const uint32_t (&dv)[32], const float (&del_c)[32], float delta_row,
+                                              const float (&keep)[32], const PairGeom& g, int R, int cbase,
+                                              float* sbias, float2& row_sum, float& acc_lo, float& acc_hi,
+                                              uint32_t (&pk)[16]) {
+  constexpr bool kSoftmax = ACT == 2;
+#pragma unroll
+  for (int e2 = 0; e2 < 16; ++e2) {
+    const int cl = 2 * e2, c = cbase + cl;
+    const float2 dp = make_float2(__uint_as_float(dv[cl]), __uint_as_float(dv[cl + 1]));
+    const float2 kv = make_float2(keep[cl], keep[cl + 1]);
+    float2 ds;
+    if constexpr (kSoftmax) {
+      const float2 dl = KV_MAJOR ? make_float2(del_c[cl], del_c[cl + 1]) : f2(delta_row);
+      ds = __fmul2_rn(kv, __fadd2_rn(dp, make_float2(-dl.x, -dl.y)));
+    } else {
+      ds = __fmul2_rn(dp, kv);
+    }
+    pk[e2] = pack_bf16(ds.x, ds.y);
+    if constexpr (DBIAS == 1) row_sum = __fadd2_rn(row_sum, ds);
+    if constexpr (DBIAS == 2) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int rel = g.rel0 + (c + e);
+        const float v = e ? ds.y : ds.x;
+        if (rel >= R) acc_hi += v;
+        else if (rel <= -R) acc_lo += v;
+        else atomicAdd(sbias + rel + R, v);
+      }
+    }
+  }
+}
+
 template <int D, int ACT, bool KV_MAJOR>
 __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units, Fail fail) {
   using C = BwdCfg<D>;
@@ -394,7 +480,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       tc_fence_after();
 
       // ---- phase A: S -> (P, act'(x)) [softmax: P]; P^T to TMEM (dkdv)
-      float keep[64];  // act'(x) (GELU/SiLU) or P (softmax) per owned column
+      float keep0[32], keep1[32];  // act'(x) (GELU/SiLU) or P (softmax) per owned column
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int cbase = 64 * half + 32 * chunk;
@@ -409,41 +495,23 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         }
         tmem_ld_wait(sv);
         uint32_t pk[16];
-#pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          const int cl = 2 * e2, c = cbase + cl;
-          float2 bias = f2(g.bconst);
-          if (g.band)
-            bias = make_float2(bias_lookup(brow, g.rel0 + g.sgn * c, R),
-                               bias_lookup(brow, g.rel0 + g.sgn * (c + 1), R));
-          const float2 sval = make_float2(__uint_as_float(sv[cl]), __uint_as_float(sv[cl + 1]));
-          const bool v0 = !g.masked || (c >= g.lo && c < g.hi);
-          const bool v1 = !g.masked || (c + 1 >= g.lo && c + 1 < g.hi);
-          float2 pv, kv;
-          if constexpr (kSoftmax) {
-            const float2 x2 = __ffma2_rn(sval, f2(s2), __fmul2_rn(bias, f2(kLog2e)));
-            const float2 l2 = KV_MAJOR ? make_float2(lse_c[cl], lse_c[cl + 1]) : f2(lse2_row);
-            const float2 z = __fadd2_rn(x2, make_float2(-l2.x, -l2.y));
-            pv = make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
-            kv = pv;
+        float(&keep)[32] = chunk == 0 ? keep0 : keep1;
+#define JG_PHASE_A(CH, BAND, MASKED)                                                                         \
+  phase_a_chunk<ACT, KV_MAJOR, CH, BAND, MASKED>(sv, lse_c, lse2_row, g, brow, R, cbase, hs, s2, keep, pk)
+        if (chunk == 0) {
+          if (g.band) {
+            if (g.masked) JG_PHASE_A(0, true, true); else JG_PHASE_A(0, true, false);
           } else {
-            const float2 hx = __ffma2_rn(sval, f2(hs), __fmul2_rn(bias, f2(0.5f)));
-            // one 16-column group of the 64 owned columns takes the ALU route
-            if (chunk == 1 && e2 >= 8) pv = act2_d<ACT, true>(hx, kv);
-            else pv = act2_d<ACT, false>(hx, kv);
+            if (g.masked) JG_PHASE_A(0, false, true); else JG_PHASE_A(0, false, false);
           }
-          if (!v0) {
-            pv.x = 0.f;
-            kv.x = 0.f;
+        } else {
+          if (g.band) {
+            if (g.masked) JG_PHASE_A(1, true, true); else JG_PHASE_A(1, true, false);
+          } else {
+            if (g.masked) JG_PHASE_A(1, false, true); else JG_PHASE_A(1, false, false);
           }
-          if (!v1) {
-            pv.y = 0.f;
-            kv.y = 0.f;
-          }
-          keep[32 * chunk + cl] = kv.x;
-          keep[32 * chunk + cl + 1] = kv.y;
-          pk[e2] = pack_bf16(pv.x, pv.y);
         }
+#undef JG_PHASE_A
         if constexpr (KV_MAJOR) tmem_st16(t_s + 16 * chunk, pk);  // P^T over S^T columns already read
       }
       if constexpr (KV_MAJOR) {
@@ -456,7 +524,8 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       if (!(ok = mbar_wait(&bars->dp_full, dp_it & 1, fail))) break;
       ++dp_it;
       tc_fence_after();
-      float row_sum = 0.f;
+      float2 row_sum = f2(0.f);
+      const int dmode = !want_dbias ? 0 : (g.band ? 2 : 1);
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int cbase = 64 * half + 32 * chunk;
@@ -471,40 +540,19 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         }
         tmem_ld_wait(dv);
         uint32_t pk[16];
-#pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          const int cl = 2 * e2, c = cbase + cl;
-          const float2 dp = make_float2(__uint_as_float(dv[cl]), __uint_as_float(dv[cl + 1]));
-          const float2 kv = make_float2(keep[32 * chunk + cl], keep[32 * chunk + cl + 1]);
-          float2 ds;
-          if constexpr (kSoftmax) {
-            const float2 dl = KV_MAJOR ? make_float2(del_c[cl], del_c[cl + 1]) : f2(delta_row);
-            ds = __fmul2_rn(kv, __fadd2_rn(dp, make_float2(-dl.x, -dl.y)));
-          } else {
-            ds = __fmul2_rn(dp, kv);
-          }
-          pk[e2] = pack_bf16(ds.x, ds.y);
-          if (want_dbias) {
-            if (g.band) {
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int rel = g.rel0 + (c + e);
-                const float v = e ? ds.y : ds.x;
-                if (rel >= R) acc_hi += v;
-                else if (rel <= -R) acc_lo += v;
-                else atomicAdd(sbias + rel + R, v);
-              }
-            } else {
-              row_sum += ds.x + ds.y;
-            }
-          }
-        }
+        const float(&keep)[32] = chunk == 0 ? keep0 : keep1;
+        if (dmode == 0)
+          phase_b_chunk<ACT, KV_MAJOR, 0>(dv, del_c, delta_row, keep, g, R, cbase, sbias, row_sum, acc_lo, acc_hi, pk);
+        else if (dmode == 1)
+          phase_b_chunk<ACT, KV_MAJOR, 1>(dv, del_c, delta_row, keep, g, R, cbase, sbias, row_sum, acc_lo, acc_hi, pk);
+        else
+          phase_b_chunk<ACT, KV_MAJOR, 2>(dv, del_c, delta_row, keep, g, R, cbase, sbias, row_sum, acc_lo, acc_hi, pk);
         // dS^T over dP^T columns (dkdv) / dS over S columns (dq), already read
         tmem_st16((KV_MAJOR ? t_dp : t_s) + 16 * chunk, pk);
       }
-      if (want_dbias && !g.band) {
-        if (g.upper) acc_hi += row_sum;  // the whole tile clamps to one end of the table
-        else acc_lo += row_sum;
+      if (dmode == 1) {
+        if (g.upper) acc_hi += row_sum.x + row_sum.y;  // the whole tile clamps to one end of the table
+        else acc_lo += row_sum.x + row_sum.y;
       }
       tmem_st_wait();
       tc_fence_before();

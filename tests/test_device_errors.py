@@ -1,0 +1,91 @@
+"""Errors only the device can see: corrupt offsets are found by the scheduling
+kernel, recorded in the workspace status word and turn the remaining kernels
+into no-ops (the outputs keep their previous contents).  Nothing here can
+fault: every kernel checks the status before touching memory."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def jg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import jagged_gdpa_gb300 as m
+    return m
+
+
+def _bad_inputs(kind):
+    x = workloads.random_case(5, batch=4, heads=2, head_dim=64, act="gelu", lq_range=(10, 200),
+                              lkv_range=(10, 200), bias_len=7)
+    qo = x.q_offsets.clone()
+    if kind == "non_monotone":
+        qo[2] = qo[3] + 5          # segment 2 ends before it starts
+    elif kind == "wrong_end":
+        qo[-1] = qo[-1] - 1        # offsets[B] != total_q
+    elif kind == "nonzero_start":
+        qo[0] = 1
+    return x, qo
+
+
+@pytest.mark.parametrize("kind", ["non_monotone", "wrong_end", "nonzero_start"])
+def test_bad_offsets_reported_and_outputs_untouched(jg, kind):
+    x, qo = _bad_inputs(kind)
+    d = x.to("cuda")
+    qo = qo.cuda()
+    total_q, heads, hd = x.q.shape
+    nbytes = jg.jgdpa_workspace_bytes(x.batch, total_q, x.k.shape[0], heads, hd, x.act, x.bias_len, False)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.full_like(d.q, 7.0)
+    jg.jgdpa_fwd(d.q, d.k, d.v, qo, d.kv_offsets, x.act, x.scale, bias_table=d.bias, out=out, workspace=ws)
+    assert jg.jgdpa_read_device_status(ws) == 6  # JGDPA_ERR_BAD_OFFSETS
+    assert torch.all(out == 7.0)
+    nb = jg.jgdpa_workspace_bytes(x.batch, total_q, x.k.shape[0], heads, hd, x.act, x.bias_len, True)
+    wsb = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    dq = torch.full_like(d.q, 3.0)
+    dk = torch.full_like(d.k, 3.0)
+    dv = torch.full_like(d.v, 3.0)
+    jg.jgdpa_bwd(d.q, d.k, d.v, None, None, d.dout, qo, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
+                 dq=dq, dk=dk, dv=dv, workspace=wsb)
+    assert jg.jgdpa_read_device_status(wsb) == 6
+    assert torch.all(dq == 3.0) and torch.all(dk == 3.0) and torch.all(dv == 3.0)
+
+
+def test_status_clears_on_the_next_good_call(jg):
+    x, qo = _bad_inputs("non_monotone")
+    d = x.to("cuda")
+    total_q, heads, hd = x.q.shape
+    nbytes = jg.jgdpa_workspace_bytes(x.batch, total_q, x.k.shape[0], heads, hd, x.act, x.bias_len, False)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    jg.jgdpa_fwd(d.q, d.k, d.v, qo.cuda(), d.kv_offsets, x.act, x.scale, bias_table=d.bias, workspace=ws)
+    assert jg.jgdpa_read_device_status(ws) == 6
+    out, _ = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
+                          workspace=ws)
+    assert jg.jgdpa_read_device_status(ws) == 0
+    assert torch.isfinite(out.float()).all()
+
+
+def test_workspace_too_small_is_rejected_before_launch(jg):
+    x = workloads.random_case(6, batch=2, heads=1, head_dim=32, act="silu")
+    d = x.to("cuda")
+    ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(jg.JgdpaError) as e:
+        jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, workspace=ws)
+    assert e.value.code == 4
+
+
+def test_misaligned_pointer_is_rejected(jg):
+    x = workloads.random_case(7, batch=2, heads=1, head_dim=32, act="silu", lq_range=(4, 9))
+    d = x.to("cuda")
+    flat = torch.empty(d.q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    q_mis = flat[1:1 + d.q.numel()].view_as(d.q)  # 2-byte offset from a 16-byte boundary
+    q_mis.copy_(d.q)
+    with pytest.raises(jg.JgdpaError) as e:
+        jg.jgdpa_fwd(q_mis, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale)
+    assert e.value.code == 3
+    del np
