@@ -33,6 +33,14 @@
 
 namespace jg {
 
+// Number of the four 16-column groups that each activation thread owns per
+// tile whose act / act' take the ALU route (the rest use the
+// special-function unit).
+#ifndef JGDPA_BWD_ALU_GROUPS
+#define JGDPA_BWD_ALU_GROUPS 1
+#endif
+constexpr int kBwdAluGroups = JGDPA_BWD_ALU_GROUPS;
+
 template <int D>
 struct BwdCfg {
   static constexpr int kBlockCols = D < 64 ? D : 64;
@@ -177,7 +185,12 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
 }
 
 // ---------------------------------------------------------------- MMA issuer
-// dkdv, per query tile: S^T, dP^T, [P^T ready] dV, [dS^T ready] dK.
+// dkdv.  Issue order over query tiles i:
+//   S^T(0), dP^T(0), { [P^T(i) ready] dV(i), S^T(i+1), [dS^T(i) ready] dK(i),
+//   dP^T(i+1) }
+// S^T(i+1) may follow dV(i) (which has consumed P^T(i) from the same TMEM
+// columns) and dP^T(i+1) follows dK(i) (which has consumed dS^T(i)), so the
+// activation warps get two MMAs of slack for each phase.
 template <int D>
 __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                            Fail fail) {
@@ -193,7 +206,7 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
     if (u.count == 0) continue;
     if (!(ok = mbar_wait(&bars->res_full, res_it & 1, fail))) break;
     ++res_it;
-    for (int i = 0; i < u.count; ++i) {
+    {  // S^T and dP^T of the first query tile
       const int st = st_it % C::kStages;
       const uint32_t q_t = str_base + st * 2 * C::kTileBytes, do_t = q_t + C::kTileBytes;
       if (!(ok = mbar_wait(&bars->st_full[st], (st_it / C::kStages) & 1, fail))) break;
@@ -202,6 +215,14 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
       mma_commit(&bars->s_full[0]);
       mma_tile_nt<D>(tmem + 128, v_t, do_t);  // dP^T = V  dO^T
       mma_commit(&bars->dp_full);
+    }
+    for (int i = 0; i < u.count; ++i) {
+      const uint32_t it = st_it + i;
+      const int st = it % C::kStages;
+      const uint32_t q_t = str_base + st * 2 * C::kTileBytes, do_t = q_t + C::kTileBytes;
+      const bool more = i + 1 < u.count;
+      const int st1 = (it + 1) % C::kStages;
+      const uint32_t q1 = str_base + st1 * 2 * C::kTileBytes, do1 = q1 + C::kTileBytes;
       if (i == 0) {
         if (!(ok = mbar_wait(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
         ++acc_it;
@@ -209,17 +230,26 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
       if (!(ok = mbar_wait(&bars->p_full, p_it & 1, fail))) break;
       tc_fence_after();
       mma_tile_tn<D>(tmem + 256, tmem + 0, tmem + 64, do_t, i > 0);  // dV += P^T dO
+      if (more) {
+        if (!(ok = mbar_wait(&bars->st_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
+        tc_fence_after();
+        mma_tile_nt<D>(tmem, k_t, q1);  // S^T of the next query tile
+        mma_commit(&bars->s_full[0]);
+      }
       if (!(ok = mbar_wait(&bars->ds_full, p_it & 1, fail))) break;
       ++p_it;
       tc_fence_after();
       mma_tile_tn<D>(tmem + 256 + D, tmem + 128, tmem + 192, q_t, i > 0);  // dK += dS^T Q
       mma_commit(&bars->st_empty[st]);
-      ++st_it;
-      if (i == u.count - 1) {
-        mma_commit(&bars->acc_full);
-        mma_commit(&bars->res_empty);
+      if (more) {
+        mma_tile_nt<D>(tmem + 128, v_t, do1);  // dP^T of the next query tile
+        mma_commit(&bars->dp_full);
       }
     }
+    if (!ok) break;
+    st_it += u.count;
+    mma_commit(&bars->acc_full);
+    mma_commit(&bars->res_empty);
   }
   mma_commit(&bars->drain);
   mbar_wait_drain(&bars->drain, 0);
@@ -329,8 +359,8 @@ __device__ __forceinline__ float bias_lookup(const float* brow, int rel, int R) 
 
 // Phase A on one 32-column chunk: x from S (+ bias), P (bf16, packed into pk)
 // and what phase B needs (act'(x), or P for softmax) into keep.  BAND and
-// MASKED are decided once per tile.  CHUNK 1's upper 16 columns take the ALU
-// route (GELU/SiLU).
+// MASKED are decided once per tile; CHUNK (0 or 1) selects which of the
+// thread's 16-column groups take the ALU route (GELU/SiLU).
 template <int ACT, bool KV_MAJOR, int CHUNK, bool BAND, bool MASKED>
 __device__ __forceinline__ void phase_a_chunk(const uint32_t (&sv)[32], const float (&lse_c)[32], float lse2_row,
                                               const PairGeom& g, const float* brow, int R, int cbase, float hs,
@@ -354,12 +384,9 @@ __device__ __forceinline__ void phase_a_chunk(const uint32_t (&sv)[32], const fl
       kv = pv;
     } else {
       const float2 hx = BAND ? __ffma2_rn(sval, f2(hs), __fmul2_rn(bias, f2(0.5f))) : __ffma2_rn(sval, f2(hs), f2(hb));
-      if constexpr (CHUNK == 1) {
-        if (e2 >= 8) pv = act2_d<ACT, true>(hx, kv);
-        else pv = act2_d<ACT, false>(hx, kv);
-      } else {
-        pv = act2_d<ACT, false>(hx, kv);
-      }
+      // the last kBwdAluGroups of the four 16-column groups take the ALU route
+      if (CHUNK * 2 + (e2 >= 8 ? 1 : 0) >= 4 - kBwdAluGroups) pv = act2_d<ACT, true>(hx, kv);
+      else pv = act2_d<ACT, false>(hx, kv);
     }
     if constexpr (MASKED) {
       if (!(c >= g.lo && c < g.hi)) {

@@ -88,4 +88,3 @@ def test_misaligned_pointer_is_rejected(jg):
     with pytest.raises(jg.JgdpaError) as e:
         jg.jgdpa_fwd(q_mis, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale)
     assert e.value.code == 3
-    del np
