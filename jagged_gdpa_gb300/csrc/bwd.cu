@@ -37,7 +37,7 @@ namespace jg {
 // tile whose act / act' take the ALU route (the rest use the
 // special-function unit).
 #ifndef JGDPA_BWD_ALU_GROUPS
-#define JGDPA_BWD_ALU_GROUPS 1
+#define JGDPA_BWD_ALU_GROUPS 0
 #endif
 constexpr int kBwdAluGroups = JGDPA_BWD_ALU_GROUPS;
 

@@ -35,7 +35,7 @@ namespace jg {
 // Number of the four 32-column chunks of every S tile whose activation takes
 // the ALU route (the rest use the special-function unit).
 #ifndef JGDPA_FWD_ALU_CHUNKS
-#define JGDPA_FWD_ALU_CHUNKS 1
+#define JGDPA_FWD_ALU_CHUNKS 0
 #endif
 constexpr int kFwdAluChunks = JGDPA_FWD_ALU_CHUNKS;
 
