@@ -507,12 +507,16 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       tc_fence_after();
 
       // ---- phase A: S -> (P, act'(x)) [softmax: P]; P^T to TMEM (dkdv)
+      // (chunk 1's TMEM load is in flight while chunk 0 is computed and stored)
       float keep0[32], keep1[32];  // act'(x) (GELU/SiLU) or P (softmax) per owned column
+      uint32_t sv0[32], sv1[32];
+      tmem_ld32(t_s, sv0);
+      tmem_ld_wait(sv0);
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int cbase = 64 * half + 32 * chunk;
-        uint32_t sv[32];
-        tmem_ld32(t_s + 32 * chunk, sv);
+        if (chunk == 0) tmem_ld32(t_s + 32, sv1);
+        const uint32_t(&sv)[32] = chunk == 0 ? sv0 : sv1;
         float lse_c[32];
         if constexpr (kSoftmax && KV_MAJOR) {
           const int64_t q0 = static_cast<int64_t>(u.h) * p.total_q + u.seg.q0 + pt * kTile + cbase;
@@ -520,7 +524,6 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
 #pragma unroll
           for (int e = 0; e < 32; ++e) lse_c[e] = e < lim ? __ldg(p.lse + q0 + e) * kLog2e : 0.f;
         }
-        tmem_ld_wait(sv);
         uint32_t pk[16];
         float(&keep)[32] = chunk == 0 ? keep0 : keep1;
 #define JG_PHASE_A(CH, BAND, MASKED)                                                                         \
@@ -540,6 +543,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         }
 #undef JG_PHASE_A
         if constexpr (KV_MAJOR) tmem_st16(t_s + 16 * chunk, pk);  // P^T over S^T columns already read
+        if (chunk == 0) tmem_ld_wait(sv1);
       }
       if constexpr (KV_MAJOR) {
         tmem_st_wait();
@@ -553,11 +557,14 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       tc_fence_after();
       float2 row_sum = f2(0.f);
       const int dmode = !want_dbias ? 0 : (g.band ? 2 : 1);
+      uint32_t dv0[32], dv1[32];
+      tmem_ld32(t_dp, dv0);
+      tmem_ld_wait(dv0);
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int cbase = 64 * half + 32 * chunk;
-        uint32_t dv[32];
-        tmem_ld32(t_dp + 32 * chunk, dv);
+        if (chunk == 0) tmem_ld32(t_dp + 32, dv1);
+        const uint32_t(&dv)[32] = chunk == 0 ? dv0 : dv1;
         float del_c[32];
         if constexpr (kSoftmax && KV_MAJOR) {
           const int64_t q0 = static_cast<int64_t>(u.h) * p.total_q + u.seg.q0 + pt * kTile + cbase;
@@ -565,7 +572,6 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
 #pragma unroll
           for (int e = 0; e < 32; ++e) del_c[e] = e < lim ? __ldg(p.delta + q0 + e) : 0.f;
         }
-        tmem_ld_wait(dv);
         uint32_t pk[16];
         const float(&keep)[32] = chunk == 0 ? keep0 : keep1;
         if (dmode == 0)
@@ -576,6 +582,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
           phase_b_chunk<ACT, KV_MAJOR, 2>(dv, del_c, delta_row, keep, g, R, cbase, sbias, row_sum, acc_lo, acc_hi, pk);
         // dS^T over dP^T columns (dkdv) / dS over S columns (dq), already read
         tmem_st16((KV_MAJOR ? t_dp : t_s) + 16 * chunk, pk);
+        if (chunk == 0) tmem_ld_wait(dv1);
       }
       if (dmode == 1) {
         if (g.upper) acc_hi += row_sum.x + row_sum.y;  // the whole tile clamps to one end of the table

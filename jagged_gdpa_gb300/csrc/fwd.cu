@@ -301,21 +301,25 @@ __device__ __forceinline__ float2 band_bias2(const TileBias& tb, int c, float mu
 // for one 128 x 128 tile, GELU / SiLU, two columns per packed instruction.
 // The last NALU of the four 32-column chunks take the ALU route.  MASKED:
 // columns >= nvalid (the subtraction-scheme count) get P = act(0) = 0.
+// The four 32-column chunks are software-pipelined: the TMEM load of chunk
+// q + 1 is in flight while chunk q is computed and its P stored (P of chunk q
+// lands in columns [16q, 16q + 16), all read already).
 template <int ACT, int NALU, bool BAND, bool MASKED>
 __device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias& tb, int nvalid) {
   const float hb = 0.5f * tb.value;
+  uint32_t buf0[32], buf1[32];
+  tmem_ld32(t_s, buf0);
+  tmem_ld_wait(buf0);
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t a[32], b[32];
-    tmem_ld32(t_s + half * 64, a);
-    tmem_ld32(t_s + half * 64 + 32, b);
-    tmem_ld_wait2(a, b);
-    uint32_t pk[32];
+  for (int q = 0; q < 4; ++q) {
+    uint32_t(&cur)[32] = (q & 1) ? buf1 : buf0;
+    uint32_t(&nxt)[32] = (q & 1) ? buf0 : buf1;
+    if (q < 3) tmem_ld32(t_s + 32 * (q + 1), nxt);
+    uint32_t pk[16];
 #pragma unroll
-    for (int c2 = 0; c2 < 32; ++c2) {
-      const int cl = 2 * c2, c = half * 64 + cl;
-      const float2 sv = cl < 32 ? make_float2(__uint_as_float(a[cl]), __uint_as_float(a[cl + 1]))
-                                : make_float2(__uint_as_float(b[cl - 32]), __uint_as_float(b[cl - 31]));
+    for (int c2 = 0; c2 < 16; ++c2) {
+      const int c = 32 * q + 2 * c2;
+      const float2 sv = make_float2(__uint_as_float(cur[2 * c2]), __uint_as_float(cur[2 * c2 + 1]));
       const float2 bias = BAND ? band_bias2(tb, c, 0.5f) : f2(hb);
       float2 hx = __ffma2_rn(sv, f2(hs), bias);  // x / 2
       if (MASKED) {
@@ -323,11 +327,12 @@ __device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias&
         if (c + 1 >= nvalid) hx.y = 0.f;
       }
       float2 y;
-      if (c >= kTile - 32 * NALU) y = act2<ACT, true>(hx);
+      if (q >= 4 - NALU) y = act2<ACT, true>(hx);
       else y = act2<ACT, false>(hx);
       pk[c2] = pack_bf16(y.x, y.y);
     }
-    tmem_st32(t_s + half * 32, pk);
+    tmem_st16(t_s + 16 * q, pk);
+    if (q < 3) tmem_ld_wait(nxt);
   }
 }
 
