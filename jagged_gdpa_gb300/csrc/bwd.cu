@@ -41,21 +41,32 @@ namespace jg {
 #endif
 constexpr int kBwdAluGroups = JGDPA_BWD_ALU_GROUPS;
 
+// Layout of one swizzled [128][D] bf16 tile in shared memory.
 template <int D>
-struct BwdCfg {
+struct TileCfg {
   static constexpr int kBlockCols = D < 64 ? D : 64;
   static constexpr int kRowBytes = kBlockCols * 2;
   static constexpr int kBlockBytes = kTile * kRowBytes;
   static constexpr int kNumBlocks = D / kBlockCols;
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
   static constexpr uint32_t kSwizzle = kRowBytes == 128 ? 2u : 4u;
   static constexpr int kSBO = 8 * kRowBytes;
-  // resident pair (K,V for dkdv / Q,dO for dq), then the streamed pairs
+};
+
+// Shared memory of one pass.  Resident pair: K, V (dkdv) or Q, dO (dq).
+// Streamed operand A: Q (dkdv) or K (dq); streamed operand B: dO (dkdv) or
+// V (dq); each has its own ring.  The dq pass needs no dbias accumulator and
+// spends that room on a third K stage at d = 128.
+template <int D, bool KV_MAJOR>
+struct BwdCfg : TileCfg<D> {
+  using T = TileCfg<D>;
+  static constexpr int kStagesA = D == 128 ? (KV_MAJOR ? 2 : 3) : (D == 64 ? (KV_MAJOR ? 3 : 4) : 4);
+  static constexpr int kStagesB = D == 128 ? 2 : (D == 64 ? 3 : 4);
   static constexpr int kResOff = 0;
-  static constexpr int kStreamOff = 2 * kTileBytes;
-  static constexpr int kBiasOff = kStreamOff + kStages * 2 * kTileBytes;
-  static constexpr int kBarOff = kBiasOff + 4 * (kMaxBiasLen + 1);
+  static constexpr int kAOff = 2 * T::kTileBytes;
+  static constexpr int kBOff = kAOff + kStagesA * T::kTileBytes;
+  static constexpr int kBiasOff = kBOff + kStagesB * T::kTileBytes;
+  static constexpr int kBarOff = kBiasOff + (KV_MAJOR ? 4 * (kMaxBiasLen + 1) : 0);
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;
 };
 
@@ -64,7 +75,7 @@ struct BwdBars {
   uint64_t s_full[2], dp_full, p_full, ds_full, acc_full, acc_empty;
   uint64_t drain;
   uint64_t grp[2];
-  uint64_t st_full[4], st_empty[4];
+  uint64_t a_full[4], a_empty[4], b_full[4], b_empty[4];
   uint32_t tmem_base;
   int abort;
 };
@@ -72,14 +83,14 @@ struct BwdBars {
 // K-major operand at column offset kk*16 inside a [128][D] tile.
 template <int D>
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-  using C = BwdCfg<D>;
+  using C = TileCfg<D>;
   const uint32_t off = (kk * 16 / C::kBlockCols) * C::kBlockBytes + (kk * 16 % C::kBlockCols) * 2;
   return sdesc(tile + off, 16, C::kSBO, C::kSwizzle);
 }
 // MN-major operand (N = D columns, K = 128 rows) at row offset kk*16.
 template <int D>
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
-  using C = BwdCfg<D>;
+  using C = TileCfg<D>;
   return sdesc(tile + kk * 16 * C::kRowBytes, C::kBlockBytes, C::kSBO, C::kSwizzle);
 }
 
@@ -137,7 +148,7 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int idx) {
 // (Q, dO) of each query tile (dkdv) or (K, V) of each key tile (dq).
 template <int D, bool KV_MAJOR>
 __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, int n_units, Fail fail) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, KV_MAJOR>;
   const CUtensorMap* res0 = KV_MAJOR ? &p.tm_k : &p.tm_q;
   const CUtensorMap* res1 = KV_MAJOR ? &p.tm_v : &p.tm_do;
   const CUtensorMap* str0 = KV_MAJOR ? &p.tm_q : &p.tm_k;
@@ -163,24 +174,29 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
       }
     }
     for (int i = 0; i < u.count; ++i) {
-      const int st = st_it % C::kStages;
-      if (!(ok = mbar_wait(&bars->st_empty[st], ((st_it / C::kStages) & 1) ^ 1, fail))) break;
       const int row = (KV_MAJOR ? u.seg.q0 : u.seg.k0) + (u.first + i) * kTile;
-      mbar_arrive_tx(&bars->st_full[st], 2 * C::kTileBytes);
-      uint8_t* d0 = smem + C::kStreamOff + st * 2 * C::kTileBytes;
+      const int sa = st_it % C::kStagesA, sb = st_it % C::kStagesB;
+      if (!(ok = mbar_wait(&bars->a_empty[sa], ((st_it / C::kStagesA) & 1) ^ 1, fail))) break;
+      mbar_arrive_tx(&bars->a_full[sa], C::kTileBytes);
+      uint8_t* da = smem + C::kAOff + sa * C::kTileBytes;
 #pragma unroll
-      for (int cb = 0; cb < C::kNumBlocks; ++cb) {
-        tma_load_3d(d0 + cb * C::kBlockBytes, str0, &bars->st_full[st], cb * C::kBlockCols, u.h, row);
-        tma_load_3d(d0 + C::kTileBytes + cb * C::kBlockBytes, str1, &bars->st_full[st], cb * C::kBlockCols, u.h,
-                    row);
-      }
+      for (int cb = 0; cb < C::kNumBlocks; ++cb)
+        tma_load_3d(da + cb * C::kBlockBytes, str0, &bars->a_full[sa], cb * C::kBlockCols, u.h, row);
+      if (!(ok = mbar_wait(&bars->b_empty[sb], ((st_it / C::kStagesB) & 1) ^ 1, fail))) break;
+      mbar_arrive_tx(&bars->b_full[sb], C::kTileBytes);
+      uint8_t* db = smem + C::kBOff + sb * C::kTileBytes;
+#pragma unroll
+      for (int cb = 0; cb < C::kNumBlocks; ++cb)
+        tma_load_3d(db + cb * C::kBlockBytes, str1, &bars->b_full[sb], cb * C::kBlockCols, u.h, row);
       ++st_it;
     }
   }
   if (!ok) {
     if (res_it) mbar_wait_drain(&bars->res_full, (res_it - 1) & 1);
-    for (uint32_t i = st_it > C::kStages ? st_it - C::kStages : 0; i < st_it; ++i)
-      mbar_wait_drain(&bars->st_full[i % C::kStages], (i / C::kStages) & 1);
+    for (uint32_t i = st_it > C::kStagesA ? st_it - C::kStagesA : 0; i < st_it; ++i)
+      mbar_wait_drain(&bars->a_full[i % C::kStagesA], (i / C::kStagesA) & 1);
+    for (uint32_t i = st_it > C::kStagesB ? st_it - C::kStagesB : 0; i < st_it; ++i)
+      mbar_wait_drain(&bars->b_full[i % C::kStagesB], (i / C::kStagesB) & 1);
   }
 }
 
@@ -194,9 +210,9 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
 template <int D>
 __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                            Fail fail) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, true>;
   const uint32_t k_t = smem_u32(smem + C::kResOff), v_t = k_t + C::kTileBytes;
-  const uint32_t str_base = smem_u32(smem + C::kStreamOff);
+  const uint32_t a_base = smem_u32(smem + C::kAOff), b_base = smem_u32(smem + C::kBOff);
   uint32_t res_it = 0, st_it = 0, p_it = 0, acc_it = 0;
   bool ok = true;
   for (int r = 0; ok; ++r) {
@@ -207,22 +223,22 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
     if (!(ok = mbar_wait(&bars->res_full, res_it & 1, fail))) break;
     ++res_it;
     {  // S^T and dP^T of the first query tile
-      const int st = st_it % C::kStages;
-      const uint32_t q_t = str_base + st * 2 * C::kTileBytes, do_t = q_t + C::kTileBytes;
-      if (!(ok = mbar_wait(&bars->st_full[st], (st_it / C::kStages) & 1, fail))) break;
+      const int sa = st_it % C::kStagesA, sb = st_it % C::kStagesB;
+      if (!(ok = mbar_wait(&bars->a_full[sa], (st_it / C::kStagesA) & 1, fail))) break;
       tc_fence_after();
-      mma_tile_nt<D>(tmem, k_t, q_t);  // S^T  = K  Q^T
+      mma_tile_nt<D>(tmem, k_t, a_base + sa * C::kTileBytes);  // S^T  = K  Q^T
       mma_commit(&bars->s_full[0]);
-      mma_tile_nt<D>(tmem + 128, v_t, do_t);  // dP^T = V  dO^T
+      if (!(ok = mbar_wait(&bars->b_full[sb], (st_it / C::kStagesB) & 1, fail))) break;
+      tc_fence_after();
+      mma_tile_nt<D>(tmem + 128, v_t, b_base + sb * C::kTileBytes);  // dP^T = V  dO^T
       mma_commit(&bars->dp_full);
     }
     for (int i = 0; i < u.count; ++i) {
       const uint32_t it = st_it + i;
-      const int st = it % C::kStages;
-      const uint32_t q_t = str_base + st * 2 * C::kTileBytes, do_t = q_t + C::kTileBytes;
+      const int sa = it % C::kStagesA, sb = it % C::kStagesB;
+      const int sa1 = (it + 1) % C::kStagesA, sb1 = (it + 1) % C::kStagesB;
+      const uint32_t q_t = a_base + sa * C::kTileBytes, do_t = b_base + sb * C::kTileBytes;
       const bool more = i + 1 < u.count;
-      const int st1 = (it + 1) % C::kStages;
-      const uint32_t q1 = str_base + st1 * 2 * C::kTileBytes, do1 = q1 + C::kTileBytes;
       if (i == 0) {
         if (!(ok = mbar_wait(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
         ++acc_it;
@@ -230,19 +246,22 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
       if (!(ok = mbar_wait(&bars->p_full, p_it & 1, fail))) break;
       tc_fence_after();
       mma_tile_tn<D>(tmem + 256, tmem + 0, tmem + 64, do_t, i > 0);  // dV += P^T dO
+      mma_commit(&bars->b_empty[sb]);  // dO(i) fully read once dV(i) completes
       if (more) {
-        if (!(ok = mbar_wait(&bars->st_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
+        if (!(ok = mbar_wait(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
         tc_fence_after();
-        mma_tile_nt<D>(tmem, k_t, q1);  // S^T of the next query tile
+        mma_tile_nt<D>(tmem, k_t, a_base + sa1 * C::kTileBytes);  // S^T of the next query tile
         mma_commit(&bars->s_full[0]);
       }
       if (!(ok = mbar_wait(&bars->ds_full, p_it & 1, fail))) break;
       ++p_it;
       tc_fence_after();
       mma_tile_tn<D>(tmem + 256 + D, tmem + 128, tmem + 192, q_t, i > 0);  // dK += dS^T Q
-      mma_commit(&bars->st_empty[st]);
+      mma_commit(&bars->a_empty[sa]);  // Q(i) fully read once dK(i) completes
       if (more) {
-        mma_tile_nt<D>(tmem + 128, v_t, do1);  // dP^T of the next query tile
+        if (!(ok = mbar_wait(&bars->b_full[sb1], ((it + 1) / C::kStagesB) & 1, fail))) break;
+        tc_fence_after();
+        mma_tile_nt<D>(tmem + 128, v_t, b_base + sb1 * C::kTileBytes);  // dP^T of the next query tile
         mma_commit(&bars->dp_full);
       }
     }
@@ -259,9 +278,9 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
 template <int D>
 __device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                           Fail fail) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, false>;
   const uint32_t q_t = smem_u32(smem + C::kResOff), do_t = q_t + C::kTileBytes;
-  const uint32_t str_base = smem_u32(smem + C::kStreamOff);
+  const uint32_t a_base = smem_u32(smem + C::kAOff), b_base = smem_u32(smem + C::kBOff);
   const uint32_t t_s[2] = {tmem, tmem + 384};
   uint32_t res_it = 0, st_it = 0, ds_it = 0, acc_it = 0, s_cnt = 0;
   bool ok = true;
@@ -273,25 +292,28 @@ __device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint
     if (!(ok = mbar_wait(&bars->res_full, res_it & 1, fail))) break;
     ++res_it;
     {  // S of the first key tile
-      const int st = st_it % C::kStages;
-      if (!(ok = mbar_wait(&bars->st_full[st], (st_it / C::kStages) & 1, fail))) break;
+      const int sa = st_it % C::kStagesA;
+      if (!(ok = mbar_wait(&bars->a_full[sa], (st_it / C::kStagesA) & 1, fail))) break;
       tc_fence_after();
-      mma_tile_nt<D>(t_s[s_cnt & 1], q_t, str_base + st * 2 * C::kTileBytes);
+      mma_tile_nt<D>(t_s[s_cnt & 1], q_t, a_base + sa * C::kTileBytes);
       mma_commit(&bars->s_full[s_cnt & 1]);
     }
     for (int i = 0; i < u.count; ++i) {
       const uint32_t it = st_it + i;
-      const int st = it % C::kStages;
-      const uint32_t k_t = str_base + st * 2 * C::kTileBytes, v_t = k_t + C::kTileBytes;
-      const uint32_t sb = (s_cnt + i) & 1;
+      const int sa = it % C::kStagesA, sb = it % C::kStagesB;
+      const uint32_t k_t = a_base + sa * C::kTileBytes, v_t = b_base + sb * C::kTileBytes;
+      const uint32_t sbuf = (s_cnt + i) & 1;
+      if (!(ok = mbar_wait(&bars->b_full[sb], (it / C::kStagesB) & 1, fail))) break;
+      tc_fence_after();
       mma_tile_nt<D>(tmem + 128, do_t, v_t);  // dP = dO V^T
       mma_commit(&bars->dp_full);
+      mma_commit(&bars->b_empty[sb]);  // V(i) fully read once dP(i) completes
       if (i + 1 < u.count) {  // S of the next key tile into the other buffer
-        const int st1 = (it + 1) % C::kStages;
-        if (!(ok = mbar_wait(&bars->st_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
+        const int sa1 = (it + 1) % C::kStagesA;
+        if (!(ok = mbar_wait(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
         tc_fence_after();
-        mma_tile_nt<D>(t_s[sb ^ 1], q_t, str_base + st1 * 2 * C::kTileBytes);
-        mma_commit(&bars->s_full[sb ^ 1]);
+        mma_tile_nt<D>(t_s[sbuf ^ 1], q_t, a_base + sa1 * C::kTileBytes);
+        mma_commit(&bars->s_full[sbuf ^ 1]);
       }
       if (i == 0) {
         if (!(ok = mbar_wait(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
@@ -300,8 +322,8 @@ __device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint
       if (!(ok = mbar_wait(&bars->ds_full, ds_it & 1, fail))) break;
       ++ds_it;
       tc_fence_after();
-      mma_tile_tn<D>(tmem + 256, t_s[sb], t_s[sb] + 64, k_t, i > 0);  // dQ += dS K
-      mma_commit(&bars->st_empty[st]);
+      mma_tile_tn<D>(tmem + 256, t_s[sbuf], t_s[sbuf] + 64, k_t, i > 0);  // dQ += dS K
+      mma_commit(&bars->a_empty[sa]);  // K(i) fully read once dQ(i) completes
     }
     if (!ok) break;
     st_it += u.count;
@@ -442,7 +464,7 @@ __device__ __forceinline__ void phase_b_chunk(const uint32_t (&dv)[32], const fl
 
 template <int D, int ACT, bool KV_MAJOR>
 __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units, Fail fail) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, KV_MAJOR>;
   constexpr bool kSoftmax = ACT == 2;
   const int warp = threadIdx.x >> 5;
   const int quad = warp & 3;
@@ -674,7 +696,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
 // ------------------------------------------------------------------- kernel
 template <int D, int ACT, bool KV_MAJOR>
 __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant__ BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, KV_MAJOR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kBarOff);
@@ -693,9 +715,11 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->grp[0], 256);
     mbar_init(&bars->grp[1], 256);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bars->st_full[s], 1);
-      mbar_init(&bars->st_empty[s], 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->a_full[s], 1);
+      mbar_init(&bars->a_empty[s], 1);
+      mbar_init(&bars->b_full[s], 1);
+      mbar_init(&bars->b_empty[s], 1);
     }
     bars->abort = 0;
     fence_mbar_init();
@@ -768,7 +792,7 @@ __global__ void dbias_reduce_kernel(const float* __restrict__ part, float* __res
 // ------------------------------------------------------------------- launch
 template <int D, int ACT, bool KV_MAJOR>
 static cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t stream) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, KV_MAJOR>;
   auto kern = gdpa_bwd_kernel<D, ACT, KV_MAJOR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;

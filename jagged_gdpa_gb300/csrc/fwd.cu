@@ -61,7 +61,7 @@ struct FwdBars {
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t drain;
-  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint32_t tmem_base;
   int abort;
 };
@@ -117,16 +117,19 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
         tma_load_3d(dst + cb * C::kBlockBytes, &p.tm_q, &bars->q_full[s], cb * C::kBlockCols, u.h, row);
       ++q_it[s];
     }
+    // K and V of a stage are released separately (K after the last S that
+    // reads it, V after the last P V), so K loads run well ahead of use.
     for (int kt = 0; kt < u.nkv && ok; ++kt) {
       const int st = kv_it % C::kStages;
-      ok = mbar_wait(&bars->kv_empty[st], ((kv_it / C::kStages) & 1) ^ 1, fail);
-      if (!ok) break;
+      const uint32_t empty_phase = ((kv_it / C::kStages) & 1) ^ 1;
+      if (!(ok = mbar_wait(&bars->k_empty[st], empty_phase, fail))) break;
       const int row = u.seg.k0 + kt * kTile;
       mbar_arrive_tx(&bars->k_full[st], C::kTileBytes);
       uint8_t* kd = smem + C::kKOff + st * C::kTileBytes;
 #pragma unroll
       for (int cb = 0; cb < C::kNumBlocks; ++cb)
         tma_load_3d(kd + cb * C::kBlockBytes, &p.tm_k, &bars->k_full[st], cb * C::kBlockCols, u.h, row);
+      if (!(ok = mbar_wait(&bars->v_empty[st], empty_phase, fail))) break;
       mbar_arrive_tx(&bars->v_full[st], C::kTileBytes);
       uint8_t* vd = smem + C::kVOff + st * C::kTileBytes;
 #pragma unroll
@@ -206,6 +209,7 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
         mma_commit(&bars->s_full[s]);
         if (u.nkv_s[s] == 1) mma_commit(&bars->q_empty[s]);
       }
+      mma_commit(&bars->k_empty[st]);  // both S of K(0) issued
     }
     for (int kt = 0; kt < u.nkv && ok; ++kt) {
       const uint32_t it = kv_it + kt;
@@ -247,12 +251,13 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
         issue_pv<D>(t_o[1], t_s[1], v_addr, kt > 0);
         if (kt == u.nkv_s[1] - 1) mma_commit(&bars->o_full[1]);
       }
-      mma_commit(&bars->kv_empty[st]);
+      mma_commit(&bars->v_empty[st]);  // every P V of V(kt) issued
       if (more && kt + 1 < u.nkv_s[1]) {
         issue_qk<D>(t_s[1], q_addr[1], k_base + st1 * C::kTileBytes);
         mma_commit(&bars->s_full[1]);
         if (kt + 1 == u.nkv_s[1] - 1) mma_commit(&bars->q_empty[1]);
       }
+      if (more) mma_commit(&bars->k_empty[st1]);  // every S of K(kt+1) issued
     }
     kv_it += u.nkv;
   }
@@ -521,8 +526,9 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
