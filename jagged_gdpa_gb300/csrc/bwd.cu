@@ -202,11 +202,13 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
 
 // ---------------------------------------------------------------- MMA issuer
 // dkdv.  Issue order over query tiles i:
-//   S^T(0), dP^T(0), { [P^T(i) ready] dV(i), S^T(i+1), [dS^T(i) ready] dK(i),
-//   dP^T(i+1) }
-// S^T(i+1) may follow dV(i) (which has consumed P^T(i) from the same TMEM
-// columns) and dP^T(i+1) follows dK(i) (which has consumed dS^T(i)), so the
-// activation warps get two MMAs of slack for each phase.
+//   S^T(0), dP^T(0), { [P^T(i) ready] dV(i), [dS^T(i) ready] dK(i),
+//   S^T(i+1), dP^T(i+1) }
+// The tensor core pays a pipeline switch whenever it alternates between MMAs
+// that read A from shared memory (S^T, dP^T) and from TMEM (dV, dK), so the
+// two kinds are issued in pairs: two switches per query tile.  S^T(i+1) and
+// dP^T(i+1) overwrite the TMEM columns that dV(i) and dK(i) read; they are
+// issued after them and MMAs execute in issue order.
 template <int D>
 __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                            Fail fail) {
@@ -247,18 +249,16 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
       tc_fence_after();
       mma_tile_tn<D>(tmem + 256, tmem + 0, tmem + 64, do_t, i > 0);  // dV += P^T dO
       mma_commit(&bars->b_empty[sb]);  // dO(i) fully read once dV(i) completes
-      if (more) {
-        if (!(ok = mbar_wait(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
-        tc_fence_after();
-        mma_tile_nt<D>(tmem, k_t, a_base + sa1 * C::kTileBytes);  // S^T of the next query tile
-        mma_commit(&bars->s_full[0]);
-      }
       if (!(ok = mbar_wait(&bars->ds_full, p_it & 1, fail))) break;
       ++p_it;
       tc_fence_after();
       mma_tile_tn<D>(tmem + 256 + D, tmem + 128, tmem + 192, q_t, i > 0);  // dK += dS^T Q
       mma_commit(&bars->a_empty[sa]);  // Q(i) fully read once dK(i) completes
       if (more) {
+        if (!(ok = mbar_wait(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
+        tc_fence_after();
+        mma_tile_nt<D>(tmem, k_t, a_base + sa1 * C::kTileBytes);  // S^T of the next query tile
+        mma_commit(&bars->s_full[0]);
         if (!(ok = mbar_wait(&bars->b_full[sb1], ((it + 1) / C::kStagesB) & 1, fail))) break;
         tc_fence_after();
         mma_tile_nt<D>(tmem + 128, v_t, b_base + sb1 * C::kTileBytes);  // dP^T of the next query tile
