@@ -194,7 +194,9 @@ JGDPA_API const char* jgdpa_status_string(jgdpa_status s);
  * forward and backward kernels use them, on n fp32 inputs.  act is GELU or
  * SiLU; y[i] = act(x[i]) and dy[i] = act'(x[i]) (dy may be NULL).  `path`
  * selects the evaluation route: 0 = the special-function-unit route (hardware
- * tanh), 1 = the ALU-only polynomial route.  x, y, dy are device pointers.
+ * tanh), 1 = the ALU-only polynomial route, 2 = the exponential route
+ * (hardware ex2, reciprocal on the FMA pipe; forward only, so its dy is the
+ * route-0 derivative).  x, y, dy are device pointers.
  */
 JGDPA_API jgdpa_status jgdpa_eval_activation(jgdpa_act act, int32_t path, const float* x, int64_t n,
                                    float* y, float* dy, jgdpa_stream_t stream);

@@ -204,6 +204,40 @@ __device__ __forceinline__ float2 act2(float2 hx) {
   else return act2_sfu<ACT>(hx);
 }
 
+// Exponential route: sigmoid(z) = 1 / (1 + 2^(-z log2 e)) with the hardware
+// ex2 (twice the special-function rate of tanh on this GPU) and the
+// reciprocal from the integer seed plus one Newton step on the FMA pipe
+// (relative error 2.6e-3, below the bf16 rounding of P).  Forward only.
+__device__ __forceinline__ float2 rcp1_alu2(float2 a) {
+  const float2 y = make_float2(__int_as_float(kRcpSeed - __float_as_int(a.x)),
+                               __int_as_float(kRcpSeed - __float_as_int(a.y)));
+  const float2 e = __ffma2_rn(make_float2(-a.x, -a.y), y, f2(1.0f));
+  return __ffma2_rn(y, e, y);
+}
+template <int ACT>
+__device__ __forceinline__ float2 act2_ex2(float2 hx) {
+  float2 w;  // w = -k(x) log2 e with x = 2 hx
+  if constexpr (ACT == 0)
+    w = __fmul2_rn(hx, __ffma2_rn(__fmul2_rn(hx, hx), f2(-8.0f * kGeluB * kLog2e), f2(-2.0f * kGeluA * kLog2e)));
+  else
+    w = __fmul2_rn(hx, f2(-2.0f * kLog2e));
+  // 2^w overflows to +inf for w > 128: then 1 + e = inf and the seed gives a
+  // tiny positive y, so sigmoid -> 0 as it should; clamp keeps it finite.
+  w = make_float2(fminf(w.x, 64.0f), fminf(w.y, 64.0f));
+  const float2 e = make_float2(ex2_sfu(w.x), ex2_sfu(w.y));
+  const float2 s = rcp1_alu2(__fadd2_rn(e, f2(1.0f)));
+  const float2 hs = __fmul2_rn(hx, s);
+  return __fadd2_rn(hs, hs);
+}
+
+// Route of one forward element group: 0 SFU tanh, 1 ALU polynomial, 2 ex2.
+template <int ACT, int ROUTE>
+__device__ __forceinline__ float2 act2_route(float2 hx) {
+  if constexpr (ROUTE == 1) return act2_alu<ACT>(hx);
+  else if constexpr (ROUTE == 2) return act2_ex2<ACT>(hx);
+  else return act2_sfu<ACT>(hx);
+}
+
 // act(x) and act'(x) for two lanes from hx = x / 2 (SFU route).
 //   GELU: act' = s + x s (1 - s) k'(x), s = (1 + t) / 2, s (1 - s) = (1 - t^2) / 4,
 //         k'(x) / 2 = a / 2 + 6 b hx^2  ->  act' = s + hx (1 - t^2) k'/2

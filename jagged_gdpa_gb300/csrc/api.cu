@@ -169,12 +169,12 @@ cudaError_t fill_f32(float* p, int64_t n, float v, cudaStream_t s) {
 // Evaluates the kernels' packed activation routines (act2: forward value,
 // act2_d: backward derivative) on two elements per thread, from hx = x / 2
 // exactly as the kernels form it.
-template <int ACT, bool ALU>
+template <int ACT, int PATH>
 __device__ void eval_act_pair(const float* x, int64_t i, int64_t n, float* y, float* dy) {
   const float2 hx = make_float2(0.5f * x[i], i + 1 < n ? 0.5f * x[i + 1] : 0.f);
-  const float2 a = jg::act2<ACT, ALU>(hx);
-  float2 d;
-  (void)jg::act2_d<ACT, ALU>(hx, d);
+  const float2 a = jg::act2_route<ACT, PATH>(hx);
+  float2 d;  // the ex2 route is forward-only: its derivative is the SFU one
+  (void)jg::act2_d<ACT, PATH == 1>(hx, d);
   y[i] = a.x;
   if (dy) dy[i] = d.x;
   if (i + 1 < n) {
@@ -187,11 +187,13 @@ __global__ void eval_act_kernel(int act, int path, const float* x, int64_t n, fl
   const int64_t i = 2 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
   if (i >= n) return;
   if (act == 0) {
-    if (path) eval_act_pair<0, true>(x, i, n, y, dy);
-    else eval_act_pair<0, false>(x, i, n, y, dy);
+    if (path == 1) eval_act_pair<0, 1>(x, i, n, y, dy);
+    else if (path == 2) eval_act_pair<0, 2>(x, i, n, y, dy);
+    else eval_act_pair<0, 0>(x, i, n, y, dy);
   } else {
-    if (path) eval_act_pair<1, true>(x, i, n, y, dy);
-    else eval_act_pair<1, false>(x, i, n, y, dy);
+    if (path == 1) eval_act_pair<1, 1>(x, i, n, y, dy);
+    else if (path == 2) eval_act_pair<1, 2>(x, i, n, y, dy);
+    else eval_act_pair<1, 0>(x, i, n, y, dy);
   }
 }
 
@@ -393,7 +395,7 @@ const char* jgdpa_status_string(jgdpa_status s) {
 jgdpa_status jgdpa_eval_activation(jgdpa_act act, int32_t path, const float* x, int64_t n, float* y, float* dy,
                                    jgdpa_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if ((act != JGDPA_ACT_GELU && act != JGDPA_ACT_SILU) || (path != 0 && path != 1) || n < 0)
+  if ((act != JGDPA_ACT_GELU && act != JGDPA_ACT_SILU) || path < 0 || path > 2 || n < 0)
     return JGDPA_ERR_INVALID_ARGUMENT;
   if (n == 0) return JGDPA_OK;
   if (x == nullptr || y == nullptr) return JGDPA_ERR_INVALID_ARGUMENT;

@@ -32,12 +32,21 @@
 
 namespace jg {
 
-// Number of the four 32-column chunks of every S tile whose activation takes
-// the ALU route (the rest use the special-function unit).
+// Routes of the four 32-column chunks of every S tile: the last
+// JGDPA_FWD_ALU_CHUNKS take the ALU polynomial route, the
+// JGDPA_FWD_EX2_CHUNKS before them the ex2 route, the rest the hardware tanh.
+// On GB300 tanh issues at 16 and ex2 at 32 results per clock per SM while the
+// FMA pipe does 128, so splitting tanh / ex2 evenly balances the special-
+// function unit against the FMA pipe.
 #ifndef JGDPA_FWD_ALU_CHUNKS
 #define JGDPA_FWD_ALU_CHUNKS 0
 #endif
+#ifndef JGDPA_FWD_EX2_CHUNKS
+#define JGDPA_FWD_EX2_CHUNKS 2
+#endif
 constexpr int kFwdAluChunks = JGDPA_FWD_ALU_CHUNKS;
+constexpr int kFwdEx2Chunks = JGDPA_FWD_EX2_CHUNKS;
+static_assert(kFwdAluChunks + kFwdEx2Chunks <= 4, "four 32-column chunks per tile");
 
 template <int D>
 struct FwdCfg {
@@ -218,39 +227,50 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
       if (!(ok = mbar_wait(&bars->v_full[st], (it / C::kStages) & 1, fail))) break;
       const bool more = kt + 1 < u.nkv;
       const int st1 = (it + 1) % C::kStages;
-      // Both P V of this tile, then both S of the next: the tensor core pays
-      // a pipeline switch every time it alternates between MMAs that read A
-      // from shared memory (S) and from TMEM (P V), so the two kinds are
-      // issued in groups (two switches per key/value tile instead of four).
-      // S_s(kt+1) overwrites the columns that PV_s(kt) reads; it is issued
-      // after it, and MMAs execute in issue order.
-#pragma unroll
-      for (int s = 0; s < 2 && ok; ++s) {
-        if (kt >= u.nkv_s[s]) continue;
+      // Order per tile: PV0(kt), S0(kt+1), PV1(kt), S1(kt+1).  Each slot's
+      // activation then has the other slot's PV and S (two MMA groups) to
+      // hide behind.  S_s(kt+1) overwrites the columns that PV_s(kt) reads;
+      // it is issued after it, and MMAs execute in issue order.
+      // slot 0: O0 += P0 V, then S0 of the next tile
+      if (kt < u.nkv_s[0]) {
         if (kt == 0) {
-          if (!(ok = mbar_wait(&bars->o_empty[s], (o_it[s] & 1) ^ 1, fail))) break;
-          ++o_it[s];
+          if (!(ok = mbar_wait(&bars->o_empty[0], (o_it[0] & 1) ^ 1, fail))) break;
+          ++o_it[0];
         }
-        if (!(ok = mbar_wait(&bars->p_full[s], p_it[s] & 1, fail))) break;
-        ++p_it[s];
+        if (!(ok = mbar_wait(&bars->p_full[0], p_it[0] & 1, fail))) break;
+        ++p_it[0];
         tc_fence_after();
-        issue_pv<D>(t_o[s], t_s[s], v_addr, kt > 0);
-        if (kt == u.nkv_s[s] - 1) mma_commit(&bars->o_full[s]);
+        issue_pv<D>(t_o[0], t_s[0], v_addr, kt > 0);
+        if (kt == u.nkv_s[0] - 1) mma_commit(&bars->o_full[0]);
       }
-      if (!ok) break;
-      mma_commit(&bars->v_empty[st]);  // every P V of V(kt) issued
       if (more) {
         if (!(ok = mbar_wait(&bars->k_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
         tc_fence_after();
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          if (kt + 1 >= u.nkv_s[s]) continue;
-          issue_qk<D>(t_s[s], q_addr[s], k_base + st1 * C::kTileBytes);
-          mma_commit(&bars->s_full[s]);
-          if (kt + 1 == u.nkv_s[s] - 1) mma_commit(&bars->q_empty[s]);
+        if (kt + 1 < u.nkv_s[0]) {
+          issue_qk<D>(t_s[0], q_addr[0], k_base + st1 * C::kTileBytes);
+          mma_commit(&bars->s_full[0]);
+          if (kt + 1 == u.nkv_s[0] - 1) mma_commit(&bars->q_empty[0]);
         }
-        mma_commit(&bars->k_empty[st1]);  // every S of K(kt+1) issued
       }
+      // slot 1: O1 += P1 V, release V, then S1 of the next tile, release K
+      if (kt < u.nkv_s[1]) {
+        if (kt == 0) {
+          if (!(ok = mbar_wait(&bars->o_empty[1], (o_it[1] & 1) ^ 1, fail))) break;
+          ++o_it[1];
+        }
+        if (!(ok = mbar_wait(&bars->p_full[1], p_it[1] & 1, fail))) break;
+        ++p_it[1];
+        tc_fence_after();
+        issue_pv<D>(t_o[1], t_s[1], v_addr, kt > 0);
+        if (kt == u.nkv_s[1] - 1) mma_commit(&bars->o_full[1]);
+      }
+      mma_commit(&bars->v_empty[st]);  // every P V of V(kt) issued
+      if (more && kt + 1 < u.nkv_s[1]) {
+        issue_qk<D>(t_s[1], q_addr[1], k_base + st1 * C::kTileBytes);
+        mma_commit(&bars->s_full[1]);
+        if (kt + 1 == u.nkv_s[1] - 1) mma_commit(&bars->q_empty[1]);
+      }
+      if (more) mma_commit(&bars->k_empty[st1]);  // every S of K(kt+1) issued
     }
     kv_it += u.nkv;
   }
@@ -325,8 +345,9 @@ __device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias&
         if (c + 1 >= nvalid) hx.y = 0.f;
       }
       float2 y;
-      if (q >= 4 - NALU) y = act2<ACT, true>(hx);
-      else y = act2<ACT, false>(hx);
+      if (q >= 4 - NALU) y = act2_route<ACT, 1>(hx);
+      else if (q >= 4 - NALU - kFwdEx2Chunks) y = act2_route<ACT, 2>(hx);
+      else y = act2_route<ACT, 0>(hx);
       pk[c2] = pack_bf16(y.x, y.y);
     }
     tmem_st16(t_s + 16 * q, pk);

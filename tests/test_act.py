@@ -23,7 +23,7 @@ def jg():
 
 
 @pytest.mark.parametrize("act", ["gelu", "silu"])
-@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("path", [0, 1, 2])
 def test_activation_accuracy(jg, act, path):
     x = torch.linspace(-16.0, 16.0, 1 << 20, dtype=torch.float32)
     x = torch.cat([x, torch.tensor([0.0, -0.0, 1e-30, -1e-30, 1e-3, -1e-3])])
