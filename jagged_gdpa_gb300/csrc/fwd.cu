@@ -35,14 +35,15 @@ namespace jg {
 // Routes of the four 32-column chunks of every S tile: the last
 // JGDPA_FWD_ALU_CHUNKS take the ALU polynomial route, the
 // JGDPA_FWD_EX2_CHUNKS before them the ex2 route, the rest the hardware tanh.
-// On GB300 tanh issues at 16 and ex2 at 32 results per clock per SM while the
-// FMA pipe does 128, so splitting tanh / ex2 evenly balances the special-
-// function unit against the FMA pipe.
+// Measured on GB300 (long-tail workload, 24 heads, d = 128, GELU): every chunk
+// moved off the tanh route made the forward slower (0/1/3/4 ex2 chunks:
+// 2.83/3.06/3.49/3.85 ms; ALU chunks likewise), so both default to 0 and
+// the other routes stay available as compile-time options.
 #ifndef JGDPA_FWD_ALU_CHUNKS
 #define JGDPA_FWD_ALU_CHUNKS 0
 #endif
 #ifndef JGDPA_FWD_EX2_CHUNKS
-#define JGDPA_FWD_EX2_CHUNKS 2
+#define JGDPA_FWD_EX2_CHUNKS 0
 #endif
 constexpr int kFwdAluChunks = JGDPA_FWD_ALU_CHUNKS;
 constexpr int kFwdEx2Chunks = JGDPA_FWD_EX2_CHUNKS;
