@@ -429,15 +429,23 @@ __device__ __forceinline__ void phase_a_chunk(const uint32_t (&sv)[32], const fl
 // Phase B on one 32-column chunk: dS = act'(x) dP (softmax: P (dP - D)),
 // packed into pk.  DBIAS: 0 none, 1 the tile clamps to one table end (sum
 // into row_sum), 2 per-element table entries (band tile).
-template <int ACT, bool KV_MAJOR, int DBIAS>
+//
+// Band tiles (KV-major): element (lane l, chunk column m) of a warp has
+// rel = W + m - l with W uniform over the warp and chunk, so it belongs to
+// diagonal d = m - l in [-31, 31].  At column m lane L takes the value of
+// lane (m - L) mod 32 by a shuffle, whose diagonal is L if m >= L and L - 32
+// otherwise; each lane thus sums two diagonals per chunk.  Chunk 1's W is
+// chunk 0's plus 32, so its lower diagonal is chunk 0's upper one, and the
+// three sums dacc[0..2] hold the diagonals W0 + L - 32, W0 + L, W0 + L + 32.
+template <int ACT, bool KV_MAJOR, int DBIAS, int CHUNK>
 __device__ __forceinline__ void phase_b_chunk(const uint32_t (&dv)[32], const float (&del_c)[32], float delta_row,
-                                              const float (&keep)[32], const PairGeom& g, int R, int cbase,
-                                              float* sbias, float2& row_sum, float& acc_lo, float& acc_hi,
+                                              const float (&keep)[32], float2& row_sum, float (&dacc)[3],
                                               uint32_t (&pk)[16]) {
   constexpr bool kSoftmax = ACT == 2;
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int e2 = 0; e2 < 16; ++e2) {
-    const int cl = 2 * e2, c = cbase + cl;
+    const int cl = 2 * e2;
     const float2 dp = make_float2(__uint_as_float(dv[cl]), __uint_as_float(dv[cl + 1]));
     const float2 kv = make_float2(keep[cl], keep[cl + 1]);
     float2 ds;
@@ -452,11 +460,10 @@ __device__ __forceinline__ void phase_b_chunk(const uint32_t (&dv)[32], const fl
     if constexpr (DBIAS == 2) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int rel = g.rel0 + (c + e);
-        const float v = e ? ds.y : ds.x;
-        if (rel >= R) acc_hi += v;
-        else if (rel <= -R) acc_lo += v;
-        else atomicAdd(sbias + rel + R, v);
+        const int m = cl + e;
+        const float v = __shfl_sync(0xffffffffu, e ? ds.y : ds.x, (m - lane) & 31);
+        if (m >= lane) dacc[CHUNK + 1] += v;
+        else dacc[CHUNK] += v;
       }
     }
   }
@@ -578,6 +585,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       ++dp_it;
       tc_fence_after();
       float2 row_sum = f2(0.f);
+      float dacc[3] = {0.f, 0.f, 0.f};
       const int dmode = !want_dbias ? 0 : (g.band ? 2 : 1);
       uint32_t dv0[32], dv1[32];
       tmem_ld32(t_dp, dv0);
@@ -596,12 +604,17 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         }
         uint32_t pk[16];
         const float(&keep)[32] = chunk == 0 ? keep0 : keep1;
-        if (dmode == 0)
-          phase_b_chunk<ACT, KV_MAJOR, 0>(dv, del_c, delta_row, keep, g, R, cbase, sbias, row_sum, acc_lo, acc_hi, pk);
-        else if (dmode == 1)
-          phase_b_chunk<ACT, KV_MAJOR, 1>(dv, del_c, delta_row, keep, g, R, cbase, sbias, row_sum, acc_lo, acc_hi, pk);
-        else
-          phase_b_chunk<ACT, KV_MAJOR, 2>(dv, del_c, delta_row, keep, g, R, cbase, sbias, row_sum, acc_lo, acc_hi, pk);
+#define JG_PHASE_B(DB) \
+  phase_b_chunk<ACT, KV_MAJOR, DB, 0>(dv, del_c, delta_row, keep, row_sum, dacc, pk)
+#define JG_PHASE_B1(DB) \
+  phase_b_chunk<ACT, KV_MAJOR, DB, 1>(dv, del_c, delta_row, keep, row_sum, dacc, pk)
+        if (chunk == 0) {
+          if (dmode == 0) JG_PHASE_B(0); else if (dmode == 1) JG_PHASE_B(1); else JG_PHASE_B(2);
+        } else {
+          if (dmode == 0) JG_PHASE_B1(0); else if (dmode == 1) JG_PHASE_B1(1); else JG_PHASE_B1(2);
+        }
+#undef JG_PHASE_B
+#undef JG_PHASE_B1
         // dS^T over dP^T columns (dkdv) / dS over S columns (dq), already read
         tmem_st16((KV_MAJOR ? t_dp : t_s) + 16 * chunk, pk);
         if (chunk == 0) tmem_ld_wait(dv1);
@@ -609,6 +622,16 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       if (dmode == 1) {
         if (g.upper) acc_hi += row_sum.x + row_sum.y;  // the whole tile clamps to one end of the table
         else acc_lo += row_sum.x + row_sum.y;
+      } else if (dmode == 2) {
+        // diagonal sums -> table entries (rel of diagonal k: see phase_b_chunk)
+        const int rel1 = g.rel0 + 2 * (threadIdx.x & 31) + 64 * half;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int rel = rel1 + 32 * (k - 1);
+          if (rel >= R) acc_hi += dacc[k];
+          else if (rel <= -R) acc_lo += dacc[k];
+          else atomicAdd(sbias + rel + R, dacc[k]);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
