@@ -6,27 +6,33 @@
 // Workloads", aiuniverse.news):
 //
 //   dkdv pass, unit = (segment, head, 128-row key/value tile):
-//     for every query tile that meets it:
+//     for every query tile i that meets it:
 //       S^T = K Q^T, dP^T = V dO^T                       (tcgen05, TMEM)
-//       phase A: P^T = act(x)^T, act'(x) kept in registers
-//       phase B: dS^T = dP^T act'(x)^T, dbias partials
-//       (softmax: P = exp(x - LSE_i), dS = P (dP - D_i))
-//       dV += P^T dO (after phase A), dK += dS^T Q (after phase B)
+//       phase A: P^T = act(x)^T (bf16, to shared memory), act'(x) kept in
+//                registers (softmax: P = exp(x - LSE_i))
+//       phase B: dS^T = dP^T act'(x)^T (softmax: P (dP - D_i)), to shared
+//                memory; dbias partial sums
+//       dV += P^T dO, dK += dS^T Q                       (tcgen05, TMEM)
 //     dK *= s; store dK, dV
 //   dq pass, unit = (segment, head, 128-row query tile):
-//     for every key/value tile: S = Q K^T (double-buffered), dP = dO V^T,
-//       phase A: act'(x); phase B: dS = dP act'(x); dQ += dS K
+//     for every key/value tile: S = Q K^T, dP = dO V^T,
+//       phase A: act'(x); phase B: dS = dP act'(x) to shared memory;
+//       dQ += dS K
 //     dQ *= s; store
 //
-// Phase A runs while the tensor core computes dP; phase B runs while it
-// computes dV (dkdv) or the next tile's S (dq), so the activation work hides
-// behind the MMAs.
+// Every MMA reads both operands from shared memory: the bf16 P^T / dS^T /
+// dS that the activation warps produce go to a shared "X" tile rather than
+// back to TMEM, because on this GPU the tensor core stalls for ~300 cycles
+// each time it switches between MMAs whose A operand comes from shared
+// memory and from TMEM, while its operand reads from shared memory do not
+// compete with the warps' own shared-memory traffic.  The activation warps
+// load a whole S (dP) tile into registers and release its TMEM columns
+// before computing, so the next tile's S (dP) is computed while they work.
 //
 // TMEM (512 columns): dkdv uses S^T [0,128), dP^T [128,256), dV [256,256+D),
-// dK [256+D, 256+2D); dq uses S0 [0,128), dP [128,256), dQ [256,256+D),
-// S1 [384,512).  Two activation warpgroups split the 128 columns of a tile;
-// each writes its bf16 P / dS over S / dP columns that it has already read,
-// and the MMA picks the operand columns per 16-wide K step.
+// dK [256+D, 256+2D); dq uses S [0,128), dP [128,256), dQ [256,256+D).  Two
+// activation warpgroups split the 128 columns of a tile; warpgroup h owns
+// columns [64h, 64h + 64), which is column block h of the X tile.
 #include "act.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
@@ -55,62 +61,82 @@ struct TileCfg {
 
 // Shared memory of one pass.  Resident pair: K, V (dkdv) or Q, dO (dq).
 // Streamed operand A: Q (dkdv) or K (dq); streamed operand B: dO (dkdv) or
-// V (dq); each has its own ring.  The dq pass needs no dbias accumulator and
-// spends that room on a third K stage at d = 128.
+// V (dq); each has its own ring.  X: ring of [128][128] bf16 tiles written by
+// the activation warps (P^T then dS^T per query tile in dkdv, dS in dq).
+// Stage counts at d = 128 (seven 32 KB tiles fit): dkdv keeps two of each
+// stream and one X; dq reads V only in dP, early in a tile's life, and K in S
+// and again in dQ at its end, so it keeps three K stages and one V stage.
 template <int D, bool KV_MAJOR>
 struct BwdCfg : TileCfg<D> {
   using T = TileCfg<D>;
   static constexpr int kStagesA = D == 128 ? (KV_MAJOR ? 2 : 3) : (D == 64 ? (KV_MAJOR ? 3 : 4) : 4);
-  static constexpr int kStagesB = D == 128 ? 2 : (D == 64 ? 3 : 4);
+  static constexpr int kStagesB = D == 128 ? (KV_MAJOR ? 2 : 1) : (D == 64 ? (KV_MAJOR ? 3 : 2) : 4);
+  static constexpr int kNumX = D == 128 ? 1 : 2;
+  static constexpr int kXBytes = kTile * kTile * 2;
   static constexpr int kResOff = 0;
   static constexpr int kAOff = 2 * T::kTileBytes;
   static constexpr int kBOff = kAOff + kStagesA * T::kTileBytes;
-  static constexpr int kBiasOff = kBOff + kStagesB * T::kTileBytes;
-  static constexpr int kBarOff = kBiasOff + (KV_MAJOR ? 4 * (kMaxBiasLen + 1) : 0);
+  static constexpr int kXOff = kBOff + kStagesB * T::kTileBytes;
+  static constexpr int kBarOff = kXOff + kNumX * kXBytes;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;
+  static_assert(kXOff % 1024 == 0, "X tiles need 1024-byte alignment for the 128-byte swizzle");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct BwdBars {
   uint64_t res_full, res_empty;
-  uint64_t s_full[2], dp_full, p_full, ds_full, acc_full, acc_empty;
+  uint64_t s_full, s_free, dp_full, dp_free, acc_full, acc_empty;
   uint64_t drain;
-  uint64_t grp[2];
+  uint64_t x_full[2], x_empty[2];
   uint64_t a_full[4], a_empty[4], b_full[4], b_empty[4];
   uint32_t tmem_base;
   int abort;
 };
 
-// K-major operand at column offset kk*16 inside a [128][D] tile.
+// K-major operand at column offset kk*16 inside a [128][D] tile: byte
+// offset from the tile start (the descriptor's address field counts 16-byte
+// units and never carries: shared addresses stay below 256 KB).
 template <int D>
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+__host__ __device__ constexpr uint32_t kmajor_off(int kk) {
   using C = TileCfg<D>;
-  const uint32_t off = (kk * 16 / C::kBlockCols) * C::kBlockBytes + (kk * 16 % C::kBlockCols) * 2;
-  return sdesc(tile + off, 16, C::kSBO, C::kSwizzle);
+  return (kk * 16 / C::kBlockCols) * C::kBlockBytes + (kk * 16 % C::kBlockCols) * 2;
+}
+template <int D>
+__device__ __forceinline__ uint64_t kmajor_desc0(uint32_t tile) {
+  using C = TileCfg<D>;
+  return sdesc(tile, 16, C::kSBO, C::kSwizzle);
 }
 // MN-major operand (N = D columns, K = 128 rows) at row offset kk*16.
 template <int D>
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+__device__ __forceinline__ uint64_t mnmajor_desc0(uint32_t tile) {
   using C = TileCfg<D>;
-  return sdesc(tile + kk * 16 * C::kRowBytes, C::kBlockBytes, C::kSBO, C::kSwizzle);
+  return sdesc(tile, C::kBlockBytes, C::kSBO, C::kSwizzle);
 }
 
-// C(tmem) = A_tile(128 x D) * B_tile(128 x D)^T : both K-major.
+// C(tmem) = A_tile(128 x D) * B_tile(128 x D)^T : both K-major.  Called by
+// the whole MMA warp; `leader` issues.
 template <int D>
-__device__ __forceinline__ void mma_tile_nt(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
+__device__ __forceinline__ void mma_tile_nt(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile, bool leader) {
   constexpr uint32_t idesc = idesc_bf16(kTile, kTile, 0, 0);
+  const uint64_t a0 = kmajor_desc0<D>(a_tile), b0 = kmajor_desc0<D>(b_tile);
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
-    mma_ss(d_tmem, kmajor_desc<D>(a_tile, kk), kmajor_desc<D>(b_tile, kk), idesc, kk > 0 ? 1u : 0u);
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = kmajor_off<D>(kk) >> 4;
+    if (leader) mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+  }
 }
-// C(tmem, 128 x D) (+)= A(tmem, 128 x 128 bf16, split halves) * B_tile(128 x D, MN-major)
+// C(tmem, 128 x D) (+)= X(128 x 128, K-major, 128-byte swizzle) * B_tile(128 x D, MN-major)
 template <int D>
-__device__ __forceinline__ void mma_tile_tn(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_tile,
-                                            bool accumulate) {
+__device__ __forceinline__ void mma_tile_xs(uint32_t d_tmem, uint32_t x_tile, uint32_t b_tile, bool accumulate,
+                                            bool leader) {
+  using C = TileCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(kTile, D, 0, 1);
+  const uint64_t a0 = kmajor_desc0<kTile>(x_tile), b0 = mnmajor_desc0<D>(b_tile);
 #pragma unroll
   for (int kk = 0; kk < kTile / 16; ++kk) {
-    const uint32_t a = kk < 4 ? a_lo + kk * 8 : a_hi + (kk - 4) * 8;
-    mma_ts(d_tmem, a, mnmajor_desc<D>(b_tile, kk), idesc, (accumulate || kk > 0) ? 1u : 0u);
+    const uint64_t aoff = kmajor_off<kTile>(kk) >> 4;
+    const uint64_t boff = static_cast<uint64_t>(kk * 16 * C::kRowBytes) >> 4;
+    if (leader) mma_ss(d_tmem, a0 + aoff, b0 + boff, idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -145,95 +171,116 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int idx) {
 
 // ----------------------------------------------------------------- producer
 // Resident pair: (K, V) of the unit (dkdv) or (Q, dO) (dq).  Streamed pairs:
-// (Q, dO) of each query tile (dkdv) or (K, V) of each key tile (dq).
-template <int D, bool KV_MAJOR>
+// (Q, dO) of each query tile (dkdv) or (K, V) of each key tile (dq).  Two
+// producer threads: STREAM 0 loads the resident pair and stream A, STREAM 1
+// stream B, so that a full ring of one stream never holds up the other.
+template <int D, bool KV_MAJOR, int STREAM>
 __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, int n_units, Fail fail) {
   using C = BwdCfg<D, KV_MAJOR>;
+  constexpr int kStages = STREAM == 0 ? C::kStagesA : C::kStagesB;
   const CUtensorMap* res0 = KV_MAJOR ? &p.tm_k : &p.tm_q;
   const CUtensorMap* res1 = KV_MAJOR ? &p.tm_v : &p.tm_do;
-  const CUtensorMap* str0 = KV_MAJOR ? &p.tm_q : &p.tm_k;
-  const CUtensorMap* str1 = KV_MAJOR ? &p.tm_do : &p.tm_v;
+  const CUtensorMap* str = STREAM == 0 ? (KV_MAJOR ? &p.tm_q : &p.tm_k) : (KV_MAJOR ? &p.tm_do : &p.tm_v);
+  uint64_t* full = STREAM == 0 ? bars->a_full : bars->b_full;
+  uint64_t* empty = STREAM == 0 ? bars->a_empty : bars->b_empty;
+  uint8_t* ring = smem + (STREAM == 0 ? C::kAOff : C::kBOff);
   uint32_t res_it = 0, st_it = 0;
+  const bool leader = elect_one();
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
     if (idx >= n_units) break;
     const BwdUnit u = bwd_unit<KV_MAJOR>(p, idx);
     if (u.count == 0) continue;
-    if (!(ok = mbar_wait(&bars->res_empty, (res_it & 1) ^ 1, fail))) break;
-    ++res_it;
-    {
+    if constexpr (STREAM == 0) {
+      if (!(ok = mbar_wait_warp(&bars->res_empty, (res_it & 1) ^ 1, fail))) break;
+      ++res_it;
       const int row = (KV_MAJOR ? u.seg.k0 : u.seg.q0) + u.tile * kTile;
-      mbar_arrive_tx(&bars->res_full, 2 * C::kTileBytes);
-      uint8_t* d0 = smem + C::kResOff;
+      if (leader) {
+        mbar_arrive_tx(&bars->res_full, 2 * C::kTileBytes);
+        uint8_t* d0 = smem + C::kResOff;
 #pragma unroll
-      for (int cb = 0; cb < C::kNumBlocks; ++cb) {
-        tma_load_3d(d0 + cb * C::kBlockBytes, res0, &bars->res_full, cb * C::kBlockCols, u.h, row);
-        tma_load_3d(d0 + C::kTileBytes + cb * C::kBlockBytes, res1, &bars->res_full, cb * C::kBlockCols, u.h,
-                    row);
+        for (int cb = 0; cb < C::kNumBlocks; ++cb) {
+          tma_load_3d(d0 + cb * C::kBlockBytes, res0, &bars->res_full, cb * C::kBlockCols, u.h, row);
+          tma_load_3d(d0 + C::kTileBytes + cb * C::kBlockBytes, res1, &bars->res_full, cb * C::kBlockCols, u.h,
+                      row);
+        }
       }
     }
     for (int i = 0; i < u.count; ++i) {
       const int row = (KV_MAJOR ? u.seg.q0 : u.seg.k0) + (u.first + i) * kTile;
-      const int sa = st_it % C::kStagesA, sb = st_it % C::kStagesB;
-      if (!(ok = mbar_wait(&bars->a_empty[sa], ((st_it / C::kStagesA) & 1) ^ 1, fail))) break;
-      mbar_arrive_tx(&bars->a_full[sa], C::kTileBytes);
-      uint8_t* da = smem + C::kAOff + sa * C::kTileBytes;
+      const int st = st_it % kStages;
+      if (!(ok = mbar_wait_warp(&empty[st], ((st_it / kStages) & 1) ^ 1, fail))) break;
+      if (leader) {
+        mbar_arrive_tx(&full[st], C::kTileBytes);
+        uint8_t* dst = ring + st * C::kTileBytes;
 #pragma unroll
-      for (int cb = 0; cb < C::kNumBlocks; ++cb)
-        tma_load_3d(da + cb * C::kBlockBytes, str0, &bars->a_full[sa], cb * C::kBlockCols, u.h, row);
-      if (!(ok = mbar_wait(&bars->b_empty[sb], ((st_it / C::kStagesB) & 1) ^ 1, fail))) break;
-      mbar_arrive_tx(&bars->b_full[sb], C::kTileBytes);
-      uint8_t* db = smem + C::kBOff + sb * C::kTileBytes;
-#pragma unroll
-      for (int cb = 0; cb < C::kNumBlocks; ++cb)
-        tma_load_3d(db + cb * C::kBlockBytes, str1, &bars->b_full[sb], cb * C::kBlockCols, u.h, row);
+        for (int cb = 0; cb < C::kNumBlocks; ++cb)
+          tma_load_3d(dst + cb * C::kBlockBytes, str, &full[st], cb * C::kBlockCols, u.h, row);
+      }
       ++st_it;
     }
   }
   if (!ok) {
-    if (res_it) mbar_wait_drain(&bars->res_full, (res_it - 1) & 1);
-    for (uint32_t i = st_it > C::kStagesA ? st_it - C::kStagesA : 0; i < st_it; ++i)
-      mbar_wait_drain(&bars->a_full[i % C::kStagesA], (i / C::kStagesA) & 1);
-    for (uint32_t i = st_it > C::kStagesB ? st_it - C::kStagesB : 0; i < st_it; ++i)
-      mbar_wait_drain(&bars->b_full[i % C::kStagesB], (i / C::kStagesB) & 1);
+    if (STREAM == 0 && res_it) mbar_wait_drain(&bars->res_full, (res_it - 1) & 1);
+    for (uint32_t i = st_it > kStages ? st_it - kStages : 0; i < st_it; ++i)
+      mbar_wait_drain(&full[i % kStages], (i / kStages) & 1);
   }
 }
 
 // ---------------------------------------------------------------- MMA issuer
-// dkdv.  Issue order over query tiles i:
-//   S^T(0), dP^T(0), { [P^T(i) ready] dV(i), [dS^T(i) ready] dK(i),
-//   S^T(i+1), dP^T(i+1) }
-// The tensor core pays a pipeline switch whenever it alternates between MMAs
-// that read A from shared memory (S^T, dP^T) and from TMEM (dV, dK), so the
-// two kinds are issued in pairs: two switches per query tile.  S^T(i+1) and
-// dP^T(i+1) overwrite the TMEM columns that dV(i) and dK(i) read; they are
-// issued after them and MMAs execute in issue order.
+// Counters of the hand-offs between the MMA issuer and the activation warps.
+// Waits on an "empty"/"free" barrier use parity (n & 1) ^ 1 for the n-th use,
+// which passes at once on a fresh barrier.
+struct XRing {
+  uint32_t n = 0;  // X tiles written so far
+  template <int NX>
+  __device__ __forceinline__ int slot() const { return static_cast<int>(n % NX); }
+  template <int NX>
+  __device__ __forceinline__ uint32_t full_parity() const { return (n / NX) & 1; }
+  template <int NX>
+  __device__ __forceinline__ uint32_t empty_parity() const { return ((n / NX) & 1) ^ 1; }
+};
+
+// dkdv.  Per query tile i the issuer waits for the activation warps'
+// hand-offs in the order they happen:
+//   [S^T(i) loaded]  S^T(i+1) = K Q(i+1)^T
+//   [P^T(i) in X]    dV += P^T(i) dO(i)
+//   [dP^T(i) loaded] dP^T(i+1) = V dO(i+1)^T
+//   [dS^T(i) in X]   dK += dS^T(i) Q(i)
+// so S^T(i+1) and dP^T(i+1) run while the activation warps work on tile i.
 template <int D>
 __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                            Fail fail) {
   using C = BwdCfg<D, true>;
   const uint32_t k_t = smem_u32(smem + C::kResOff), v_t = k_t + C::kTileBytes;
   const uint32_t a_base = smem_u32(smem + C::kAOff), b_base = smem_u32(smem + C::kBOff);
-  uint32_t res_it = 0, st_it = 0, p_it = 0, acc_it = 0;
+  const uint32_t x_base = smem_u32(smem + C::kXOff);
+  uint32_t res_it = 0, st_it = 0, acc_it = 0, s_n = 0, dp_n = 0;
+  XRing x;
+  const bool leader = elect_one();
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
     if (idx >= n_units) break;
     const BwdUnit u = bwd_unit<true>(p, idx);
     if (u.count == 0) continue;
-    if (!(ok = mbar_wait(&bars->res_full, res_it & 1, fail))) break;
+    if (!(ok = mbar_wait_warp(&bars->res_full, res_it & 1, fail))) break;
     ++res_it;
     {  // S^T and dP^T of the first query tile
       const int sa = st_it % C::kStagesA, sb = st_it % C::kStagesB;
-      if (!(ok = mbar_wait(&bars->a_full[sa], (st_it / C::kStagesA) & 1, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->s_free, (s_n & 1) ^ 1, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->a_full[sa], (st_it / C::kStagesA) & 1, fail))) break;
       tc_fence_after();
-      mma_tile_nt<D>(tmem, k_t, a_base + sa * C::kTileBytes);  // S^T  = K  Q^T
-      mma_commit(&bars->s_full[0]);
-      if (!(ok = mbar_wait(&bars->b_full[sb], (st_it / C::kStagesB) & 1, fail))) break;
+      mma_tile_nt<D>(tmem, k_t, a_base + sa * C::kTileBytes, leader);  // S^T = K Q^T
+      if (leader) mma_commit(&bars->s_full);
+      ++s_n;
+      if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->b_full[sb], (st_it / C::kStagesB) & 1, fail))) break;
       tc_fence_after();
-      mma_tile_nt<D>(tmem + 128, v_t, b_base + sb * C::kTileBytes);  // dP^T = V  dO^T
-      mma_commit(&bars->dp_full);
+      mma_tile_nt<D>(tmem + 128, v_t, b_base + sb * C::kTileBytes, leader);  // dP^T = V dO^T
+      if (leader) mma_commit(&bars->dp_full);
+      ++dp_n;
     }
     for (int i = 0; i < u.count; ++i) {
       const uint32_t it = st_it + i;
@@ -241,97 +288,135 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
       const int sa1 = (it + 1) % C::kStagesA, sb1 = (it + 1) % C::kStagesB;
       const uint32_t q_t = a_base + sa * C::kTileBytes, do_t = b_base + sb * C::kTileBytes;
       const bool more = i + 1 < u.count;
+      if (more) {  // S^T of the next query tile, once S^T(i) is in registers
+        if (!(ok = mbar_wait_warp(&bars->s_free, (s_n & 1) ^ 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
+        tc_fence_after();
+        mma_tile_nt<D>(tmem, k_t, a_base + sa1 * C::kTileBytes, leader);
+        if (leader) mma_commit(&bars->s_full);
+        ++s_n;
+      }
       if (i == 0) {
-        if (!(ok = mbar_wait(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
         ++acc_it;
       }
-      if (!(ok = mbar_wait(&bars->p_full, p_it & 1, fail))) break;
-      tc_fence_after();
-      mma_tile_tn<D>(tmem + 256, tmem + 0, tmem + 64, do_t, i > 0);  // dV += P^T dO
-      mma_commit(&bars->b_empty[sb]);  // dO(i) fully read once dV(i) completes
-      if (!(ok = mbar_wait(&bars->ds_full, p_it & 1, fail))) break;
-      ++p_it;
-      tc_fence_after();
-      mma_tile_tn<D>(tmem + 256 + D, tmem + 128, tmem + 192, q_t, i > 0);  // dK += dS^T Q
-      mma_commit(&bars->a_empty[sa]);  // Q(i) fully read once dK(i) completes
-      if (more) {
-        if (!(ok = mbar_wait(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
+      {  // dV += P^T dO
+        const int xs = x.slot<C::kNumX>();
+        if (!(ok = mbar_wait_warp(&bars->x_full[xs], x.full_parity<C::kNumX>(), fail))) break;
         tc_fence_after();
-        mma_tile_nt<D>(tmem, k_t, a_base + sa1 * C::kTileBytes);  // S^T of the next query tile
-        mma_commit(&bars->s_full[0]);
-        if (!(ok = mbar_wait(&bars->b_full[sb1], ((it + 1) / C::kStagesB) & 1, fail))) break;
+        mma_tile_xs<D>(tmem + 256, x_base + xs * C::kXBytes, do_t, i > 0, leader);
+        if (leader) mma_commit(&bars->x_empty[xs]);
+        if (leader) mma_commit(&bars->b_empty[sb]);  // dO(i): dP^T(i) and dV(i) issued
+        ++x.n;
+      }
+      if (more) {  // dP^T of the next query tile, once dP^T(i) is in registers
+        if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->b_full[sb1], ((it + 1) / C::kStagesB) & 1, fail))) break;
         tc_fence_after();
-        mma_tile_nt<D>(tmem + 128, v_t, b_base + sb1 * C::kTileBytes);  // dP^T of the next query tile
-        mma_commit(&bars->dp_full);
+        mma_tile_nt<D>(tmem + 128, v_t, b_base + sb1 * C::kTileBytes, leader);
+        if (leader) mma_commit(&bars->dp_full);
+        ++dp_n;
+      }
+      {  // dK += dS^T Q
+        const int xs = x.slot<C::kNumX>();
+        if (!(ok = mbar_wait_warp(&bars->x_full[xs], x.full_parity<C::kNumX>(), fail))) break;
+        tc_fence_after();
+        mma_tile_xs<D>(tmem + 256 + D, x_base + xs * C::kXBytes, q_t, i > 0, leader);
+        if (leader) mma_commit(&bars->x_empty[xs]);
+        if (leader) mma_commit(&bars->a_empty[sa]);  // Q(i): S^T(i) and dK(i) issued
+        ++x.n;
       }
     }
     if (!ok) break;
     st_it += u.count;
-    mma_commit(&bars->acc_full);
-    mma_commit(&bars->res_empty);
+    if (leader) mma_commit(&bars->acc_full);
+    if (leader) mma_commit(&bars->res_empty);
   }
-  mma_commit(&bars->drain);
+  if (leader) mma_commit(&bars->drain);
   mbar_wait_drain(&bars->drain, 0);
 }
 
-// dq, per key tile i (S buffers alternate): dP(i), S(i+1), [dS(i) ready] dQ.
+// dq.  Per key tile i:
+//   [S(i) loaded]  S(i+1) = Q K(i+1)^T
+//   [dS(i) in X]   dQ += dS(i) K(i)
+//   [dP(i) loaded] dP(i+1) = dO V(i+1)^T
+// dP(i+1) goes last because with a single V stage its operand can only land
+// after dP(i) has completed.
 template <int D>
 __device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                           Fail fail) {
   using C = BwdCfg<D, false>;
   const uint32_t q_t = smem_u32(smem + C::kResOff), do_t = q_t + C::kTileBytes;
   const uint32_t a_base = smem_u32(smem + C::kAOff), b_base = smem_u32(smem + C::kBOff);
-  const uint32_t t_s[2] = {tmem, tmem + 384};
-  uint32_t res_it = 0, st_it = 0, ds_it = 0, acc_it = 0, s_cnt = 0;
+  const uint32_t x_base = smem_u32(smem + C::kXOff);
+  uint32_t res_it = 0, st_it = 0, acc_it = 0, s_n = 0, dp_n = 0;
+  XRing x;
+  const bool leader = elect_one();
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
     if (idx >= n_units) break;
     const BwdUnit u = bwd_unit<false>(p, idx);
     if (u.count == 0) continue;
-    if (!(ok = mbar_wait(&bars->res_full, res_it & 1, fail))) break;
+    if (!(ok = mbar_wait_warp(&bars->res_full, res_it & 1, fail))) break;
     ++res_it;
-    {  // S of the first key tile
-      const int sa = st_it % C::kStagesA;
-      if (!(ok = mbar_wait(&bars->a_full[sa], (st_it / C::kStagesA) & 1, fail))) break;
+    {  // S and dP of the first key tile
+      const int sa = st_it % C::kStagesA, sb = st_it % C::kStagesB;
+      if (!(ok = mbar_wait_warp(&bars->s_free, (s_n & 1) ^ 1, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->a_full[sa], (st_it / C::kStagesA) & 1, fail))) break;
       tc_fence_after();
-      mma_tile_nt<D>(t_s[s_cnt & 1], q_t, a_base + sa * C::kTileBytes);
-      mma_commit(&bars->s_full[s_cnt & 1]);
+      mma_tile_nt<D>(tmem, q_t, a_base + sa * C::kTileBytes, leader);  // S = Q K^T
+      if (leader) mma_commit(&bars->s_full);
+      ++s_n;
+      if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->b_full[sb], (st_it / C::kStagesB) & 1, fail))) break;
+      tc_fence_after();
+      mma_tile_nt<D>(tmem + 128, do_t, b_base + sb * C::kTileBytes, leader);  // dP = dO V^T
+      if (leader) mma_commit(&bars->dp_full);
+      if (leader) mma_commit(&bars->b_empty[sb]);  // V is read by dP only
+      ++dp_n;
     }
     for (int i = 0; i < u.count; ++i) {
       const uint32_t it = st_it + i;
-      const int sa = it % C::kStagesA, sb = it % C::kStagesB;
-      const uint32_t k_t = a_base + sa * C::kTileBytes, v_t = b_base + sb * C::kTileBytes;
-      const uint32_t sbuf = (s_cnt + i) & 1;
-      if (!(ok = mbar_wait(&bars->b_full[sb], (it / C::kStagesB) & 1, fail))) break;
-      tc_fence_after();
-      mma_tile_nt<D>(tmem + 128, do_t, v_t);  // dP = dO V^T
-      mma_commit(&bars->dp_full);
-      mma_commit(&bars->b_empty[sb]);  // V(i) fully read once dP(i) completes
-      if (i + 1 < u.count) {  // S of the next key tile into the other buffer
-        const int sa1 = (it + 1) % C::kStagesA;
-        if (!(ok = mbar_wait(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
+      const int sa = it % C::kStagesA;
+      const int sa1 = (it + 1) % C::kStagesA, sb1 = (it + 1) % C::kStagesB;
+      const uint32_t k_t = a_base + sa * C::kTileBytes;
+      const bool more = i + 1 < u.count;
+      if (more) {
+        if (!(ok = mbar_wait_warp(&bars->s_free, (s_n & 1) ^ 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
         tc_fence_after();
-        mma_tile_nt<D>(t_s[sbuf ^ 1], q_t, a_base + sa1 * C::kTileBytes);
-        mma_commit(&bars->s_full[sbuf ^ 1]);
+        mma_tile_nt<D>(tmem, q_t, a_base + sa1 * C::kTileBytes, leader);
+        if (leader) mma_commit(&bars->s_full);
+        ++s_n;
       }
       if (i == 0) {
-        if (!(ok = mbar_wait(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
         ++acc_it;
       }
-      if (!(ok = mbar_wait(&bars->ds_full, ds_it & 1, fail))) break;
-      ++ds_it;
+      const int xs = x.slot<C::kNumX>();
+      if (!(ok = mbar_wait_warp(&bars->x_full[xs], x.full_parity<C::kNumX>(), fail))) break;
       tc_fence_after();
-      mma_tile_tn<D>(tmem + 256, t_s[sbuf], t_s[sbuf] + 64, k_t, i > 0);  // dQ += dS K
-      mma_commit(&bars->a_empty[sa]);  // K(i) fully read once dQ(i) completes
+      mma_tile_xs<D>(tmem + 256, x_base + xs * C::kXBytes, k_t, i > 0, leader);  // dQ += dS K
+      if (leader) mma_commit(&bars->x_empty[xs]);
+      if (leader) mma_commit(&bars->a_empty[sa]);  // K(i): S(i) and dQ(i) issued
+      ++x.n;
+      if (more) {
+        if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->b_full[sb1], ((it + 1) / C::kStagesB) & 1, fail))) break;
+        tc_fence_after();
+        mma_tile_nt<D>(tmem + 128, do_t, b_base + sb1 * C::kTileBytes, leader);
+        if (leader) mma_commit(&bars->dp_full);
+        if (leader) mma_commit(&bars->b_empty[sb1]);
+        ++dp_n;
+      }
     }
     if (!ok) break;
     st_it += u.count;
-    s_cnt += u.count;
-    mma_commit(&bars->acc_full);
-    mma_commit(&bars->res_empty);
+    if (leader) mma_commit(&bars->acc_full);
+    if (leader) mma_commit(&bars->res_empty);
   }
-  mma_commit(&bars->drain);
+  if (leader) mma_commit(&bars->drain);
   mbar_wait_drain(&bars->drain, 0);
 }
 
@@ -469,6 +554,14 @@ __device__ __forceinline__ void phase_b_chunk(const uint32_t (&dv)[32], const fl
   }
 }
 
+// Stores this thread's 32 packed bf16 pairs of one chunk (columns
+// [64 half + 32 chunk, +32) of row r) into an X tile.
+__device__ __forceinline__ void store_x_chunk(uint32_t x_tile, int half, int chunk, int r, const uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared_v4(swz128_addr(x_tile, half, r, 4 * chunk + j), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+}
+
 template <int D, int ACT, bool KV_MAJOR>
 __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units, Fail fail) {
   using C = BwdCfg<D, KV_MAJOR>;
@@ -477,14 +570,15 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
   const int quad = warp & 3;
   const int half = (warp - 4) >> 2;                // which 64 columns this warpgroup owns
   const int r = quad * 32 + (threadIdx.x & 31);    // row of this unit's own tile
-  const int act_tid = threadIdx.x - 128;           // 0..255 over both warpgroups
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t t_s = tmem + lane_off + 64 * half;
   const uint32_t t_dp = tmem + lane_off + 128 + 64 * half;
+  const uint32_t x_base = smem_u32(smem + C::kXOff);
   const int H = p.heads;
   const bool want_dbias = KV_MAJOR && p.dbias_part != nullptr;
   const int R = (p.bias_len - 1) / 2;
-  float* sbias = reinterpret_cast<float*>(smem + C::kBiasOff);
-  uint32_t s_it = 0, dp_it = 0, acc_it = 0, grp_it = 0;
+  uint32_t s_it = 0, dp_it = 0, acc_it = 0;
+  XRing x;
   const float hs = 0.5f * p.scale;                 // x / 2 = hs S + bias / 2
   const float s2 = p.scale * kLog2e;               // softmax: x log2 e
 
@@ -496,6 +590,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     const bool row_ok = r < u.rows;
     const int64_t grow = static_cast<int64_t>(KV_MAJOR ? u.seg.k0 : u.seg.q0) + u.tile * kTile + r;
     const float* brow = p.bias_len ? p.bias + static_cast<int64_t>(u.h) * p.bias_len : nullptr;
+    float* part = want_dbias ? p.dbias_part + (static_cast<int64_t>(blockIdx.x) * H + u.h) * p.bias_len : nullptr;
     float acc_lo = 0.f, acc_hi = 0.f;  // dbias mass clamped to the table's ends
 
     if (u.count == 0) {  // no partner rows: the gradient rows are zero
@@ -526,25 +621,24 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     for (int i = 0; i < u.count; ++i) {
       const int pt = u.first + i;  // partner tile
       const PairGeom g = pair_geom<KV_MAJOR>(p, u, pt, r, row_ok, brow, R);
-      // S buffer of this tile: dkdv always columns 0; dq alternates 0 / 384
-      const uint32_t sbuf = KV_MAJOR ? 0u : ((s_it & 1) ? 384u : 0u);
-      const uint32_t t_s = tmem + lane_off + sbuf + 64 * half;
-      uint64_t* sfull = &bars->s_full[KV_MAJOR ? 0 : (s_it & 1)];
-      const uint32_t sphase = KV_MAJOR ? (s_it & 1) : ((s_it >> 1) & 1);
-      if (!(ok = mbar_wait(sfull, sphase, fail))) break;
+
+      // ---- S (S^T) of this tile into registers; its TMEM columns go back to
+      // the MMA issuer for the next tile
+      if (!(ok = mbar_wait(&bars->s_full, s_it & 1, fail))) break;
       ++s_it;
       tc_fence_after();
-
-      // ---- phase A: S -> (P, act'(x)) [softmax: P]; P^T to TMEM (dkdv)
-      // (chunk 1's TMEM load is in flight while chunk 0 is computed and stored)
-      float keep0[32], keep1[32];  // act'(x) (GELU/SiLU) or P (softmax) per owned column
       uint32_t sv0[32], sv1[32];
       tmem_ld32(t_s, sv0);
-      tmem_ld_wait(sv0);
+      tmem_ld32(t_s + 32, sv1);
+      tmem_ld_wait2(sv0, sv1);
+      tc_fence_before();
+      mbar_arrive_warp(&bars->s_free);
+
+      // ---- phase A: S -> (P, act'(x)) [softmax: P]; P^T to X (dkdv)
+      float keep0[32], keep1[32];  // act'(x) (GELU/SiLU) or P (softmax) per owned column
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int cbase = 64 * half + 32 * chunk;
-        if (chunk == 0) tmem_ld32(t_s + 32, sv1);
         const uint32_t(&sv)[32] = chunk == 0 ? sv0 : sv1;
         float lse_c[32];
         if constexpr (kSoftmax && KV_MAJOR) {
@@ -571,29 +665,35 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
           }
         }
 #undef JG_PHASE_A
-        if constexpr (KV_MAJOR) tmem_st16(t_s + 16 * chunk, pk);  // P^T over S^T columns already read
-        if (chunk == 0) tmem_ld_wait(sv1);
+        if constexpr (KV_MAJOR) {
+          if (chunk == 0 && !(ok = mbar_wait(&bars->x_empty[x.slot<C::kNumX>()], x.empty_parity<C::kNumX>(), fail)))
+            break;
+          store_x_chunk(x_base + x.slot<C::kNumX>() * C::kXBytes, half, chunk, r, pk);
+        }
       }
+      if (!ok) break;
       if constexpr (KV_MAJOR) {
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full);
+        fence_proxy_async_smem();
+        mbar_arrive_warp(&bars->x_full[x.slot<C::kNumX>()]);
+        ++x.n;
       }
 
-      // ---- phase B: dP -> dS (bf16 into TMEM), dbias partial sums
+      // ---- phase B: dP -> dS (bf16 into X), dbias partial sums
       if (!(ok = mbar_wait(&bars->dp_full, dp_it & 1, fail))) break;
       ++dp_it;
       tc_fence_after();
+      uint32_t dv0[32], dv1[32];
+      tmem_ld32(t_dp, dv0);
+      tmem_ld32(t_dp + 32, dv1);
+      tmem_ld_wait2(dv0, dv1);
+      tc_fence_before();
+      mbar_arrive_warp(&bars->dp_free);
       float2 row_sum = f2(0.f);
       float dacc[3] = {0.f, 0.f, 0.f};
       const int dmode = !want_dbias ? 0 : (g.band ? 2 : 1);
-      uint32_t dv0[32], dv1[32];
-      tmem_ld32(t_dp, dv0);
-      tmem_ld_wait(dv0);
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int cbase = 64 * half + 32 * chunk;
-        if (chunk == 0) tmem_ld32(t_dp + 32, dv1);
         const uint32_t(&dv)[32] = chunk == 0 ? dv0 : dv1;
         float del_c[32];
         if constexpr (kSoftmax && KV_MAJOR) {
@@ -615,10 +715,14 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         }
 #undef JG_PHASE_B
 #undef JG_PHASE_B1
-        // dS^T over dP^T columns (dkdv) / dS over S columns (dq), already read
-        tmem_st16((KV_MAJOR ? t_dp : t_s) + 16 * chunk, pk);
-        if (chunk == 0) tmem_ld_wait(dv1);
+        if (chunk == 0 && !(ok = mbar_wait(&bars->x_empty[x.slot<C::kNumX>()], x.empty_parity<C::kNumX>(), fail)))
+          break;
+        store_x_chunk(x_base + x.slot<C::kNumX>() * C::kXBytes, half, chunk, r, pk);
       }
+      if (!ok) break;
+      fence_proxy_async_smem();
+      mbar_arrive_warp(&bars->x_full[x.slot<C::kNumX>()]);
+      ++x.n;
       if (dmode == 1) {
         if (g.upper) acc_hi += row_sum.x + row_sum.y;  // the whole tile clamps to one end of the table
         else acc_lo += row_sum.x + row_sum.y;
@@ -630,12 +734,9 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
           const int rel = rel1 + 32 * (k - 1);
           if (rel >= R) acc_hi += dacc[k];
           else if (rel <= -R) acc_lo += dacc[k];
-          else atomicAdd(sbias + rel + R, dacc[k]);
+          else atomicAdd(part + rel + R, dacc[k]);
         }
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->ds_full);
     }
     if (!ok) break;
 
@@ -687,31 +788,20 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       }
     }
     tc_fence_before();
-    mbar_arrive(&bars->acc_empty);
+    mbar_arrive_warp(&bars->acc_empty);
 
     if (want_dbias) {
-      // fold the clamped mass, then flush this unit's partial sums to the
-      // CTA's private slice and clear them (bounded group syncs of the 256
-      // activation threads)
+      // the clamped mass of this unit: one red per warp and table end into
+      // this CTA's private slice
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         acc_lo += __shfl_xor_sync(0xffffffffu, acc_lo, o);
         acc_hi += __shfl_xor_sync(0xffffffffu, acc_hi, o);
       }
       if ((threadIdx.x & 31) == 0) {
-        atomicAdd(sbias, acc_lo);
-        atomicAdd(sbias + 2 * R, acc_hi);
+        atomicAdd(part, acc_lo);
+        atomicAdd(part + 2 * R, acc_hi);
       }
-      mbar_arrive(&bars->grp[0]);
-      if (!mbar_wait(&bars->grp[0], grp_it & 1, fail)) break;
-      float* part = p.dbias_part + (static_cast<int64_t>(blockIdx.x) * H + u.h) * p.bias_len;
-      for (int e = act_tid; e < p.bias_len; e += 256) {
-        part[e] += sbias[e];
-        sbias[e] = 0.f;
-      }
-      mbar_arrive(&bars->grp[1]);
-      if (!mbar_wait(&bars->grp[1], grp_it & 1, fail)) break;
-      ++grp_it;
     }
   }
 }
@@ -724,20 +814,20 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kBarOff);
   const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&bars->res_full, 1);
     mbar_init(&bars->res_empty, 1);
-    mbar_init(&bars->s_full[0], 1);
-    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 8);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_full, 256);
-    mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->dp_free, 8);
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, 256);
+    mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
-    mbar_init(&bars->grp[0], 256);
-    mbar_init(&bars->grp[1], 256);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->x_full[s], 8);
+      mbar_init(&bars->x_empty[s], 1);
+    }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->a_full[s], 1);
       mbar_init(&bars->a_empty[s], 1);
@@ -751,10 +841,6 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
-  if (KV_MAJOR && p.dbias_part != nullptr) {  // per-CTA dbias accumulator starts at zero
-    float* sbias = reinterpret_cast<float*>(smem + C::kBiasOff);
-    for (int e = threadIdx.x; e < p.bias_len; e += blockDim.x) sbias[e] = 0.f;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -763,14 +849,12 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
   if (*reinterpret_cast<volatile int*>(p.status) != kOk) n_units = 0;
   Fail fail{&bars->abort, p.status};
   if (warp == 0) {
-    if (lane == 0) bwd_producer<D, KV_MAJOR>(p, smem, bars, n_units, fail);
-    __syncwarp();
+    bwd_producer<D, KV_MAJOR, 0>(p, smem, bars, n_units, fail);
+  } else if (warp == 2) {
+    bwd_producer<D, KV_MAJOR, 1>(p, smem, bars, n_units, fail);
   } else if (warp == 1) {
-    if (lane == 0) {
-      if constexpr (KV_MAJOR) bwd_mma_kv<D>(p, smem, bars, tmem, n_units, fail);
-      else bwd_mma_q<D>(p, smem, bars, tmem, n_units, fail);
-    }
-    __syncwarp();
+    if constexpr (KV_MAJOR) bwd_mma_kv<D>(p, smem, bars, tmem, n_units, fail);
+    else bwd_mma_q<D>(p, smem, bars, tmem, n_units, fail);
   } else if (warp >= 4) {
     bwd_act<D, ACT, KV_MAJOR>(p, smem, bars, tmem, n_units, fail);
   }

@@ -109,6 +109,7 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
   using C = FwdCfg<D>;
   uint32_t q_it[2] = {0, 0};
   uint32_t kv_it = 0;
+  const bool leader = elect_one();
   bool ok = true;
   for (int r = 0;; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
@@ -117,14 +118,16 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
     if (u.nkv == 0) continue;
     for (int s = 0; s < 2 && ok; ++s) {
       if (u.nkv_s[s] == 0) continue;
-      ok = mbar_wait(&bars->q_empty[s], (q_it[s] & 1) ^ 1, fail);
+      ok = mbar_wait_warp(&bars->q_empty[s], (q_it[s] & 1) ^ 1, fail);
       if (!ok) break;
-      mbar_arrive_tx(&bars->q_full[s], C::kTileBytes);
-      uint8_t* dst = smem + C::kQOff + s * C::kTileBytes;
-      const int row = u.seg.q0 + (2 * u.pair + s) * kTile;
+      if (leader) {
+        mbar_arrive_tx(&bars->q_full[s], C::kTileBytes);
+        uint8_t* dst = smem + C::kQOff + s * C::kTileBytes;
+        const int row = u.seg.q0 + (2 * u.pair + s) * kTile;
 #pragma unroll
-      for (int cb = 0; cb < C::kNumBlocks; ++cb)
-        tma_load_3d(dst + cb * C::kBlockBytes, &p.tm_q, &bars->q_full[s], cb * C::kBlockCols, u.h, row);
+        for (int cb = 0; cb < C::kNumBlocks; ++cb)
+          tma_load_3d(dst + cb * C::kBlockBytes, &p.tm_q, &bars->q_full[s], cb * C::kBlockCols, u.h, row);
+      }
       ++q_it[s];
     }
     // K and V of a stage are released separately (K after the last S that
@@ -132,19 +135,23 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
     for (int kt = 0; kt < u.nkv && ok; ++kt) {
       const int st = kv_it % C::kStages;
       const uint32_t empty_phase = ((kv_it / C::kStages) & 1) ^ 1;
-      if (!(ok = mbar_wait(&bars->k_empty[st], empty_phase, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->k_empty[st], empty_phase, fail))) break;
       const int row = u.seg.k0 + kt * kTile;
-      mbar_arrive_tx(&bars->k_full[st], C::kTileBytes);
-      uint8_t* kd = smem + C::kKOff + st * C::kTileBytes;
+      if (leader) {
+        mbar_arrive_tx(&bars->k_full[st], C::kTileBytes);
+        uint8_t* kd = smem + C::kKOff + st * C::kTileBytes;
 #pragma unroll
-      for (int cb = 0; cb < C::kNumBlocks; ++cb)
-        tma_load_3d(kd + cb * C::kBlockBytes, &p.tm_k, &bars->k_full[st], cb * C::kBlockCols, u.h, row);
-      if (!(ok = mbar_wait(&bars->v_empty[st], empty_phase, fail))) break;
-      mbar_arrive_tx(&bars->v_full[st], C::kTileBytes);
-      uint8_t* vd = smem + C::kVOff + st * C::kTileBytes;
+        for (int cb = 0; cb < C::kNumBlocks; ++cb)
+          tma_load_3d(kd + cb * C::kBlockBytes, &p.tm_k, &bars->k_full[st], cb * C::kBlockCols, u.h, row);
+      }
+      if (!(ok = mbar_wait_warp(&bars->v_empty[st], empty_phase, fail))) break;
+      if (leader) {
+        mbar_arrive_tx(&bars->v_full[st], C::kTileBytes);
+        uint8_t* vd = smem + C::kVOff + st * C::kTileBytes;
 #pragma unroll
-      for (int cb = 0; cb < C::kNumBlocks; ++cb)
-        tma_load_3d(vd + cb * C::kBlockBytes, &p.tm_v, &bars->v_full[st], cb * C::kBlockCols, u.h, row);
+        for (int cb = 0; cb < C::kNumBlocks; ++cb)
+          tma_load_3d(vd + cb * C::kBlockBytes, &p.tm_v, &bars->v_full[st], cb * C::kBlockCols, u.h, row);
+      }
       ++kv_it;
     }
     if (!ok) break;
@@ -161,27 +168,30 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
 }
 
 // ------------------------------------------------------------- MMA issuer
+// The MMA helpers are called by the whole MMA warp (descriptors are
+// warp-uniform); `leader` issues.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr, bool leader) {
   using C = FwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(kTile, kTile, 0, 0);
+  const uint64_t a0 = sdesc(q_addr, 16, C::kSBO, C::kSwizzle), b0 = sdesc(k_addr, 16, C::kSBO, C::kSwizzle);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk * 16 / C::kBlockCols) * C::kBlockBytes + (kk * 16 % C::kBlockCols) * 2;
-    const uint64_t a = sdesc(q_addr + off, 16, C::kSBO, C::kSwizzle);
-    const uint64_t b = sdesc(k_addr + off, 16, C::kSBO, C::kSwizzle);
-    mma_ss(tmem_s, a, b, idesc, kk > 0 ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>((kk * 16 / C::kBlockCols) * C::kBlockBytes + (kk * 16 % C::kBlockCols) * 2) >> 4;
+    if (leader) mma_ss(tmem_s, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate,
+                                         bool leader) {
   using C = FwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(kTile, D, 0, 1);  // B (= V) is MN-major
+  const uint64_t b0 = sdesc(v_addr, C::kBlockBytes, C::kSBO, C::kSwizzle);
 #pragma unroll
   for (int kk = 0; kk < kTile / 16; ++kk) {
-    const uint64_t b = sdesc(v_addr + kk * 16 * C::kRowBytes, C::kBlockBytes, C::kSBO, C::kSwizzle);
-    mma_ts(tmem_o, tmem_p + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>(kk * 16 * C::kRowBytes) >> 4;
+    if (leader) mma_ts(tmem_o, tmem_p + kk * 8, b0 + off, idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -195,6 +205,7 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
   const uint32_t t_o[2] = {tmem + 256, tmem + 256 + D};
   uint32_t q_it[2] = {0, 0}, p_it[2] = {0, 0}, o_it[2] = {0, 0};
   uint32_t kv_it = 0;
+  const bool leader = elect_one();
   bool ok = true;
 
   for (int r = 0; ok; ++r) {
@@ -204,28 +215,28 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
     if (u.nkv == 0) continue;
     for (int s = 0; s < 2 && ok; ++s) {
       if (u.nkv_s[s] == 0) continue;
-      ok = mbar_wait(&bars->q_full[s], q_it[s] & 1, fail);
+      ok = mbar_wait_warp(&bars->q_full[s], q_it[s] & 1, fail);
       ++q_it[s];
     }
     if (!ok) break;
     // S(0) for both slots
     {
       const int st = kv_it % C::kStages;
-      if (!(ok = mbar_wait(&bars->k_full[st], (kv_it / C::kStages) & 1, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->k_full[st], (kv_it / C::kStages) & 1, fail))) break;
       tc_fence_after();
       for (int s = 0; s < 2; ++s) {
         if (u.nkv_s[s] == 0) continue;
-        issue_qk<D>(t_s[s], q_addr[s], k_base + st * C::kTileBytes);
-        mma_commit(&bars->s_full[s]);
-        if (u.nkv_s[s] == 1) mma_commit(&bars->q_empty[s]);
+        issue_qk<D>(t_s[s], q_addr[s], k_base + st * C::kTileBytes, leader);
+        if (leader) mma_commit(&bars->s_full[s]);
+        if (u.nkv_s[s] == 1) if (leader) mma_commit(&bars->q_empty[s]);
       }
-      mma_commit(&bars->k_empty[st]);  // both S of K(0) issued
+      if (leader) mma_commit(&bars->k_empty[st]);  // both S of K(0) issued
     }
     for (int kt = 0; kt < u.nkv && ok; ++kt) {
       const uint32_t it = kv_it + kt;
       const int st = it % C::kStages;
       const uint32_t v_addr = v_base + st * C::kTileBytes;
-      if (!(ok = mbar_wait(&bars->v_full[st], (it / C::kStages) & 1, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->v_full[st], (it / C::kStages) & 1, fail))) break;
       const bool more = kt + 1 < u.nkv;
       const int st1 = (it + 1) % C::kStages;
       // Order per tile: PV0(kt), S0(kt+1), PV1(kt), S1(kt+1).  Each slot's
@@ -235,48 +246,48 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
       // slot 0: O0 += P0 V, then S0 of the next tile
       if (kt < u.nkv_s[0]) {
         if (kt == 0) {
-          if (!(ok = mbar_wait(&bars->o_empty[0], (o_it[0] & 1) ^ 1, fail))) break;
+          if (!(ok = mbar_wait_warp(&bars->o_empty[0], (o_it[0] & 1) ^ 1, fail))) break;
           ++o_it[0];
         }
-        if (!(ok = mbar_wait(&bars->p_full[0], p_it[0] & 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->p_full[0], p_it[0] & 1, fail))) break;
         ++p_it[0];
         tc_fence_after();
-        issue_pv<D>(t_o[0], t_s[0], v_addr, kt > 0);
-        if (kt == u.nkv_s[0] - 1) mma_commit(&bars->o_full[0]);
+        issue_pv<D>(t_o[0], t_s[0], v_addr, kt > 0, leader);
+        if (kt == u.nkv_s[0] - 1) if (leader) mma_commit(&bars->o_full[0]);
       }
       if (more) {
-        if (!(ok = mbar_wait(&bars->k_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->k_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
         tc_fence_after();
         if (kt + 1 < u.nkv_s[0]) {
-          issue_qk<D>(t_s[0], q_addr[0], k_base + st1 * C::kTileBytes);
-          mma_commit(&bars->s_full[0]);
-          if (kt + 1 == u.nkv_s[0] - 1) mma_commit(&bars->q_empty[0]);
+          issue_qk<D>(t_s[0], q_addr[0], k_base + st1 * C::kTileBytes, leader);
+          if (leader) mma_commit(&bars->s_full[0]);
+          if (kt + 1 == u.nkv_s[0] - 1) if (leader) mma_commit(&bars->q_empty[0]);
         }
       }
       // slot 1: O1 += P1 V, release V, then S1 of the next tile, release K
       if (kt < u.nkv_s[1]) {
         if (kt == 0) {
-          if (!(ok = mbar_wait(&bars->o_empty[1], (o_it[1] & 1) ^ 1, fail))) break;
+          if (!(ok = mbar_wait_warp(&bars->o_empty[1], (o_it[1] & 1) ^ 1, fail))) break;
           ++o_it[1];
         }
-        if (!(ok = mbar_wait(&bars->p_full[1], p_it[1] & 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->p_full[1], p_it[1] & 1, fail))) break;
         ++p_it[1];
         tc_fence_after();
-        issue_pv<D>(t_o[1], t_s[1], v_addr, kt > 0);
-        if (kt == u.nkv_s[1] - 1) mma_commit(&bars->o_full[1]);
+        issue_pv<D>(t_o[1], t_s[1], v_addr, kt > 0, leader);
+        if (kt == u.nkv_s[1] - 1) if (leader) mma_commit(&bars->o_full[1]);
       }
-      mma_commit(&bars->v_empty[st]);  // every P V of V(kt) issued
+      if (leader) mma_commit(&bars->v_empty[st]);  // every P V of V(kt) issued
       if (more && kt + 1 < u.nkv_s[1]) {
-        issue_qk<D>(t_s[1], q_addr[1], k_base + st1 * C::kTileBytes);
-        mma_commit(&bars->s_full[1]);
-        if (kt + 1 == u.nkv_s[1] - 1) mma_commit(&bars->q_empty[1]);
+        issue_qk<D>(t_s[1], q_addr[1], k_base + st1 * C::kTileBytes, leader);
+        if (leader) mma_commit(&bars->s_full[1]);
+        if (kt + 1 == u.nkv_s[1] - 1) if (leader) mma_commit(&bars->q_empty[1]);
       }
-      if (more) mma_commit(&bars->k_empty[st1]);  // every S of K(kt+1) issued
+      if (more) if (leader) mma_commit(&bars->k_empty[st1]);  // every S of K(kt+1) issued
     }
     kv_it += u.nkv;
   }
   // Make sure every MMA issued so far has finished before TMEM is released.
-  mma_commit(&bars->drain);
+  if (leader) mma_commit(&bars->drain);
   mbar_wait_drain(&bars->drain, 0);
 }
 
@@ -489,7 +500,7 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[slot]);
+      mbar_arrive_warp(&bars->p_full[slot]);
     }
     if (!ok) break;
     // epilogue: O (TMEM) -> bf16 -> global, rows < Lq only
@@ -514,7 +525,7 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
       }
     }
     tc_fence_before();
-    mbar_arrive(&bars->o_empty[slot]);
+    mbar_arrive_warp(&bars->o_empty[slot]);
     if (kSoftmax && row_ok && p.lse)
       p.lse[static_cast<int64_t>(u.h) * p.total_q + grow] = (m_run + __log2f(l_run)) * kLn2;
   }
@@ -528,16 +539,15 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::kBarOff);
   const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->p_full[s], 4);
       mbar_init(&bars->o_full[s], 1);
-      mbar_init(&bars->o_empty[s], 128);
+      mbar_init(&bars->o_empty[s], 4);
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
@@ -562,11 +572,9 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   Fail fail{&bars->abort, p.status};
 
   if (warp == 0) {
-    if (lane == 0) fwd_producer<D>(p, smem, bars, n_units, fail);
-    __syncwarp();
+    fwd_producer<D>(p, smem, bars, n_units, fail);
   } else if (warp == 1) {
-    if (lane == 0) fwd_mma<D>(p, smem, bars, tmem, n_units, fail);
-    __syncwarp();
+    fwd_mma<D>(p, smem, bars, tmem, n_units, fail);
   } else if (warp >= 4) {
     fwd_act<D, ACT, NALU>(p, bars, tmem, (warp - 4) >> 2, n_units, fail);
   }

@@ -60,9 +60,14 @@ struct Fail {
   int* status;          // global status word of the workspace
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, Fail f) {
+// Wait for completion of the phase with the given parity; false = gave up.
+// Inline on purpose: these waits sit inside loops that keep most registers
+// live, where a call would cost saves and restores around it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Fail f) {
+  if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (;;) {
+#pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try(bar, parity)) return true;
     if (*f.abort) return false;
@@ -74,10 +79,30 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   }
 }
 
-// Wait for completion of the phase with the given parity; false = gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Fail f) {
-  if (mbar_try(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, f);
+// One arrival for the whole warp, by lane 0 after the warp has synchronised
+// (for barriers that count warps).  Each lane's own fences come first.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Issue roles (TMA producer, MMA issuer) run as whole warps: every lane walks
+// the same loop, computes the same (warp-uniform) descriptors and waits on
+// the same barriers, and one elected lane issues the asynchronous
+// instruction.  A single-lane issuer shares its scheduler with activation
+// warps whose integer and conversion work starves it of issue slots; on this
+// GPU that slowed a back-to-back MMA stream from 64 to 84-95 cycles per MMA,
+// while the whole-warp form stays at 64.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+// mbar_wait for a whole warp, with one outcome for all lanes (lane 0's).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, Fail f) {
+  return __shfl_sync(0xffffffffu, mbar_wait(bar, parity, f) ? 1 : 0, 0) != 0;
 }
 
 // Bounded wait used on the way out of a kernel (also after a failure): it
@@ -256,6 +281,24 @@ __device__ __forceinline__ float ld_nc_f32(const float* p) {
   float v;
   asm("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+// Makes this thread's shared-memory stores visible to the tensor core (the
+// async proxy) once a later mbarrier arrive is observed by the MMA issuer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One 16-byte piece of row r of a [128][128] bf16 tile stored K-major with
+// the 128-byte swizzle (two column blocks of 64 columns, 16 KB each, rows of
+// 128 bytes in 8-row atoms): piece j (0..7) of column block blk lands at
+// piece j ^ (r & 7) of its row -- the layout TMA writes and the MMA
+// descriptors with swizzle mode 2 read.
+__device__ __forceinline__ uint32_t swz128_addr(uint32_t tile, int blk, int r, int j) {
+  return tile + blk * 16384 + r * 128 + ((j ^ (r & 7)) << 4);
 }
 
 }  // namespace jg
