@@ -8,8 +8,8 @@
 //   dkdv pass, unit = (segment, head, 128-row key/value tile):
 //     for every query tile i that meets it:
 //       S^T = K Q^T, dP^T = V dO^T                       (tcgen05, TMEM)
-//       phase A: P^T = act(x)^T (bf16, to shared memory), act'(x) kept in
-//                registers (softmax: P = exp(x - LSE_i))
+//       phase A: P^T = act(x)^T (bf16, into TMEM over S^T), act'(x) kept
+//                in registers (softmax: P = exp(x - LSE_i))
 //       phase B: dS^T = dP^T act'(x)^T (softmax: P (dP - D_i)), to shared
 //                memory; dbias partial sums
 //       dV += P^T dO, dK += dS^T Q                       (tcgen05, TMEM)
@@ -20,14 +20,18 @@
 //       dQ += dS K
 //     dQ *= s; store
 //
-// Every MMA reads both operands from shared memory: the bf16 P^T / dS^T /
-// dS that the activation warps produce go to a shared "X" tile rather than
-// back to TMEM, because on this GPU the tensor core stalls for ~300 cycles
-// each time it switches between MMAs whose A operand comes from shared
-// memory and from TMEM, while its operand reads from shared memory do not
-// compete with the warps' own shared-memory traffic.  The activation warps
-// load a whole S (dP) tile into registers and release its TMEM columns
-// before computing, so the next tile's S (dP) is computed while they work.
+// The bf16 dS^T / dS that the activation warps produce go to a shared "X"
+// tile and dK / dQ read both operands from shared memory: on this GPU the
+// tensor core stalls for ~300 cycles each time it switches between MMAs whose
+// A operand comes from shared memory and from TMEM, while its shared-memory
+// operand reads do not compete with the warps' own shared-memory traffic.
+// The dq pass is therefore all shared-operand.  In dkdv only one X tile fits
+// at d = 128, and P^T and dS^T sharing it serialised phase B behind dV; P^T
+// goes back into TMEM over S^T instead (dV reads it from there) and the
+// switch this costs stays hidden because that pass is bound by the
+// activation warps.  The activation warps load a whole S (dP) tile into
+// registers before computing, so the next tile's S (dP) is computed while
+// they work.
 //
 // TMEM (512 columns): dkdv uses S^T [0,128), dP^T [128,256), dV [256,256+D),
 // dK [256+D, 256+2D); dq uses S [0,128), dP [128,256), dQ [256,256+D).  Two
@@ -63,14 +67,15 @@ struct TileCfg {
 // Streamed operand A: Q (dkdv) or K (dq); streamed operand B: dO (dkdv) or
 // V (dq); each has its own ring.  X: ring of [128][128] bf16 tiles written by
 // the activation warps (P^T then dS^T per query tile in dkdv, dS in dq).
-// Stage counts at d = 128 (seven 32 KB tiles fit): dkdv keeps two of each
-// stream and one X; dq reads V only in dP, early in a tile's life, and K in S
-// and again in dQ at its end, so it keeps three K stages and one V stage.
+// Stage counts at d = 128 (seven 32 KB tiles fit): stream A (Q in dkdv, K in
+// dq) is read at the start of a tile's life (S) and again at its end (dK /
+// dQ), so it keeps three stages; stream B (dO / V) is read early (dP) and,
+// in dkdv, once more by dV right after phase A, so one stage suffices; one X.
 template <int D, bool KV_MAJOR>
 struct BwdCfg : TileCfg<D> {
   using T = TileCfg<D>;
-  static constexpr int kStagesA = D == 128 ? (KV_MAJOR ? 2 : 3) : (D == 64 ? (KV_MAJOR ? 3 : 4) : 4);
-  static constexpr int kStagesB = D == 128 ? (KV_MAJOR ? 2 : 1) : (D == 64 ? (KV_MAJOR ? 3 : 2) : 4);
+  static constexpr int kStagesA = D == 128 ? 3 : 4;
+  static constexpr int kStagesB = D == 128 ? 1 : (D == 64 ? 2 : 4);
   static constexpr int kNumX = D == 128 ? 1 : 2;
   static constexpr int kXBytes = kTile * kTile * 2;
   static constexpr int kResOff = 0;
@@ -85,7 +90,7 @@ struct BwdCfg : TileCfg<D> {
 
 struct BwdBars {
   uint64_t res_full, res_empty;
-  uint64_t s_full, s_free, dp_full, dp_free, acc_full, acc_empty;
+  uint64_t s_full, s_free, p_full, dp_full, dp_free, acc_full, acc_empty;
   uint64_t drain;
   uint64_t x_full[2], x_empty[2];
   uint64_t a_full[4], a_empty[4], b_full[4], b_empty[4];
@@ -137,6 +142,22 @@ __device__ __forceinline__ void mma_tile_xs(uint32_t d_tmem, uint32_t x_tile, ui
     const uint64_t aoff = kmajor_off<kTile>(kk) >> 4;
     const uint64_t boff = static_cast<uint64_t>(kk * 16 * C::kRowBytes) >> 4;
     if (leader) mma_ss(d_tmem, a0 + aoff, b0 + boff, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// C(tmem, 128 x D) (+)= A(tmem, 128 x 128 bf16: K steps 0-3 from a_lo, 4-7
+// from a_hi) * B_tile(128 x D, MN-major)
+template <int D>
+__device__ __forceinline__ void mma_tile_ts(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_tile,
+                                            bool accumulate, bool leader) {
+  using C = TileCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(kTile, D, 0, 1);
+  const uint64_t b0 = mnmajor_desc0<D>(b_tile);
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk) {
+    const uint32_t a = kk < 4 ? a_lo + kk * 8 : a_hi + (kk - 4) * 8;
+    const uint64_t boff = static_cast<uint64_t>(kk * 16 * C::kRowBytes) >> 4;
+    if (leader) mma_ts(d_tmem, a, b0 + boff, idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -242,13 +263,15 @@ struct XRing {
   __device__ __forceinline__ uint32_t empty_parity() const { return ((n / NX) & 1) ^ 1; }
 };
 
-// dkdv.  Per query tile i the issuer waits for the activation warps'
-// hand-offs in the order they happen:
-//   [S^T(i) loaded]  S^T(i+1) = K Q(i+1)^T
-//   [P^T(i) in X]    dV += P^T(i) dO(i)
-//   [dP^T(i) loaded] dP^T(i+1) = V dO(i+1)^T
+// dkdv.  Per query tile i:
+//   [P^T(i) in TMEM] dV += P^T(i) dO(i)          (P^T over S^T's columns)
+//                    S^T(i+1) = K Q(i+1)^T        (after dV(i) has read P^T)
 //   [dS^T(i) in X]   dK += dS^T(i) Q(i)
-// so S^T(i+1) and dP^T(i+1) run while the activation warps work on tile i.
+//   [dP^T(i) loaded] dP^T(i+1) = V dO(i+1)^T
+// P^T stays in TMEM (A operand from TMEM) and only dS^T goes through the
+// shared X tile, so the two products of a tile never wait on each other for
+// X; the pass is bound by the activation warps, which hides the pipeline
+// switch between the TMEM-operand dV and the shared-operand MMAs.
 template <int D>
 __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                            Fail fail) {
@@ -256,7 +279,7 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
   const uint32_t k_t = smem_u32(smem + C::kResOff), v_t = k_t + C::kTileBytes;
   const uint32_t a_base = smem_u32(smem + C::kAOff), b_base = smem_u32(smem + C::kBOff);
   const uint32_t x_base = smem_u32(smem + C::kXOff);
-  uint32_t res_it = 0, st_it = 0, acc_it = 0, s_n = 0, dp_n = 0;
+  uint32_t res_it = 0, st_it = 0, acc_it = 0, p_n = 0, dp_n = 0;
   XRing x;
   const bool leader = elect_one();
   bool ok = true;
@@ -267,14 +290,13 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
     if (u.count == 0) continue;
     if (!(ok = mbar_wait_warp(&bars->res_full, res_it & 1, fail))) break;
     ++res_it;
-    {  // S^T and dP^T of the first query tile
+    {  // S^T and dP^T of the first query tile (S^T after the previous unit's
+       // last dV in issue order, which has read its P^T)
       const int sa = st_it % C::kStagesA, sb = st_it % C::kStagesB;
-      if (!(ok = mbar_wait_warp(&bars->s_free, (s_n & 1) ^ 1, fail))) break;
       if (!(ok = mbar_wait_warp(&bars->a_full[sa], (st_it / C::kStagesA) & 1, fail))) break;
       tc_fence_after();
       mma_tile_nt<D>(tmem, k_t, a_base + sa * C::kTileBytes, leader);  // S^T = K Q^T
       if (leader) mma_commit(&bars->s_full);
-      ++s_n;
       if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
       if (!(ok = mbar_wait_warp(&bars->b_full[sb], (st_it / C::kStagesB) & 1, fail))) break;
       tc_fence_after();
@@ -288,34 +310,21 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
       const int sa1 = (it + 1) % C::kStagesA, sb1 = (it + 1) % C::kStagesB;
       const uint32_t q_t = a_base + sa * C::kTileBytes, do_t = b_base + sb * C::kTileBytes;
       const bool more = i + 1 < u.count;
-      if (more) {  // S^T of the next query tile, once S^T(i) is in registers
-        if (!(ok = mbar_wait_warp(&bars->s_free, (s_n & 1) ^ 1, fail))) break;
-        if (!(ok = mbar_wait_warp(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
-        tc_fence_after();
-        mma_tile_nt<D>(tmem, k_t, a_base + sa1 * C::kTileBytes, leader);
-        if (leader) mma_commit(&bars->s_full);
-        ++s_n;
-      }
       if (i == 0) {
         if (!(ok = mbar_wait_warp(&bars->acc_empty, (acc_it & 1) ^ 1, fail))) break;
         ++acc_it;
       }
-      {  // dV += P^T dO
-        const int xs = x.slot<C::kNumX>();
-        if (!(ok = mbar_wait_warp(&bars->x_full[xs], x.full_parity<C::kNumX>(), fail))) break;
+      // dV += P^T dO, P^T in TMEM columns [0,32) (queries 0-63) and [64,96)
+      if (!(ok = mbar_wait_warp(&bars->p_full, p_n & 1, fail))) break;
+      ++p_n;
+      tc_fence_after();
+      mma_tile_ts<D>(tmem + 256, tmem, tmem + 64, do_t, i > 0, leader);
+      if (leader) mma_commit(&bars->b_empty[sb]);  // dO(i): dP^T(i) and dV(i) issued
+      if (more) {  // S^T of the next query tile over the columns dV(i) reads
+        if (!(ok = mbar_wait_warp(&bars->a_full[sa1], ((it + 1) / C::kStagesA) & 1, fail))) break;
         tc_fence_after();
-        mma_tile_xs<D>(tmem + 256, x_base + xs * C::kXBytes, do_t, i > 0, leader);
-        if (leader) mma_commit(&bars->x_empty[xs]);
-        if (leader) mma_commit(&bars->b_empty[sb]);  // dO(i): dP^T(i) and dV(i) issued
-        ++x.n;
-      }
-      if (more) {  // dP^T of the next query tile, once dP^T(i) is in registers
-        if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
-        if (!(ok = mbar_wait_warp(&bars->b_full[sb1], ((it + 1) / C::kStagesB) & 1, fail))) break;
-        tc_fence_after();
-        mma_tile_nt<D>(tmem + 128, v_t, b_base + sb1 * C::kTileBytes, leader);
-        if (leader) mma_commit(&bars->dp_full);
-        ++dp_n;
+        mma_tile_nt<D>(tmem, k_t, a_base + sa1 * C::kTileBytes, leader);
+        if (leader) mma_commit(&bars->s_full);
       }
       {  // dK += dS^T Q
         const int xs = x.slot<C::kNumX>();
@@ -325,6 +334,14 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
         if (leader) mma_commit(&bars->x_empty[xs]);
         if (leader) mma_commit(&bars->a_empty[sa]);  // Q(i): S^T(i) and dK(i) issued
         ++x.n;
+      }
+      if (more) {  // dP^T of the next query tile, once dP^T(i) is in registers
+        if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
+        if (!(ok = mbar_wait_warp(&bars->b_full[sb1], ((it + 1) / C::kStagesB) & 1, fail))) break;
+        tc_fence_after();
+        mma_tile_nt<D>(tmem + 128, v_t, b_base + sb1 * C::kTileBytes, leader);
+        if (leader) mma_commit(&bars->dp_full);
+        ++dp_n;
       }
     }
     if (!ok) break;
@@ -631,8 +648,10 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       tmem_ld32(t_s, sv0);
       tmem_ld32(t_s + 32, sv1);
       tmem_ld_wait2(sv0, sv1);
-      tc_fence_before();
-      mbar_arrive_warp(&bars->s_free);
+      if constexpr (!KV_MAJOR) {  // dkdv reuses these columns for P^T instead
+        tc_fence_before();
+        mbar_arrive_warp(&bars->s_free);
+      }
 
       // ---- phase A: S -> (P, act'(x)) [softmax: P]; P^T to X (dkdv)
       float keep0[32], keep1[32];  // act'(x) (GELU/SiLU) or P (softmax) per owned column
@@ -665,36 +684,35 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
           }
         }
 #undef JG_PHASE_A
-        if constexpr (KV_MAJOR) {
-          if (chunk == 0 && !(ok = mbar_wait(&bars->x_empty[x.slot<C::kNumX>()], x.empty_parity<C::kNumX>(), fail)))
-            break;
-          store_x_chunk(x_base + x.slot<C::kNumX>() * C::kXBytes, half, chunk, r, pk);
-        }
+        if constexpr (KV_MAJOR) tmem_st16(t_s + 16 * chunk, pk);  // P^T over S^T columns already read
       }
-      if (!ok) break;
       if constexpr (KV_MAJOR) {
-        fence_proxy_async_smem();
-        mbar_arrive_warp(&bars->x_full[x.slot<C::kNumX>()]);
-        ++x.n;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(&bars->p_full);
       }
 
       // ---- phase B: dP -> dS (bf16 into X), dbias partial sums
       if (!(ok = mbar_wait(&bars->dp_full, dp_it & 1, fail))) break;
       ++dp_it;
       tc_fence_after();
-      uint32_t dv0[32], dv1[32];
-      tmem_ld32(t_dp, dv0);
-      tmem_ld32(t_dp + 32, dv1);
-      tmem_ld_wait2(dv0, dv1);
-      tc_fence_before();
-      mbar_arrive_warp(&bars->dp_free);
       float2 row_sum = f2(0.f);
       float dacc[3] = {0.f, 0.f, 0.f};
       const int dmode = !want_dbias ? 0 : (g.band ? 2 : 1);
+      // dP columns are loaded one 32-column chunk at a time (both halves of
+      // dP and of act' live at once would exceed the register budget); the
+      // TMEM columns go back after the second load -- the next dP is not
+      // needed before the next tile's phase B.
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int cbase = 64 * half + 32 * chunk;
-        const uint32_t(&dv)[32] = chunk == 0 ? dv0 : dv1;
+        uint32_t dv[32];
+        tmem_ld32(t_dp + 32 * chunk, dv);
+        tmem_ld_wait(dv);
+        if (chunk == 1) {
+          tc_fence_before();
+          mbar_arrive_warp(&bars->dp_free);
+        }
         float del_c[32];
         if constexpr (kSoftmax && KV_MAJOR) {
           const int64_t q0 = static_cast<int64_t>(u.h) * p.total_q + u.seg.q0 + pt * kTile + cbase;
@@ -819,6 +837,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
     mbar_init(&bars->res_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 8);
+    mbar_init(&bars->p_full, 8);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->dp_free, 8);
     mbar_init(&bars->acc_full, 1);
