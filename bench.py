@@ -81,6 +81,17 @@ WORKLOAD_TEXT = {
 }
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum per launch on the full
+# long-tail workload: an ncu capture of the first 24 segments of the same
+# workload, scaled by the tile pairs processed (x2.0163); to be replaced
+# whenever the kernels change.
+TRAFFIC = {
+    "gdpa_fwd_kernel": round((566.334976e6 + 119.337728e6) * 2.016340),
+    "gdpa_bwd_kernel (dK/dV pass)": round((739.939840e6 + 217.105408e6) * 2.016340),
+    "gdpa_bwd_kernel (dQ pass)": round((688.729856e6 + 107.835392e6) * 2.016340),
+}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -267,9 +278,10 @@ def run_native(args, world, rank, local):
         jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
                      causal=x.causal, out=out, lse=lse, workspace=ws_f)
 
-    def bwd():
+    def bwd(pass_events=None):
         jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
-                     bias_table=d.bias, causal=x.causal, dq=dq, dk=dk, dv=dv, dbias=dbias, workspace=ws_b)
+                     bias_table=d.bias, causal=x.causal, dq=dq, dk=dk, dv=dv, dbias=dbias, workspace=ws_b,
+                     pass_events=pass_events)
 
     # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, dQ, [dbias reduce])
     launches_per_step = 2 + 3 + int(softmax) + int(bias_len > 0)
@@ -281,6 +293,13 @@ def run_native(args, world, rank, local):
         raise RuntimeError("device status error during warm-up")
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # per-pass events inside the backward call (dK/dV kernel, dQ kernel); one
+    # record each first so that the CUDA events exist before the timed loop
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for e in ev + pev:
+        for ee in e:
+            ee.record(stream)
+    torch.cuda.synchronize()
     with Clocks(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
@@ -291,7 +310,7 @@ def run_native(args, world, rank, local):
             ev[s][0].record(stream)
             fwd()
             ev[s][1].record(stream)
-            bwd()
+            bwd(pev[s])
             ev[s][2].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -300,6 +319,8 @@ def run_native(args, world, rank, local):
     ms_total = t_start.elapsed_time(t_end)
     ms_fwd = [e[0].elapsed_time(e[1]) for e in ev]
     ms_bwd = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_kv = [e[0].elapsed_time(e[1]) for e in pev]
+    ms_q = [e[1].elapsed_time(e[2]) for e in pev]
     ms_step, value = aggregate(world, f_fwd + f_bwd, ms_total / args.steps)
 
     # end to end through the public API: pinned host inputs -> device, step,
@@ -341,10 +362,26 @@ def run_native(args, world, rank, local):
         barrier(world)
 
     bf16_burst, bf16_sust, hbm, peak_kind = peaks()
-    # dominant kernel: the backward passes share one call; the forward kernel
-    # is timed alone (its call adds only the small scheduling kernel)
     fwd_ms = statistics.mean(ms_fwd)
     bwd_ms = statistics.mean(ms_bwd)
+    # Per-kernel rooflines.  Algorithmic FLOPs per launch: forward 2 matmuls
+    # (S, PV) = f_fwd; dK/dV pass S^T, dP^T, dV, dK = 2 f_fwd; dQ pass dQ =
+    # f_fwd / 4 (its recomputed S and dP are overhead of the split-dQ scheme,
+    # not algorithmic work).  The forward's time includes the ~10 us
+    # scheduling kernel of its call; the passes are timed by events recorded
+    # between their launches inside the backward call.
+    kernels = {
+        "gdpa_fwd_kernel": (fwd_ms, f_fwd),
+        "gdpa_bwd_kernel (dK/dV pass)": (statistics.mean(ms_kv), 2.0 * f_fwd),
+        "gdpa_bwd_kernel (dQ pass)": (statistics.mean(ms_q), 0.25 * f_fwd),
+    }
+    per_kernel = {k: {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+                      "frac": round(fl / (ms * 1e-3) / 1e12 / bf16_sust, 4)} for k, (ms, fl) in kernels.items()}
+    dom = max(kernels, key=lambda k: kernels[k][0])
+    dom_ms, dom_fl = kernels[dom]
+    # dram bytes per launch of the dominant kernel from the ncu capture
+    # above, valid for the full long-tail workload only
+    traffic = TRAFFIC.get(dom) if (args.workload == 5 and not args.segments) else None
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -380,16 +417,16 @@ def run_native(args, world, rank, local):
         "fwd_tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
         "bwd_tflops": round(f_bwd / (bwd_ms * 1e-3) / 1e12, 2),
         "roofline": {
-            "kernel": "gdpa_fwd_kernel (timed with CUDA events around jgdpa_fwd; includes the ~10 us "
-                      "scheduling kernel)",
+            "kernel": dom,
             "bound": "tensor",
-            "achieved": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
+            "achieved": round(dom_fl / (dom_ms * 1e-3) / 1e12, 2),
             "peak": bf16_sust,
             "unit": "TFLOP/s",
-            "frac": round(f_fwd / (fwd_ms * 1e-3) / 1e12 / bf16_sust, 4),
+            "frac": round(dom_fl / (dom_ms * 1e-3) / 1e12 / bf16_sust, 4),
             "peak_kind": f"{peak_kind} bf16 sustained",
-            "traffic": None,
+            "traffic": traffic,
         },
+        "kernels": per_kernel,
         "e2e": {
             "value": round(world * (f_fwd + f_bwd) / (ms_e2e * 1e-3) / 1e12, 2),
             "unit": "TFLOPS",

@@ -147,6 +147,24 @@ JGDPA_API jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v,
                        void* workspace, size_t workspace_bytes, jgdpa_stream_t stream);
 
 /*
+ * jgdpa_bwd plus timing: pass_events points to three CUDA events (cudaEvent_t,
+ * created by the caller on the current device; any entry, or pass_events
+ * itself, may be NULL).  They are recorded on `stream` right before the dK/dV
+ * pass kernel, between the dK/dV and dQ pass kernels, and right after the
+ * dQ pass kernel, so cudaEventElapsedTime gives each pass's duration.
+ * Everything else, including errors, is as for jgdpa_bwd.
+ */
+JGDPA_API jgdpa_status jgdpa_bwd_timed(const void* q, const void* k, const void* v,
+                       const void* out, const float* lse, const void* dout,
+                       const int32_t* q_offsets, const int32_t* kv_offsets,
+                       int32_t batch, int64_t total_q, int64_t total_kv,
+                       int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
+                       const float* bias_table, int32_t bias_len, int32_t causal,
+                       void* dq, void* dk, void* dv, float* dbias,
+                       void* workspace, size_t workspace_bytes, jgdpa_stream_t stream,
+                       void* const* pass_events);
+
+/*
  * Forward pass without a caller-provided workspace: the same computation and
  * arguments as jgdpa_fwd minus (workspace, workspace_bytes).  There is no
  * counterpart on the pages; this entry point exists for callers that cannot

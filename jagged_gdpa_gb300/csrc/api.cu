@@ -292,12 +292,23 @@ jgdpa_status jgdpa_fwd(const void* q, const void* k, const void* v, const int32_
   return JGDPA_OK;
 }
 
-jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                       const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
-                       int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
-                       float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq, void* dk,
-                       void* dv, float* dbias, void* workspace, size_t workspace_bytes, jgdpa_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+// The backward; `ev` (3 caller events, entries may be null) is recorded on
+// the stream before the dK/dV pass, between the passes and after the dQ pass.
+jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
+                      int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
+                      float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq, void* dk,
+                      void* dv, float* dbias, void* workspace, size_t workspace_bytes, jgdpa_stream_t stream_,
+                      void* const* ev) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  auto record = [&](int i) -> cudaError_t {
+    return (ev != nullptr && ev[i] != nullptr) ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), stream)
+                                               : cudaSuccess;
+  };
   jgdpa_status st = check_common(batch, total_q, total_kv, heads, head_dim, act, scale, bias_table, bias_len,
                                  causal, q_offsets, kv_offsets);
   if (st != JGDPA_OK) return st;
@@ -359,13 +370,41 @@ jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v, const void* 
   p.dbias_part = part;
   p.units = reinterpret_cast<const jg::Unit*>(ws + L.units0);
   p.n_units = hdr + 1;
+  JG_CUDA(record(0));
   JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, true, grid_kv, stream));
+  JG_CUDA(record(1));
   p.dbias_part = nullptr;
   p.units = reinterpret_cast<const jg::Unit*>(ws + L.units1);
   p.n_units = hdr + 2;
   JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
+  JG_CUDA(record(2));
   if (part) JG_CUDA(jg::launch_dbias_reduce(part, dbias, grid_kv, heads * bias_len, stream));
   return JGDPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                       const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
+                       int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
+                       float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq, void* dk,
+                       void* dv, float* dbias, void* workspace, size_t workspace_bytes, jgdpa_stream_t stream) {
+  return bwd_impl(q, k, v, out, lse, dout, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act,
+                  scale, bias_table, bias_len, causal, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
+                  nullptr);
+}
+
+jgdpa_status jgdpa_bwd_timed(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                             const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
+                             int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
+                             float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq,
+                             void* dk, void* dv, float* dbias, void* workspace, size_t workspace_bytes,
+                             jgdpa_stream_t stream, void* const* pass_events) {
+  return bwd_impl(q, k, v, out, lse, dout, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act,
+                  scale, bias_table, bias_len, causal, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
+                  pass_events);
 }
 
 jgdpa_status jgdpa_read_device_status(const void* workspace, jgdpa_stream_t stream_) {
