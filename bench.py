@@ -82,14 +82,9 @@ WORKLOAD_TEXT = {
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch on the full
-# long-tail workload: an ncu capture of the first 24 segments of the same
-# workload, scaled by the tile pairs processed (x2.0163); to be replaced
-# whenever the kernels change.
-TRAFFIC = {
-    "gdpa_fwd_kernel": round((566.334976e6 + 119.337728e6) * 2.016340),
-    "gdpa_bwd_kernel (dK/dV pass)": round((739.939840e6 + 217.105408e6) * 2.016340),
-    "gdpa_bwd_kernel (dQ pass)": round((688.729856e6 + 107.835392e6) * 2.016340),
-}
+# long-tail workload, from an ncu capture of the current kernels; empty when
+# the kernels have changed since the last capture.
+TRAFFIC = {}
 
 
 def peaks():
@@ -273,6 +268,9 @@ def run_native(args, world, rank, local):
                        dtype=torch.uint8, device=dev)
     ws_b = torch.empty(jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, True),
                        dtype=torch.uint8, device=dev)
+    # stored-dS backward: scratch sized from the (host) segment lengths
+    ds_scratch = torch.empty(max(1, jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, heads)),
+                             dtype=torch.uint8, device=dev)
 
     def fwd():
         jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
@@ -281,7 +279,7 @@ def run_native(args, world, rank, local):
     def bwd(pass_events=None):
         jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
                      bias_table=d.bias, causal=x.causal, dq=dq, dk=dk, dv=dv, dbias=dbias, workspace=ws_b,
-                     pass_events=pass_events)
+                     ds_scratch=ds_scratch, pass_events=pass_events)
 
     # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, dQ, [dbias reduce])
     launches_per_step = 2 + 3 + int(softmax) + int(bias_len > 0)
@@ -341,7 +339,7 @@ def run_native(args, world, rank, local):
                              workspace=ws_f)
         jg.jgdpa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, l2, dev_in["dout"], dev_in["q_offsets"],
                      dev_in["kv_offsets"], x.act, x.scale, bias_table=dev_in.get("bias"), causal=x.causal, dq=dq,
-                     dk=dk, dv=dv, dbias=dbias, workspace=ws_b)
+                     dk=dk, dv=dv, dbias=dbias, workspace=ws_b, ds_scratch=ds_scratch)
         for k, t in results:
             host_out[k].copy_(t, non_blocking=True)
 
@@ -365,9 +363,8 @@ def run_native(args, world, rank, local):
     fwd_ms = statistics.mean(ms_fwd)
     bwd_ms = statistics.mean(ms_bwd)
     # Per-kernel rooflines.  Algorithmic FLOPs per launch: forward 2 matmuls
-    # (S, PV) = f_fwd; dK/dV pass S^T, dP^T, dV, dK = 2 f_fwd; dQ pass dQ =
-    # f_fwd / 4 (its recomputed S and dP are overhead of the split-dQ scheme,
-    # not algorithmic work).  The forward's time includes the ~10 us
+    # (S, PV) = f_fwd; dK/dV pass S^T, dP^T, dV, dK = 2 f_fwd; dQ pass (dQ
+    # from the dS tiles the dK/dV pass stored) = f_fwd / 4.  The forward's time includes the ~10 us
     # scheduling kernel of its call; the passes are timed by events recorded
     # between their launches inside the backward call.
     kernels = {

@@ -82,7 +82,7 @@ typedef enum {
     JGDPA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, bad enum, even bias_len */
     JGDPA_ERR_UNSUPPORTED = 2,        /* head_dim not in {32, 64, 128}, sizes beyond int32 rows */
     JGDPA_ERR_MISALIGNED = 3,         /* a tensor or the workspace is not suitably aligned */
-    JGDPA_ERR_WORKSPACE_TOO_SMALL = 4,
+    JGDPA_ERR_WORKSPACE_TOO_SMALL = 4,  /* also device-detected: stored-dS scratch too small */
     JGDPA_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
     JGDPA_ERR_BAD_OFFSETS = 6,        /* device-detected: offsets not monotone / wrong ends */
     JGDPA_ERR_DEVICE_TIMEOUT = 7      /* device-detected: an internal wait gave up */
@@ -147,21 +147,44 @@ JGDPA_API jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v,
                        void* workspace, size_t workspace_bytes, jgdpa_stream_t stream);
 
 /*
- * jgdpa_bwd plus timing: pass_events points to three CUDA events (cudaEvent_t,
- * created by the caller on the current device; any entry, or pass_events
- * itself, may be NULL).  They are recorded on `stream` right before the dK/dV
- * pass kernel, between the dK/dV and dQ pass kernels, and right after the
- * dQ pass kernel, so cudaEventElapsedTime gives each pass's duration.
- * Everything else, including errors, is as for jgdpa_bwd.
+ * Bytes of stored-dS scratch that jgdpa_bwd_ex needs for these segment
+ * lengths: heads * sum_b ceil(Lq_b/128) * ceil(Lkv_b/128) tiles of 32 KB.
+ * q_offsets_host / kv_offsets_host are HOST copies of the offsets
+ * ([batch + 1] each).  Returns 0 for invalid arguments (and for batch 0).
  */
-JGDPA_API jgdpa_status jgdpa_bwd_timed(const void* q, const void* k, const void* v,
+JGDPA_API size_t jgdpa_ds_scratch_bytes(const int32_t* q_offsets_host, const int32_t* kv_offsets_host,
+                                        int32_t batch, int32_t heads);
+
+/*
+ * Backward pass, extended.  The same computation, arguments and errors as
+ * jgdpa_bwd, plus:
+ *   ds_scratch, ds_scratch_bytes
+ *       optional caller-owned device scratch (256-byte aligned) for the
+ *       stored-dS backward; NULL selects the recompute backward of
+ *       jgdpa_bwd.  With scratch the dK/dV pass writes every bf16 dS tile it
+ *       forms to the scratch and the dQ pass is one streaming matmul
+ *       dQ = s * dS K over the stored tiles, instead of recomputing S, dP and
+ *       the activation derivative.  It needs jgdpa_ds_scratch_bytes(...)
+ *       bytes; if the device finds the scratch too small for the actual
+ *       lengths it records JGDPA_ERR_WORKSPACE_TOO_SMALL in the status word
+ *       and computes nothing (read it with jgdpa_read_device_status).  The
+ *       scratch contents need no initialisation and are clobbered.
+ *   pass_events
+ *       optional three CUDA events (cudaEvent_t, created by the caller on the
+ *       current device; any entry, or pass_events itself, may be NULL),
+ *       recorded on `stream` right before the dK/dV pass kernel, between the
+ *       dK/dV and dQ pass kernels, and right after the dQ pass kernel, so
+ *       that cudaEventElapsedTime gives each pass's duration.
+ */
+JGDPA_API jgdpa_status jgdpa_bwd_ex(const void* q, const void* k, const void* v,
                        const void* out, const float* lse, const void* dout,
                        const int32_t* q_offsets, const int32_t* kv_offsets,
                        int32_t batch, int64_t total_q, int64_t total_kv,
                        int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
                        const float* bias_table, int32_t bias_len, int32_t causal,
                        void* dq, void* dk, void* dv, float* dbias,
-                       void* workspace, size_t workspace_bytes, jgdpa_stream_t stream,
+                       void* workspace, size_t workspace_bytes,
+                       void* ds_scratch, size_t ds_scratch_bytes, jgdpa_stream_t stream,
                        void* const* pass_events);
 
 /*

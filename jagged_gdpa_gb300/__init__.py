@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     EXPORTS,
     JgdpaError,
     jgdpa_bwd,
+    jgdpa_ds_scratch_bytes,
     jgdpa_eval_activation,
     jgdpa_fwd,
     jgdpa_read_device_status,

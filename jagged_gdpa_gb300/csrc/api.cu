@@ -21,6 +21,7 @@ cudaError_t launch_softmax_delta(const void* out, const void* dout, float* delta
                                  int head_dim, const int* status, cudaStream_t stream);
 cudaError_t launch_dbias_reduce(const float* part, float* dbias, int n_parts, int n, cudaStream_t stream);
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t stream);
+cudaError_t launch_dq_ds(const BwdParams& p, int head_dim, int grid, cudaStream_t stream);
 }  // namespace jg
 
 namespace {
@@ -80,6 +81,22 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int heads, int d) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D view of the stored-dS scratch: rows of 128 bf16 (one tile row), boxes
+// of 64 columns x 128 rows with the 128-byte swizzle (one column block of a
+// tile, the shared-memory layout of the kernels' X tiles).
+bool make_ds_map(CUtensorMap* m, void* ptr, int64_t tiles) {
+  std::memset(m, 0, sizeof(*m));
+  EncodeFn enc = encode_fn();
+  if (!enc || tiles <= 0) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kTile), static_cast<cuuint64_t>(tiles) * kTile};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kTile) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTile / 2), static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------- workspace
 struct Layout {
   size_t header = 0;      // status word + unit counters
@@ -88,6 +105,7 @@ struct Layout {
   size_t units1 = 0;      // dq units (bwd)
   size_t delta = 0;       // softmax bwd: [H][total_q]
   size_t dbias = 0;       // bwd with dbias: [grid][H][T]
+  size_t ds_base = 0;     // bwd: first stored-dS tile per segment, int64 [batch + 1]
   size_t total = 0;
   int max0 = 0, max1 = 0;
   int grid = 0;
@@ -125,6 +143,8 @@ bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
   if (bwd && act == JGDPA_ACT_SOFTMAX) off += up(static_cast<size_t>(heads) * total_q * sizeof(float));
   L->dbias = off;
   if (bwd && bias_len > 0) off += up(static_cast<size_t>(sms) * heads * bias_len * sizeof(float));
+  L->ds_base = off;
+  if (bwd) off += up((static_cast<size_t>(batch) + 1) * sizeof(int64_t));
   L->total = off;
   return true;
 }
@@ -199,8 +219,12 @@ __global__ void eval_act_kernel(int act, int path, const float* x, int64_t n, fl
 
 jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batch, int32_t heads,
                           int64_t total_q, int64_t total_kv, int32_t causal, uint8_t* ws, const Layout& L,
-                          bool bwd, cudaStream_t stream) {
+                          bool bwd, cudaStream_t stream, int64_t ds_capacity = -1) {
   jg::SchedParams sp{};
+  if (ds_capacity >= 0) {
+    sp.ds_base = reinterpret_cast<int64_t*>(ws + L.ds_base);
+    sp.ds_capacity = ds_capacity;
+  }
   sp.q_off = q_off;
   sp.kv_off = kv_off;
   sp.batch = batch;
@@ -303,7 +327,7 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
                       int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
                       float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq, void* dk,
                       void* dv, float* dbias, void* workspace, size_t workspace_bytes, jgdpa_stream_t stream_,
-                      void* const* ev) {
+                      void* ds_scratch, size_t ds_scratch_bytes, void* const* ev) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   auto record = [&](int i) -> cudaError_t {
     return (ev != nullptr && ev[i] != nullptr) ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), stream)
@@ -325,6 +349,10 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, true, &L)) return JGDPA_ERR_CUDA;
   if (workspace == nullptr || workspace_bytes < L.total) return JGDPA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, kAlign)) return JGDPA_ERR_MISALIGNED;
+  // stored dS: capacity in tiles (the device checks the lengths against it)
+  const int64_t ds_tiles = ds_scratch ? static_cast<int64_t>(ds_scratch_bytes / jg::kDsTileBytes) : -1;
+  if (ds_scratch && !aligned(ds_scratch, kAlign)) return JGDPA_ERR_MISALIGNED;
+  if (ds_scratch && ds_tiles > INT32_MAX / jg::kTile) return JGDPA_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   JG_CUDA(cudaMemsetAsync(ws + L.header, 0, 64 * sizeof(int), stream));
   if (dbias) JG_CUDA(cudaMemsetAsync(dbias, 0, static_cast<size_t>(heads) * bias_len * sizeof(float), stream));
@@ -338,13 +366,19 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     }
     return JGDPA_OK;
   }
-  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, ws, L, true, stream);
+  const bool stored_ds = ds_scratch != nullptr && ds_tiles > 0;
+  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, ws, L, true, stream,
+                 ds_scratch ? std::max<int64_t>(ds_tiles, 0) : -1);
   if (st != JGDPA_OK) return st;
 
   jg::BwdParams p{};
   if (!make_map(&p.tm_q, q, total_q, heads, head_dim) || !make_map(&p.tm_k, k, total_kv, heads, head_dim) ||
       !make_map(&p.tm_v, v, total_kv, heads, head_dim) || !make_map(&p.tm_do, dout, total_q, heads, head_dim))
     return JGDPA_ERR_CUDA;
+  if (stored_ds) {
+    if (!make_ds_map(&p.tm_ds, ds_scratch, ds_tiles)) return JGDPA_ERR_CUDA;
+    p.ds_base = reinterpret_cast<const int64_t*>(ws + L.ds_base);
+  }
   int* hdr = reinterpret_cast<int*>(ws + L.header);
   p.q_off = q_offsets;
   p.kv_off = kv_offsets;
@@ -376,7 +410,8 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   p.dbias_part = nullptr;
   p.units = reinterpret_cast<const jg::Unit*>(ws + L.units1);
   p.n_units = hdr + 2;
-  JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
+  if (stored_ds) JG_CUDA(jg::launch_dq_ds(p, head_dim, grid_q, stream));
+  else JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
   JG_CUDA(record(2));
   if (part) JG_CUDA(jg::launch_dbias_reduce(part, dbias, grid_kv, heads * bias_len, stream));
   return JGDPA_OK;
@@ -393,18 +428,32 @@ jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v, const void* 
                        void* dv, float* dbias, void* workspace, size_t workspace_bytes, jgdpa_stream_t stream) {
   return bwd_impl(q, k, v, out, lse, dout, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act,
                   scale, bias_table, bias_len, causal, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
-                  nullptr);
+                  nullptr, 0, nullptr);
 }
 
-jgdpa_status jgdpa_bwd_timed(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                             const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
-                             int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
-                             float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq,
-                             void* dk, void* dv, float* dbias, void* workspace, size_t workspace_bytes,
-                             jgdpa_stream_t stream, void* const* pass_events) {
+jgdpa_status jgdpa_bwd_ex(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                          const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
+                          int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
+                          float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq,
+                          void* dk, void* dv, float* dbias, void* workspace, size_t workspace_bytes,
+                          void* ds_scratch, size_t ds_scratch_bytes, jgdpa_stream_t stream,
+                          void* const* pass_events) {
   return bwd_impl(q, k, v, out, lse, dout, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act,
                   scale, bias_table, bias_len, causal, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
-                  pass_events);
+                  ds_scratch, ds_scratch_bytes, pass_events);
+}
+
+size_t jgdpa_ds_scratch_bytes(const int32_t* q_offsets_host, const int32_t* kv_offsets_host, int32_t batch,
+                              int32_t heads) {
+  if (batch < 0 || heads < 1 || (batch > 0 && (q_offsets_host == nullptr || kv_offsets_host == nullptr))) return 0;
+  uint64_t tiles = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t lq = static_cast<int64_t>(q_offsets_host[b + 1]) - q_offsets_host[b];
+    const int64_t lkv = static_cast<int64_t>(kv_offsets_host[b + 1]) - kv_offsets_host[b];
+    if (lq < 0 || lkv < 0) return 0;
+    tiles += static_cast<uint64_t>((lq + jg::kTile - 1) / jg::kTile) * ((lkv + jg::kTile - 1) / jg::kTile);
+  }
+  return static_cast<size_t>(tiles * heads * jg::kDsTileBytes);
 }
 
 jgdpa_status jgdpa_read_device_status(const void* workspace, jgdpa_stream_t stream_) {

@@ -437,6 +437,42 @@ __device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint
   mbar_wait_drain(&bars->drain, 0);
 }
 
+// ----------------------------------------------------------- dS store role
+// dK/dV pass with stored dS: every dS^T tile the activation warps put in X is
+// also copied to the scratch array by TMA (one elected lane of warp 3); the X
+// slot is released once both the dK MMA and this copy have read it.
+template <int D>
+__device__ void bwd_ds_store(const BwdParams& p, uint8_t* smem, BwdBars* bars, int n_units, Fail fail) {
+  using C = BwdCfg<D, true>;
+  uint8_t* x_base = smem + C::kXOff;
+  XRing x;
+  const bool leader = elect_one();
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = unit_index(r, blockIdx.x, gridDim.x);
+    if (idx >= n_units) break;
+    const BwdUnit u = bwd_unit<true>(p, idx);
+    if (u.count == 0) continue;
+    for (int i = 0; i < u.count; ++i) {
+      const int xs = x.slot<C::kNumX>();
+      if (!(ok = mbar_wait_warp(&bars->x_full[xs], x.full_parity<C::kNumX>(), fail))) break;
+      if (leader) {
+        const int row = ds_row(p.ds_base, u.seg, u.b, u.h, u.tile, u.first + i);
+        const uint8_t* src = x_base + xs * C::kXBytes;
+        tma_store_2d(&p.tm_ds, src, 0, row);
+        tma_store_2d(&p.tm_ds, src + C::kXBytes / 2, kTile / 2, row);
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(&bars->x_empty[xs]);
+      }
+      __syncwarp();
+      ++x.n;
+    }
+  }
+  if (leader) bulk_wait_all();
+  __syncwarp();
+}
+
 // --------------------------------------------------------- activation warps
 // Geometry of one (own tile, partner tile) pair for the thread of row r.
 // KV-major: own row = key j, column c = query i; Q-major: own row = query i,
@@ -845,7 +881,8 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
     mbar_init(&bars->drain, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->x_full[s], 8);
-      mbar_init(&bars->x_empty[s], 1);
+      // released by the consuming MMA's commit, plus the dS copy when stored
+      mbar_init(&bars->x_empty[s], (KV_MAJOR && p.ds_base != nullptr) ? 2 : 1);
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->a_full[s], 1);
@@ -871,6 +908,10 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
     bwd_producer<D, KV_MAJOR, 0>(p, smem, bars, n_units, fail);
   } else if (warp == 2) {
     bwd_producer<D, KV_MAJOR, 1>(p, smem, bars, n_units, fail);
+  } else if (warp == 3) {
+    if constexpr (KV_MAJOR) {
+      if (p.ds_base != nullptr) bwd_ds_store<D>(p, smem, bars, n_units, fail);
+    }
   } else if (warp == 1) {
     if constexpr (KV_MAJOR) bwd_mma_kv<D>(p, smem, bars, tmem, n_units, fail);
     else bwd_mma_q<D>(p, smem, bars, tmem, n_units, fail);
@@ -881,6 +922,179 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------ dQ from the stored dS
+// dQ pass when the dK/dV pass has stored dS: per unit (segment, head, query
+// tile) dQ = s sum_kt dS(qt, kt) K(kt), a plain streaming GEMM.  The stored
+// tile is dS^T ([keys][queries]); read as the A operand in MN-major form it
+// is dS.  No activation work and no recomputation of S and dP: the pass is
+// bound by streaming the dS tiles from memory.
+//   warp 0      TMA producer (dS tile + K tile per stage)
+//   warp 1      MMA issuer; accumulators double-buffered in TMEM
+//   warps 4-7   epilogue (TMEM -> dQ rows)
+template <int D>
+struct DqCfg : TileCfg<D> {
+  using T = TileCfg<D>;
+  static constexpr int kStageBytes = kDsTileBytes + T::kTileBytes;
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+struct DqBars {
+  uint64_t full[4], empty[4];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) gdpa_dq_ds_kernel(const __grid_constant__ BwdParams p) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DqBars* bars = reinterpret_cast<DqBars*>(smem + C::kBarOff);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->acc_full[s], 1);
+      mbar_init(&bars->acc_empty[s], 4);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int n_units = *p.n_units;
+  if (*reinterpret_cast<volatile int*>(p.status) != kOk) n_units = 0;
+  Fail fail{&bars->abort, p.status};
+
+  if (warp == 0) {  // ---- producer
+    const bool leader = elect_one();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int idx = unit_index(r, blockIdx.x, gridDim.x);
+      if (idx >= n_units) break;
+      const BwdUnit u = bwd_unit<false>(p, idx);
+      if (u.rows <= 0) continue;
+      for (int kt = 0; kt < u.count; ++kt, ++it) {
+        const int st = it % C::kStages;
+        if (!(ok = mbar_wait_warp(&bars->empty[st], ((it / C::kStages) & 1) ^ 1, fail))) break;
+        if (leader) {
+          uint8_t* dst = smem + st * C::kStageBytes;
+          mbar_arrive_tx(&bars->full[st], C::kStageBytes);
+          const int row = ds_row(p.ds_base, u.seg, u.b, u.h, kt, u.tile);
+          tma_load_2d(dst, &p.tm_ds, &bars->full[st], 0, row);
+          tma_load_2d(dst + kDsTileBytes / 2, &p.tm_ds, &bars->full[st], kTile / 2, row);
+#pragma unroll
+          for (int cb = 0; cb < C::kNumBlocks; ++cb)
+            tma_load_3d(dst + kDsTileBytes + cb * C::kBlockBytes, &p.tm_k, &bars->full[st], cb * C::kBlockCols,
+                        u.h, u.seg.k0 + kt * kTile);
+        }
+      }
+    }
+    if (!ok) {
+      for (uint32_t i = it > C::kStages ? it - C::kStages : 0; i < it; ++i)
+        mbar_wait_drain(&bars->full[i % C::kStages], (i / C::kStages) & 1);
+    }
+  } else if (warp == 1) {  // ---- MMA issuer
+    const bool leader = elect_one();
+    constexpr uint32_t idesc = idesc_bf16(kTile, D, 1, 1);  // A (dS) and B (K) MN-major
+    uint32_t it = 0, acc_n = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int idx = unit_index(r, blockIdx.x, gridDim.x);
+      if (idx >= n_units) break;
+      const BwdUnit u = bwd_unit<false>(p, idx);
+      if (u.rows <= 0 || u.count == 0) continue;
+      const int buf = acc_n & 1;
+      if (!(ok = mbar_wait_warp(&bars->acc_empty[buf], ((acc_n >> 1) & 1) ^ 1, fail))) break;
+      const uint32_t d_acc = tmem + buf * D;
+      for (int kt = 0; kt < u.count; ++kt, ++it) {
+        const int st = it % C::kStages;
+        if (!(ok = mbar_wait_warp(&bars->full[st], (it / C::kStages) & 1, fail))) break;
+        tc_fence_after();
+        const uint32_t a_t = smem_u32(smem + st * C::kStageBytes);
+        const uint64_t a0 = mnmajor_desc0<kTile>(a_t), b0 = mnmajor_desc0<D>(a_t + kDsTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t aoff = static_cast<uint64_t>(kk * 16 * TileCfg<kTile>::kRowBytes) >> 4;
+          const uint64_t boff = static_cast<uint64_t>(kk * 16 * C::kRowBytes) >> 4;
+          if (leader) mma_ss(d_acc, a0 + aoff, b0 + boff, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (leader) mma_commit(&bars->empty[st]);
+      }
+      if (!ok) break;
+      if (leader) mma_commit(&bars->acc_full[buf]);
+      ++acc_n;
+    }
+    if (leader) mma_commit(&bars->drain);
+    mbar_wait_drain(&bars->drain, 0);
+  } else if (warp >= 4) {  // ---- epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + (threadIdx.x & 31);
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int H = p.heads;
+    uint32_t acc_n = 0;
+    for (int rr = 0;; ++rr) {
+      const int idx = unit_index(rr, blockIdx.x, gridDim.x);
+      if (idx >= n_units) break;
+      const BwdUnit u = bwd_unit<false>(p, idx);
+      if (u.rows <= 0) continue;
+      const bool row_ok = r < u.rows;
+      const int64_t grow = static_cast<int64_t>(u.seg.q0) + u.tile * kTile + r;
+      __nv_bfloat16* dst = p.dq + (grow * H + u.h) * D;
+      if (u.count == 0) {  // no keys: zero rows
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < D; c += 8) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      const int buf = acc_n & 1;
+      if (!mbar_wait(&bars->acc_full[buf], (acc_n >> 1) & 1, fail)) break;
+      ++acc_n;
+      tc_fence_after();
+      const uint32_t t_acc = tmem + lane_off + buf * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_acc + c0, o);
+        tmem_ld_wait(o);
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * p.scale, __uint_as_float(o[c + 2 * e + 1]) * p.scale);
+            st_global_v4(dst + c0 + c, w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_warp(&bars->acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 // delta_i = <dO_i, O_i> per (row, head), fp32 from bf16 (softmax backward).
@@ -943,6 +1157,23 @@ cudaError_t launch_bwd_pass(const BwdParams& p, int head_dim, int act, bool kv_m
   JG_BWD_CASE(64)
   JG_BWD_CASE(32)
 #undef JG_BWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <int D>
+static cudaError_t launch_dq_ds_t(const BwdParams& p, int grid, cudaStream_t stream) {
+  using C = DqCfg<D>;
+  auto kern = gdpa_dq_ds_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 256, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_ds(const BwdParams& p, int head_dim, int grid, cudaStream_t stream) {
+  if (head_dim == 128) return launch_dq_ds_t<128>(p, grid, stream);
+  if (head_dim == 64) return launch_dq_ds_t<64>(p, grid, stream);
+  if (head_dim == 32) return launch_dq_ds_t<32>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -40,6 +40,8 @@ struct SchedParams {
   int32_t* item_base;   // scratch [batch + 1] per list
   SchedList list[2];
   int n_lists;
+  int64_t* ds_base;     // backward with stored dS: first dS tile of each segment [batch + 1], or nullptr
+  int64_t ds_capacity;  // dS tiles the caller's scratch holds
 };
 
 // Lengths and tile counts of one segment.
@@ -119,6 +121,19 @@ struct BwdParams {
   int32_t bias_len;
   int32_t causal;
   float scale;             // s
+  // Stored dS (optional): the dK/dV pass writes every bf16 dS^T tile to a
+  // scratch array of [128 keys][128 queries] tiles; tile of (segment b, head
+  // h, key tile kt, query tile qt) = ds_base[b] + (h nk_b + kt) nq_b + qt.
+  CUtensorMap tm_ds;       // 2-D over the scratch: 128 columns x (tiles * 128) rows
+  const int64_t* ds_base;  // nullptr: no stored dS
 };
+
+constexpr int kDsTileBytes = kTile * kTile * 2;
+
+// First row of a dS tile in the scratch's 2-D view.
+__device__ __forceinline__ int ds_row(const int64_t* ds_base, const Seg& s, int b, int h, int kt, int qt) {
+  const int64_t nq = ceil_div(s.lq, kTile), nk = ceil_div(s.lkv, kTile);
+  return static_cast<int>((__ldg(ds_base + b) + (static_cast<int64_t>(h) * nk + kt) * nq + qt) * kTile);
+}
 
 }  // namespace jg

@@ -61,6 +61,31 @@ __device__ int block_inclusive_scan(int v, int* warp_tot) {
   return v;
 }
 
+// The same for 64-bit values.
+__device__ long long block_inclusive_scan64(long long v, long long* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_tot[lane] = w;
+  }
+  __syncthreads();
+  if (warp > 0) v += warp_tot[warp - 1];
+  __syncthreads();
+  return v;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_constant__ SchedParams p) {
@@ -96,6 +121,37 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
       *L.n_units = 0;
     }
     return;
+  }
+
+  // ---- stored dS (backward): first scratch tile of each segment, H nq nk
+  // tiles per segment, checked against the caller's capacity
+  if (p.ds_base != nullptr && blockIdx.x == 0) {
+    __shared__ long long warp_tot64[32];
+    __shared__ long long carry64;
+    if (tid == 0) carry64 = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < p.batch; c0 += kSchedThreads) {
+      const int b = c0 + tid;
+      long long v = 0;
+      if (b < p.batch) {
+        const Seg sg = load_seg(p.q_off, p.kv_off, b);
+        v = static_cast<long long>(p.heads) * ceil_div(sg.lq, kTile) * ceil_div(sg.lkv, kTile);
+      }
+      const long long incl = block_inclusive_scan64(v, warp_tot64);
+      if (b < p.batch) p.ds_base[b] = carry64 + incl - v;
+      __syncthreads();
+      if (tid == kSchedThreads - 1) carry64 += incl;
+      __syncthreads();
+    }
+    if (tid == 0) {
+      p.ds_base[p.batch] = carry64;
+      if (carry64 > p.ds_capacity) {  // the scratch is too small for these lengths
+        atomicCAS(p.status, kOk, kErrScratchTooSmall);
+        *L.n_units = 0;
+      }
+    }
+    __syncthreads();
+    if (carry64 > p.ds_capacity) return;
   }
 
   // ---- items per segment, exclusive prefix sum into base[]

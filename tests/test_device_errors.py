@@ -88,3 +88,26 @@ def test_misaligned_pointer_is_rejected(jg):
     with pytest.raises(jg.JgdpaError) as e:
         jg.jgdpa_fwd(q_mis, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale)
     assert e.value.code == 3
+
+
+def test_stored_ds_scratch_too_small_is_reported(jg):
+    """A stored-dS scratch smaller than the lengths need: the device records
+    status 4 and the passes do nothing; the next call with enough scratch
+    succeeds."""
+    x = workloads.random_case(8, batch=3, heads=2, head_dim=64, act="gelu", lq_range=(200, 300),
+                              lkv_range=(200, 300))
+    d = x.to("cuda")
+    out, lse = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale)
+    need = jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, x.heads)
+    assert need == x.heads * 32768 * sum(-(-int(a) // 128) * -(-int(b) // 128) for a, b in zip(x.lq, x.lkv))
+    nbytes = jg.jgdpa_workspace_bytes(x.batch, x.q.shape[0], x.k.shape[0], x.heads, x.head_dim, x.act, 0, True)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    small = torch.empty(need - 32768, dtype=torch.uint8, device="cuda")
+    jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale, workspace=ws,
+                 ds_scratch=small)
+    assert jg.jgdpa_read_device_status(ws) == 4
+    enough = torch.empty(need, dtype=torch.uint8, device="cuda")
+    dq, dk, dv, _ = jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
+                                 workspace=ws, ds_scratch=enough)
+    assert jg.jgdpa_read_device_status(ws) == 0
+    assert torch.isfinite(dq.float()).all() and torch.isfinite(dk.float()).all()

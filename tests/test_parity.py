@@ -33,14 +33,23 @@ def run_fwd(jg, x):
     return out.cpu(), (None if lse is None else lse.cpu())
 
 
-def run_bwd(jg, x, out=None, lse=None):
+def run_bwd(jg, x, out=None, lse=None, stored=False):
+    """Backward through the C ABI; stored=True takes the stored-dS path
+    (jgdpa_bwd_ex with a scratch of exactly jgdpa_ds_scratch_bytes)."""
     d = x.to("cuda")
     if x.act == "softmax":
         out, lse = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale,
                                 bias_table=d.bias, causal=x.causal)
+    scratch = None
+    if stored:
+        nbytes = jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, x.heads)
+        scratch = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(jg.jgdpa_workspace_bytes(x.batch, x.q.shape[0], x.k.shape[0], x.heads, x.head_dim, x.act,
+                                              x.bias_len, True), dtype=torch.uint8, device="cuda")
     dq, dk, dv, db = jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act,
-                                  x.scale, bias_table=d.bias, causal=x.causal)
+                                  x.scale, bias_table=d.bias, causal=x.causal, workspace=ws, ds_scratch=scratch)
     torch.cuda.synchronize()
+    assert jg.jgdpa_read_device_status(ws) == 0, "device status"
     return dq.cpu(), dk.cpu(), dv.cpu(), (None if db is None else db.cpu())
 
 
@@ -54,8 +63,9 @@ def check_fwd_full(jg, x, tag=""):
         assert_close(f"LSE {tag}", lse.numpy()[valid], rlse[valid])
 
 
-def check_bwd_full(jg, x, tag=""):
-    dq, dk, dv, db = run_bwd(jg, x)
+def check_bwd_full(jg, x, tag="", stored=False):
+    dq, dk, dv, db = run_bwd(jg, x, stored=stored)
+    tag = f"{tag}{' stored-dS' if stored else ''}"
     rq, rk, rv, rb = oracle_bwd(x)
     assert_close(f"dQ {tag}", dq, rq)
     assert_close(f"dK {tag}", dk, rk)
@@ -81,11 +91,12 @@ def test_forward_small(jg, d, act, bias_len, causal):
     check_fwd_full(jg, x, f"d={d} {act} bias={bias_len} causal={causal}")
 
 
+@pytest.mark.parametrize("stored", [False, True])
 @pytest.mark.parametrize("d,act,bias_len,causal", SMALL)
-def test_backward_small(jg, d, act, bias_len, causal):
+def test_backward_small(jg, d, act, bias_len, causal, stored):
     x = workloads.random_case(2000 + d + bias_len + int(causal), batch=4, heads=2, head_dim=d, act=act,
                               lq_range=(1, 300), lkv_range=(1, 300), causal=causal, bias_len=bias_len)
-    check_bwd_full(jg, x, f"d={d} {act} bias={bias_len} causal={causal}")
+    check_bwd_full(jg, x, f"d={d} {act} bias={bias_len} causal={causal}", stored=stored)
 
 
 @pytest.mark.parametrize("act", ["gelu", "softmax"])
@@ -97,22 +108,28 @@ def test_edge_lengths(jg, act):
     x = workloads.make_inputs(lq, lkv, 3, 64, act, causal=False, bias_len=7, rng=rng)
     check_fwd_full(jg, x, "edge fwd")
     check_bwd_full(jg, x, "edge bwd")
+    check_bwd_full(jg, x, "edge bwd", stored=True)
     x = workloads.make_inputs(lq, lkv, 3, 64, act, causal=True, bias_len=0, rng=rng)
     check_fwd_full(jg, x, "edge fwd causal")
     check_bwd_full(jg, x, "edge bwd causal")
+    check_bwd_full(jg, x, "edge bwd causal", stored=True)
 
 
 def test_workload_1_tiny_full(jg):
     x = workloads.workload_inputs(1)
     check_fwd_full(jg, x, "w1")
     check_bwd_full(jg, x, "w1")
+    check_bwd_full(jg, x, "w1", stored=True)
 
 
 # ------------------------------------------------------ full-size workloads
-def check_sampled(jg, x, units_fwd, units_bwd, tag):
+def check_sampled(jg, x, units_fwd, units_bwd, tag, stored=False):
     """Full-size GPU run; oracle on the sampled units; compare those units' rows
-    (each tensor gathered over all sampled units, then one max-relative check)."""
+    (each tensor gathered over all sampled units, then one max-relative check).
+    The forward is checked on the recompute run only."""
     out, lse = run_fwd(jg, x)
+    if stored:
+        units_fwd = []
     got, want, got_l, want_l = [], [], [], []
     for b, h, qr, kr, (o, l) in sampled_oracle(x, units_fwd, backward=False):
         got.append(out.float().numpy()[qr, h])
@@ -120,10 +137,12 @@ def check_sampled(jg, x, units_fwd, units_bwd, tag):
         if x.act == "softmax":
             got_l.append(lse.numpy()[h, qr])
             want_l.append(l)
-    assert_close(f"O {tag}", np.concatenate(got), np.concatenate(want))
-    if x.act == "softmax":
+    if got:
+        assert_close(f"O {tag}", np.concatenate(got), np.concatenate(want))
+    if got_l:
         assert_close(f"LSE {tag}", np.concatenate(got_l), np.concatenate(want_l))
-    dq, dk, dv, db = run_bwd(jg, x)
+    dq, dk, dv, db = run_bwd(jg, x, stored=stored)
+    tag = f"{tag}{' stored-dS' if stored else ''}"
     g = {"dQ": [], "dK": [], "dV": []}
     w = {"dQ": [], "dK": [], "dV": []}
     for b, h, qr, kr, (rq, rk, rv) in sampled_oracle(x, units_bwd, backward=True):
@@ -150,3 +169,4 @@ def test_full_size_workloads_sampled(jg, idx, n_random, max_pairs_fwd, max_pairs
     uf = sample_units(x, n_random, seed=idx, max_pairs=max_pairs_fwd)
     ub = sample_units(x, n_random, seed=100 + idx, max_pairs=max_pairs_bwd)
     check_sampled(jg, x, uf, ub, f"w{idx}")
+    check_sampled(jg, x, uf, ub, f"w{idx}", stored=True)
