@@ -447,6 +447,7 @@ __device__ void bwd_ds_store(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
   uint8_t* x_base = smem + C::kXOff;
   XRing x;
   const bool leader = elect_one();
+  const uint64_t policy = l2_evict_first_policy();
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
@@ -459,8 +460,8 @@ __device__ void bwd_ds_store(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
       if (leader) {
         const int row = ds_row(p.ds_base, u.seg, u.b, u.h, u.tile, u.first + i);
         const uint8_t* src = x_base + xs * C::kXBytes;
-        tma_store_2d(&p.tm_ds, src, 0, row);
-        tma_store_2d(&p.tm_ds, src + C::kXBytes / 2, kTile / 2, row);
+        tma_store_2d_hint(&p.tm_ds, src, 0, row, policy);
+        tma_store_2d_hint(&p.tm_ds, src + C::kXBytes / 2, kTile / 2, row, policy);
         bulk_commit();
         bulk_wait_read_all();
         mbar_arrive(&bars->x_empty[xs]);
@@ -985,6 +986,7 @@ __global__ void __launch_bounds__(256, 1) gdpa_dq_ds_kernel(const __grid_constan
 
   if (warp == 0) {  // ---- producer
     const bool leader = elect_one();
+    const uint64_t policy = l2_evict_first_policy();  // each dS tile is read once
     uint32_t it = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -999,8 +1001,8 @@ __global__ void __launch_bounds__(256, 1) gdpa_dq_ds_kernel(const __grid_constan
           uint8_t* dst = smem + st * C::kStageBytes;
           mbar_arrive_tx(&bars->full[st], C::kStageBytes);
           const int row = ds_row(p.ds_base, u.seg, u.b, u.h, kt, u.tile);
-          tma_load_2d(dst, &p.tm_ds, &bars->full[st], 0, row);
-          tma_load_2d(dst + kDsTileBytes / 2, &p.tm_ds, &bars->full[st], kTile / 2, row);
+          tma_load_2d_hint(dst, &p.tm_ds, &bars->full[st], 0, row, policy);
+          tma_load_2d_hint(dst + kDsTileBytes / 2, &p.tm_ds, &bars->full[st], kTile / 2, row, policy);
 #pragma unroll
           for (int cb = 0; cb < C::kNumBlocks; ++cb)
             tma_load_3d(dst + kDsTileBytes + cb * C::kBlockBytes, &p.tm_k, &bars->full[st], cb * C::kBlockCols,
