@@ -488,9 +488,11 @@ struct PairGeom {
   float bconst;  // the bias of every element when not band (0 without a table)
 };
 
+// bc_lo / bc_hi: the table's two end entries (the bias of every element of
+// a tile that lies wholly below -R / above +R), loaded once per unit.
 template <bool KV_MAJOR>
 __device__ __forceinline__ PairGeom pair_geom(const BwdParams& p, const BwdUnit& u, int pt, int r, bool row_ok,
-                                              const float* brow, int R) {
+                                              const float* brow, int R, float bc_lo, float bc_hi) {
   PairGeom g;
   g.lo = 0;
   if constexpr (KV_MAJOR) {
@@ -510,7 +512,7 @@ __device__ __forceinline__ PairGeom pair_geom(const BwdParams& p, const BwdUnit&
   const int relmax = relmin + 2 * (kTile - 1);
   g.band = brow != nullptr && relmin < R && relmax > -R;
   g.upper = relmin >= R;
-  g.bconst = brow == nullptr ? 0.f : (g.upper ? __ldg(brow + 2 * R) : __ldg(brow));
+  g.bconst = g.upper ? bc_hi : bc_lo;
   return g;
 }
 
@@ -646,6 +648,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     const float* brow = p.bias_len ? p.bias + static_cast<int64_t>(u.h) * p.bias_len : nullptr;
     float* part = want_dbias ? p.dbias_part + (static_cast<int64_t>(blockIdx.x) * H + u.h) * p.bias_len : nullptr;
     float acc_lo = 0.f, acc_hi = 0.f;  // dbias mass clamped to the table's ends
+    const float bc_lo = brow ? __ldg(brow) : 0.f, bc_hi = brow ? __ldg(brow + 2 * R) : 0.f;
 
     if (u.count == 0) {  // no partner rows: the gradient rows are zero
       if (row_ok) {
@@ -674,7 +677,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     bool ok = true;
     for (int i = 0; i < u.count; ++i) {
       const int pt = u.first + i;  // partner tile
-      const PairGeom g = pair_geom<KV_MAJOR>(p, u, pt, r, row_ok, brow, R);
+      const PairGeom g = pair_geom<KV_MAJOR>(p, u, pt, r, row_ok, brow, R, bc_lo, bc_hi);
 
       // ---- S (S^T) of this tile into registers; its TMEM columns go back to
       // the MMA issuer for the next tile

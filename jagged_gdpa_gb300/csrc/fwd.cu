@@ -305,16 +305,18 @@ struct TileBias {
   const float* row;   // this head's table
 };
 
-__device__ __forceinline__ TileBias tile_bias(const FwdParams& p, int h, int i0, int r, int j0) {
+// bc_lo / bc_hi: the head's two end entries, loaded once per unit.
+__device__ __forceinline__ TileBias tile_bias(const FwdParams& p, int h, int i0, int r, int j0, float bc_lo,
+                                              float bc_hi) {
   TileBias t{false, 0.f, 0, p.bias_len - 1, nullptr};
   if (p.bias_len == 0) return t;
   const int R = (p.bias_len - 1) / 2;
   const int delta = i0 - j0;
   t.row = p.bias + static_cast<int64_t>(h) * p.bias_len;
   if (delta - (kTile - 1) >= R) {
-    t.value = __ldg(t.row + 2 * R);
+    t.value = bc_hi;
   } else if (delta + (kTile - 1) <= -R) {
-    t.value = __ldg(t.row);
+    t.value = bc_lo;
   } else {
     t.band = true;
     t.base = delta + r + R;
@@ -469,6 +471,12 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
       continue;
     }
     float m_run = -INFINITY, l_run = 0.f;  // softmax state (base 2)
+    float bc_lo = 0.f, bc_hi = 0.f;
+    if (p.bias_len) {
+      const float* brow = p.bias + static_cast<int64_t>(u.h) * p.bias_len;
+      bc_lo = __ldg(brow);
+      bc_hi = __ldg(brow + p.bias_len - 1);
+    }
     bool ok = true;
     for (int kt = 0; kt < nkv; ++kt) {
       if (!(ok = mbar_wait(&bars->s_full[slot], s_it & 1, fail))) break;
@@ -478,7 +486,7 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
       int nvalid = min(kTile, u.seg.lkv - j0);
       if (p.causal) nvalid = min(nvalid, t * kTile + r - j0 + 1);
       const bool tile_masked = (u.seg.lkv - j0 < kTile) || (p.causal && kt == t);
-      const TileBias tb = tile_bias(p, u.h, t * kTile, r, j0);
+      const TileBias tb = tile_bias(p, u.h, t * kTile, r, j0, bc_lo, bc_hi);
       if constexpr (!kSoftmax) {
         const float hs = 0.5f * p.scale;
         if (tb.band) {
