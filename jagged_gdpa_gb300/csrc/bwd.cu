@@ -610,14 +610,6 @@ __device__ __forceinline__ void phase_b_chunk(const uint32_t (&dv)[32], const fl
   }
 }
 
-// Stores this thread's 32 packed bf16 pairs of one chunk (columns
-// [64 half + 32 chunk, +32) of row r) into an X tile.
-__device__ __forceinline__ void store_x_chunk(uint32_t x_tile, int half, int chunk, int r, const uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    st_shared_v4(swz128_addr(x_tile, half, r, 4 * chunk + j), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-}
-
 template <int D, int ACT, bool KV_MAJOR>
 __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units, Fail fail) {
   using C = BwdCfg<D, KV_MAJOR>;

@@ -346,5 +346,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ uint32_t swz128_addr(uint32_t tile, int blk, int r, int j) {
   return tile + blk * 16384 + r * 128 + ((j ^ (r & 7)) << 4);
 }
+// Stores this thread's 16 packed bf16 pairs of one 32-column chunk (columns
+// [64 half + 32 chunk, +32) of row r) into such a tile.
+__device__ __forceinline__ void store_x_chunk(uint32_t x_tile, int half, int chunk, int r, const uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared_v4(swz128_addr(x_tile, half, r, 4 * chunk + j), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+}
 
 }  // namespace jg
