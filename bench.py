@@ -82,9 +82,13 @@ WORKLOAD_TEXT = {
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch on the full
-# long-tail workload, from an ncu capture of the current kernels; empty when
-# the kernels have changed since the last capture.
-TRAFFIC = {}
+# long-tail workload, from a one-pass ncu capture of the current kernels at
+# that size; emptied whenever a kernel changes after the capture.
+TRAFFIC = {
+    "gdpa_fwd_kernel": 1.396505e9 + 0.323991e9,
+    "gdpa_bwd_kernel (dK/dV pass)": 2.473366e9 + 13.151134e9,
+    "gdpa_bwd_kernel (dQ pass)": 12.911671e9 + 0.262393e9,
+}
 
 
 def peaks():
@@ -364,21 +368,31 @@ def run_native(args, world, rank, local):
     bwd_ms = statistics.mean(ms_bwd)
     # Per-kernel rooflines.  Algorithmic FLOPs per launch: forward 2 matmuls
     # (S, PV) = f_fwd; dK/dV pass S^T, dP^T, dV, dK = 2 f_fwd; dQ pass (dQ
-    # from the dS tiles the dK/dV pass stored) = f_fwd / 4.  The forward's time includes the ~10 us
+    # from the dS tiles the dK/dV pass stored, one matmul) = f_fwd / 2.  The
+    # forward's time includes the ~10 us
     # scheduling kernel of its call; the passes are timed by events recorded
     # between their launches inside the backward call.
     kernels = {
         "gdpa_fwd_kernel": (fwd_ms, f_fwd),
         "gdpa_bwd_kernel (dK/dV pass)": (statistics.mean(ms_kv), 2.0 * f_fwd),
-        "gdpa_bwd_kernel (dQ pass)": (statistics.mean(ms_q), 0.25 * f_fwd),
+        "gdpa_bwd_kernel (dQ pass)": (statistics.mean(ms_q), 0.5 * f_fwd),
     }
     per_kernel = {k: {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                       "frac": round(fl / (ms * 1e-3) / 1e12 / bf16_sust, 4)} for k, (ms, fl) in kernels.items()}
+    # dram bytes per launch from the ncu capture above, valid for the full
+    # long-tail workload only; with them each kernel also reports its DRAM
+    # throughput against the measured copy bandwidth (the dQ pass streams the
+    # stored dS tiles and is bound there, not on the tensor pipe)
+    full_size = args.workload == 5 and not args.segments
+    if full_size:
+        for k, (ms, _) in kernels.items():
+            if k in TRAFFIC:
+                gbs = TRAFFIC[k] / (ms * 1e-3) / 1e9
+                per_kernel[k].update({"dram_gb": round(TRAFFIC[k] / 1e9, 3), "dram_gbs": round(gbs, 1),
+                                      "dram_frac": round(gbs / hbm, 4)})
     dom = max(kernels, key=lambda k: kernels[k][0])
     dom_ms, dom_fl = kernels[dom]
-    # dram bytes per launch of the dominant kernel from the ncu capture
-    # above, valid for the full long-tail workload only
-    traffic = TRAFFIC.get(dom) if (args.workload == 5 and not args.segments) else None
+    traffic = TRAFFIC.get(dom) if full_size else None
     result = {
         "metric": METRIC,
         "value": round(value, 2),
