@@ -77,9 +77,14 @@ struct BwdCfg : TileCfg<D> {
   static constexpr int kStagesA = D == 128 ? 3 : 4;
   static constexpr int kStagesB = D == 128 ? 1 : (D == 64 ? 2 : 4);
   static constexpr int kNumX = D == 128 ? 1 : 2;
+  // resident pairs: two where they fit, so that the next unit's pair loads
+  // while this one computes (units of one partner tile are otherwise
+  // serialised on the copy latency)
+  static constexpr int kNumRes = D == 128 ? 1 : 2;
   static constexpr int kXBytes = kTile * kTile * 2;
   static constexpr int kResOff = 0;
-  static constexpr int kAOff = 2 * T::kTileBytes;
+  static constexpr int kResBytes = 2 * T::kTileBytes;
+  static constexpr int kAOff = kNumRes * kResBytes;
   static constexpr int kBOff = kAOff + kStagesA * T::kTileBytes;
   static constexpr int kXOff = kBOff + kStagesB * T::kTileBytes;
   static constexpr int kBarOff = kXOff + kNumX * kXBytes;
@@ -89,7 +94,7 @@ struct BwdCfg : TileCfg<D> {
 };
 
 struct BwdBars {
-  uint64_t res_full, res_empty;
+  uint64_t res_full[2], res_empty[2];
   uint64_t s_full, s_free, p_full, dp_full, dp_free, acc_full, acc_empty;
   uint64_t drain;
   uint64_t x_full[2], x_empty[2];
@@ -214,17 +219,18 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
     const BwdUnit u = bwd_unit<KV_MAJOR>(p, idx);
     if (u.count == 0) continue;
     if constexpr (STREAM == 0) {
-      if (!(ok = mbar_wait_warp(&bars->res_empty, (res_it & 1) ^ 1, fail))) break;
+      const int rs = res_it % C::kNumRes;
+      if (!(ok = mbar_wait_warp(&bars->res_empty[rs], ((res_it / C::kNumRes) & 1) ^ 1, fail))) break;
       ++res_it;
       const int row = (KV_MAJOR ? u.seg.k0 : u.seg.q0) + u.tile * kTile;
       if (leader) {
-        mbar_arrive_tx(&bars->res_full, 2 * C::kTileBytes);
-        uint8_t* d0 = smem + C::kResOff;
+        uint64_t* bar = &bars->res_full[rs];
+        mbar_arrive_tx(bar, 2 * C::kTileBytes);
+        uint8_t* d0 = smem + C::kResOff + rs * C::kResBytes;
 #pragma unroll
         for (int cb = 0; cb < C::kNumBlocks; ++cb) {
-          tma_load_3d(d0 + cb * C::kBlockBytes, res0, &bars->res_full, cb * C::kBlockCols, u.h, row);
-          tma_load_3d(d0 + C::kTileBytes + cb * C::kBlockBytes, res1, &bars->res_full, cb * C::kBlockCols, u.h,
-                      row);
+          tma_load_3d(d0 + cb * C::kBlockBytes, res0, bar, cb * C::kBlockCols, u.h, row);
+          tma_load_3d(d0 + C::kTileBytes + cb * C::kBlockBytes, res1, bar, cb * C::kBlockCols, u.h, row);
         }
       }
     }
@@ -243,7 +249,9 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
     }
   }
   if (!ok) {
-    if (STREAM == 0 && res_it) mbar_wait_drain(&bars->res_full, (res_it - 1) & 1);
+    if (STREAM == 0)
+      for (uint32_t i = res_it > C::kNumRes ? res_it - C::kNumRes : 0; i < res_it; ++i)
+        mbar_wait_drain(&bars->res_full[i % C::kNumRes], (i / C::kNumRes) & 1);
     for (uint32_t i = st_it > kStages ? st_it - kStages : 0; i < st_it; ++i)
       mbar_wait_drain(&full[i % kStages], (i / kStages) & 1);
   }
@@ -276,7 +284,7 @@ template <int D>
 __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                            Fail fail) {
   using C = BwdCfg<D, true>;
-  const uint32_t k_t = smem_u32(smem + C::kResOff), v_t = k_t + C::kTileBytes;
+  const uint32_t res_base = smem_u32(smem + C::kResOff);
   const uint32_t a_base = smem_u32(smem + C::kAOff), b_base = smem_u32(smem + C::kBOff);
   const uint32_t x_base = smem_u32(smem + C::kXOff);
   uint32_t res_it = 0, st_it = 0, acc_it = 0, p_n = 0, dp_n = 0;
@@ -288,8 +296,10 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
     if (idx >= n_units) break;
     const BwdUnit u = bwd_unit<true>(p, idx);
     if (u.count == 0) continue;
-    if (!(ok = mbar_wait_warp(&bars->res_full, res_it & 1, fail))) break;
+    const int rs = res_it % C::kNumRes;
+    if (!(ok = mbar_wait_warp(&bars->res_full[rs], (res_it / C::kNumRes) & 1, fail))) break;
     ++res_it;
+    const uint32_t k_t = res_base + rs * C::kResBytes, v_t = k_t + C::kTileBytes;
     {  // S^T and dP^T of the first query tile (S^T after the previous unit's
        // last dV in issue order, which has read its P^T)
       const int sa = st_it % C::kStagesA, sb = st_it % C::kStagesB;
@@ -347,7 +357,7 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
     if (!ok) break;
     st_it += u.count;
     if (leader) mma_commit(&bars->acc_full);
-    if (leader) mma_commit(&bars->res_empty);
+    if (leader) mma_commit(&bars->res_empty[rs]);
   }
   if (leader) mma_commit(&bars->drain);
   mbar_wait_drain(&bars->drain, 0);
@@ -363,7 +373,7 @@ template <int D>
 __device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                           Fail fail) {
   using C = BwdCfg<D, false>;
-  const uint32_t q_t = smem_u32(smem + C::kResOff), do_t = q_t + C::kTileBytes;
+  const uint32_t res_base = smem_u32(smem + C::kResOff);
   const uint32_t a_base = smem_u32(smem + C::kAOff), b_base = smem_u32(smem + C::kBOff);
   const uint32_t x_base = smem_u32(smem + C::kXOff);
   uint32_t res_it = 0, st_it = 0, acc_it = 0, s_n = 0, dp_n = 0;
@@ -375,8 +385,10 @@ __device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint
     if (idx >= n_units) break;
     const BwdUnit u = bwd_unit<false>(p, idx);
     if (u.count == 0) continue;
-    if (!(ok = mbar_wait_warp(&bars->res_full, res_it & 1, fail))) break;
+    const int rs = res_it % C::kNumRes;
+    if (!(ok = mbar_wait_warp(&bars->res_full[rs], (res_it / C::kNumRes) & 1, fail))) break;
     ++res_it;
+    const uint32_t q_t = res_base + rs * C::kResBytes, do_t = q_t + C::kTileBytes;
     {  // S and dP of the first key tile
       const int sa = st_it % C::kStagesA, sb = st_it % C::kStagesB;
       if (!(ok = mbar_wait_warp(&bars->s_free, (s_n & 1) ^ 1, fail))) break;
@@ -431,7 +443,7 @@ __device__ void bwd_mma_q(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint
     if (!ok) break;
     st_it += u.count;
     if (leader) mma_commit(&bars->acc_full);
-    if (leader) mma_commit(&bars->res_empty);
+    if (leader) mma_commit(&bars->res_empty[rs]);
   }
   if (leader) mma_commit(&bars->drain);
   mbar_wait_drain(&bars->drain, 0);
@@ -670,12 +682,32 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     for (int i = 0; i < u.count; ++i) {
       const int pt = u.first + i;  // partner tile
       const PairGeom g = pair_geom<KV_MAJOR>(p, u, pt, r, row_ok, brow, R, bc_lo, bc_hi);
+      // softmax, key-major: log2-scaled LSE and D of the query columns this
+      // warpgroup owns, one value per lane and 32-column chunk, loaded before
+      // the wait for S and broadcast by shuffles (every query tile is new to
+      // L1: loads issued at their use would wait on L2 four times per tile)
+      float cur_lse[2] = {0.f, 0.f}, cur_del[2] = {0.f, 0.f};
+      if constexpr (kSoftmax && KV_MAJOR) {
+        const int c0 = 64 * half + (threadIdx.x & 31);
+        const int64_t q0 = static_cast<int64_t>(u.h) * p.total_q + u.seg.q0 + pt * kTile + c0;
+        const int lim = u.seg.lq - pt * kTile - c0;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          cur_lse[c] = 32 * c < lim ? __ldg(p.lse + q0 + 32 * c) * kLog2e : 0.f;
+          cur_del[c] = 32 * c < lim ? __ldg(p.delta + q0 + 32 * c) : 0.f;
+        }
+      }
 
       // ---- S (S^T) of this tile into registers; its TMEM columns go back to
       // the MMA issuer for the next tile
       if (!(ok = mbar_wait(&bars->s_full, s_it & 1, fail))) break;
       ++s_it;
       tc_fence_after();
+      // 32-column chunks of this warpgroup's 64 columns that hold a partner
+      // row of the segment (the same for every thread); phase B skips the
+      // others and writes zero dS there (phase A's mask already zeroes P)
+      const int ncols = (KV_MAJOR ? u.seg.lq : u.seg.lkv) - pt * kTile - 64 * half;
+      const int live = ncols >= 33 ? 2 : (ncols >= 1 ? 1 : 0);
       uint32_t sv0[32], sv1[32];
       tmem_ld32(t_s, sv0);
       tmem_ld32(t_s + 32, sv1);
@@ -691,15 +723,13 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       for (int chunk = 0; chunk < 2; ++chunk) {
         const int cbase = 64 * half + 32 * chunk;
         const uint32_t(&sv)[32] = chunk == 0 ? sv0 : sv1;
-        float lse_c[32];
-        if constexpr (kSoftmax && KV_MAJOR) {
-          const int64_t q0 = static_cast<int64_t>(u.h) * p.total_q + u.seg.q0 + pt * kTile + cbase;
-          const int lim = max(0, min(32, u.seg.lq - pt * kTile - cbase));
-#pragma unroll
-          for (int e = 0; e < 32; ++e) lse_c[e] = e < lim ? __ldg(p.lse + q0 + e) * kLog2e : 0.f;
-        }
         uint32_t pk[16];
         float(&keep)[32] = chunk == 0 ? keep0 : keep1;
+        float lse_c[32];
+        if constexpr (kSoftmax && KV_MAJOR) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) lse_c[e] = __shfl_sync(0xffffffffu, cur_lse[chunk], e);
+        }
 #define JG_PHASE_A(CH, BAND, MASKED)                                                                         \
   phase_a_chunk<ACT, KV_MAJOR, CH, BAND, MASKED>(sv, lse_c, lse2_row, g, brow, R, cbase, hs, s2, keep, pk)
         if (chunk == 0) {
@@ -737,7 +767,6 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       // needed before the next tile's phase B.
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
-        const int cbase = 64 * half + 32 * chunk;
         uint32_t dv[32];
         tmem_ld32(t_dp + 32 * chunk, dv);
         tmem_ld_wait(dv);
@@ -745,26 +774,29 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
           tc_fence_before();
           mbar_arrive_warp(&bars->dp_free);
         }
-        float del_c[32];
-        if constexpr (kSoftmax && KV_MAJOR) {
-          const int64_t q0 = static_cast<int64_t>(u.h) * p.total_q + u.seg.q0 + pt * kTile + cbase;
-          const int lim = max(0, min(32, u.seg.lq - pt * kTile - cbase));
-#pragma unroll
-          for (int e = 0; e < 32; ++e) del_c[e] = e < lim ? __ldg(p.delta + q0 + e) : 0.f;
-        }
         uint32_t pk[16];
-        const float(&keep)[32] = chunk == 0 ? keep0 : keep1;
+        if (chunk < live) {
+          float del_c[32];
+          if constexpr (kSoftmax && KV_MAJOR) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) del_c[e] = __shfl_sync(0xffffffffu, cur_del[chunk], e);
+          }
+          const float(&keep)[32] = chunk == 0 ? keep0 : keep1;
 #define JG_PHASE_B(DB) \
   phase_b_chunk<ACT, KV_MAJOR, DB, 0>(dv, del_c, delta_row, keep, row_sum, dacc, pk)
 #define JG_PHASE_B1(DB) \
   phase_b_chunk<ACT, KV_MAJOR, DB, 1>(dv, del_c, delta_row, keep, row_sum, dacc, pk)
-        if (chunk == 0) {
-          if (dmode == 0) JG_PHASE_B(0); else if (dmode == 1) JG_PHASE_B(1); else JG_PHASE_B(2);
-        } else {
-          if (dmode == 0) JG_PHASE_B1(0); else if (dmode == 1) JG_PHASE_B1(1); else JG_PHASE_B1(2);
-        }
+          if (chunk == 0) {
+            if (dmode == 0) JG_PHASE_B(0); else if (dmode == 1) JG_PHASE_B(1); else JG_PHASE_B(2);
+          } else {
+            if (dmode == 0) JG_PHASE_B1(0); else if (dmode == 1) JG_PHASE_B1(1); else JG_PHASE_B1(2);
+          }
 #undef JG_PHASE_B
 #undef JG_PHASE_B1
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = 0u;
+        }
         if (chunk == 0 && !(ok = mbar_wait(&bars->x_empty[x.slot<C::kNumX>()], x.empty_parity<C::kNumX>(), fail)))
           break;
         store_x_chunk(x_base + x.slot<C::kNumX>() * C::kXBytes, half, chunk, r, pk);
@@ -865,8 +897,10 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kBarOff);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    mbar_init(&bars->res_full, 1);
-    mbar_init(&bars->res_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->res_full[i], 1);
+      mbar_init(&bars->res_empty[i], 1);
+    }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 8);
     mbar_init(&bars->p_full, 8);

@@ -336,8 +336,11 @@ __device__ __forceinline__ float2 band_bias2(const TileBias& tb, int c, float mu
 // The four 32-column chunks are software-pipelined: the TMEM load of chunk
 // q + 1 is in flight while chunk q is computed and its P stored (P of chunk q
 // lands in columns [16q, 16q + 16), all read already).
+// nchunks (>= 1, the same for every thread): 32-column chunks that hold a
+// key row of the segment; the rest are not computed, and their P is zero (the
+// PV product reads every column).
 template <int ACT, int NALU, bool BAND, bool MASKED>
-__device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias& tb, int nvalid) {
+__device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias& tb, int nvalid, int nchunks) {
   const float hb = 0.5f * tb.value;
   uint32_t buf0[32], buf1[32];
   tmem_ld32(t_s, buf0);
@@ -348,21 +351,26 @@ __device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias&
     uint32_t(&nxt)[32] = (q & 1) ? buf0 : buf1;
     if (q < 3) tmem_ld32(t_s + 32 * (q + 1), nxt);
     uint32_t pk[16];
+    if (MASKED && q >= nchunks) {
 #pragma unroll
-    for (int c2 = 0; c2 < 16; ++c2) {
-      const int c = 32 * q + 2 * c2;
-      const float2 sv = make_float2(__uint_as_float(cur[2 * c2]), __uint_as_float(cur[2 * c2 + 1]));
-      const float2 bias = BAND ? band_bias2(tb, c, 0.5f) : f2(hb);
-      float2 hx = __ffma2_rn(sv, f2(hs), bias);  // x / 2
-      if (MASKED) {
-        if (c >= nvalid) hx.x = 0.f;
-        if (c + 1 >= nvalid) hx.y = 0.f;
+      for (int c2 = 0; c2 < 16; ++c2) pk[c2] = 0u;
+    } else {
+  #pragma unroll
+      for (int c2 = 0; c2 < 16; ++c2) {
+        const int c = 32 * q + 2 * c2;
+        const float2 sv = make_float2(__uint_as_float(cur[2 * c2]), __uint_as_float(cur[2 * c2 + 1]));
+        const float2 bias = BAND ? band_bias2(tb, c, 0.5f) : f2(hb);
+        float2 hx = __ffma2_rn(sv, f2(hs), bias);  // x / 2
+        if (MASKED) {
+          if (c >= nvalid) hx.x = 0.f;
+          if (c + 1 >= nvalid) hx.y = 0.f;
+        }
+        float2 y;
+        if (q >= 4 - NALU) y = act2_route<ACT, 1>(hx);
+        else if (q >= 4 - NALU - kFwdEx2Chunks) y = act2_route<ACT, 2>(hx);
+        else y = act2_route<ACT, 0>(hx);
+        pk[c2] = pack_bf16(y.x, y.y);
       }
-      float2 y;
-      if (q >= 4 - NALU) y = act2_route<ACT, 1>(hx);
-      else if (q >= 4 - NALU - kFwdEx2Chunks) y = act2_route<ACT, 2>(hx);
-      else y = act2_route<ACT, 0>(hx);
-      pk[c2] = pack_bf16(y.x, y.y);
     }
     tmem_st16(t_s + 16 * q, pk);
     if (q < 3) tmem_ld_wait(nxt);
@@ -486,15 +494,16 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
       int nvalid = min(kTile, u.seg.lkv - j0);
       if (p.causal) nvalid = min(nvalid, t * kTile + r - j0 + 1);
       const bool tile_masked = (u.seg.lkv - j0 < kTile) || (p.causal && kt == t);
+      const int nchunks = (min(kTile, u.seg.lkv - j0) + 31) / 32;
       const TileBias tb = tile_bias(p, u.h, t * kTile, r, j0, bc_lo, bc_hi);
       if constexpr (!kSoftmax) {
         const float hs = 0.5f * p.scale;
         if (tb.band) {
-          if (tile_masked) tile_act<ACT, NALU, true, true>(t_s, hs, tb, nvalid);
-          else tile_act<ACT, NALU, true, false>(t_s, hs, tb, nvalid);
+          if (tile_masked) tile_act<ACT, NALU, true, true>(t_s, hs, tb, nvalid, nchunks);
+          else tile_act<ACT, NALU, true, false>(t_s, hs, tb, nvalid, nchunks);
         } else {
-          if (tile_masked) tile_act<ACT, NALU, false, true>(t_s, hs, tb, nvalid);
-          else tile_act<ACT, NALU, false, false>(t_s, hs, tb, nvalid);
+          if (tile_masked) tile_act<ACT, NALU, false, true>(t_s, hs, tb, nvalid, nchunks);
+          else tile_act<ACT, NALU, false, false>(t_s, hs, tb, nvalid, nchunks);
         }
       } else {
         const bool first = kt == 0;
