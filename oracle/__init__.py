@@ -46,10 +46,10 @@ def _load():
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-        lib.oracle_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32,
+        lib.oracle_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32, i32,
                                    P, i32, i32, P, P]
         lib.oracle_fwd.restype = ctypes.c_int
-        lib.oracle_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32,
+        lib.oracle_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32, i32,
                                    P, i32, i32, P, P, P, P]
         lib.oracle_bwd.restype = ctypes.c_int
         lib.oracle_act_eval.argtypes = [i32, P, i64, P, P]
@@ -98,8 +98,10 @@ def _units(units: Optional[Sequence[int]]):
 
 def fwd(q, k, v, q_offsets, kv_offsets, heads: int, head_dim: int, act: str, scale: float,
         bias=None, causal: bool = False, units: Optional[Sequence[int]] = None,
-        threads: int = 0):
+        threads: int = 0, window: int = 0):
     """O (float64 [total_q, H, d]) and LSE (float64 [H, total_q]).
+
+    ``window`` > 0 keeps only the pairs with |i - j| < window (segment-local).
 
     ``units`` restricts the work to (segment, head) units b*H + h; rows of
     other units are returned as NaN.
@@ -114,7 +116,8 @@ def fwd(q, k, v, q_offsets, kv_offsets, heads: int, head_dim: int, act: str, sca
     u, nu = _units(units)
     rc = _load().oracle_fwd(_ptr(qf), _ptr(kf), _ptr(vf), _ptr(qo), _ptr(ko), len(qo) - 1,
                             heads, head_dim, ACT_CODE[act], float(scale), _ptr(bf), bias_len,
-                            int(bool(causal)), _ptr(u), nu, int(threads), _ptr(out), _ptr(lse))
+                            int(bool(causal)), int(window), _ptr(u), nu, int(threads), _ptr(out),
+                            _ptr(lse))
     if rc:
         raise ValueError("oracle_fwd rejected its arguments")
     return out, lse
@@ -122,7 +125,7 @@ def fwd(q, k, v, q_offsets, kv_offsets, heads: int, head_dim: int, act: str, sca
 
 def bwd(q, k, v, dout, q_offsets, kv_offsets, heads: int, head_dim: int, act: str,
         scale: float, bias=None, causal: bool = False,
-        units: Optional[Sequence[int]] = None, threads: int = 0):
+        units: Optional[Sequence[int]] = None, threads: int = 0, window: int = 0):
     """dQ, dK, dV (float64, layouts of q/k/v) and dbias (float64 [H, T] or None)."""
     qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(dout)
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
@@ -135,7 +138,7 @@ def bwd(q, k, v, dout, q_offsets, kv_offsets, heads: int, head_dim: int, act: st
     u, nu = _units(units)
     rc = _load().oracle_bwd(_ptr(qf), _ptr(kf), _ptr(vf), _ptr(dof), _ptr(qo), _ptr(ko),
                             len(qo) - 1, heads, head_dim, ACT_CODE[act], float(scale), _ptr(bf),
-                            bias_len, int(bool(causal)), _ptr(u), nu, int(threads),
+                            bias_len, int(bool(causal)), int(window), _ptr(u), nu, int(threads),
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias))
     if rc:
         raise ValueError("oracle_bwd rejected its arguments")
@@ -145,10 +148,10 @@ def bwd(q, k, v, dout, q_offsets, kv_offsets, heads: int, head_dim: int, act: st
 def fwd_inputs(x, units=None, threads: int = 0):
     """``fwd`` on a ``workloads.Inputs`` bundle."""
     return fwd(x.q, x.k, x.v, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, x.act, x.scale,
-               bias=x.bias, causal=x.causal, units=units, threads=threads)
+               bias=x.bias, causal=x.causal, units=units, threads=threads, window=x.window)
 
 
 def bwd_inputs(x, units=None, threads: int = 0):
     """``bwd`` on a ``workloads.Inputs`` bundle."""
     return bwd(x.q, x.k, x.v, x.dout, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, x.act,
-               x.scale, bias=x.bias, causal=x.causal, units=units, threads=threads)
+               x.scale, bias=x.bias, causal=x.causal, units=units, threads=threads, window=x.window)

@@ -10,7 +10,8 @@
  *
  *   For every segment b and head h, with Lq = q_off[b+1]-q_off[b] and
  *   Lkv = kv_off[b+1]-kv_off[b], segment-local indices i < Lq, j < Lkv, and
- *   valid(i,j) = (j < Lkv) and (not causal or j <= i):
+ *   valid(i,j) = (j < Lkv) and (not causal or j <= i)
+ *                and (window == 0 or |i - j| < window):
  *
  *     x_ij = s * <q_i, k_j> + bias[h][clamp(i-j, -R, R) + R]   (bias optional,
  *                                                               R = (T-1)/2)
@@ -33,6 +34,12 @@
  *     clamp(i-j, -R, R)+R with segment-local i, j, added after scaling;
  *   - the scale multiplies q.k only;
  *   - causal masking is top-left aligned (j <= i);
+ *   - sliding-window attention ("Meta redesigns AI training infrastructure
+ *     ...", section "Custom Kernels and 5D Parallelism ...", names it without
+ *     defining it; the GEM page's opening list speaks of long sequences with
+ *     short attention windows) keeps the pairs with |i - j| < window, again
+ *     with segment-local indices; window = 0 means no window, and with causal
+ *     masking the two conditions combine (i - window < j <= i);
  *   - a row with no valid key gives O_i = 0 (and LSE_i = -inf in softmax mode).
  *
  * The backward pass is the analytic gradient of L = sum O * dO:
@@ -93,13 +100,14 @@ int oracle_act_eval(int32_t act, const double* x, int64_t n, double* y, double* 
 typedef struct {
     const double *q, *k, *v, *dout, *bias;
     const int32_t *q_off, *kv_off;
-    int32_t batch, heads, d, act, bias_len, causal;
+    int32_t batch, heads, d, act, bias_len, causal, window;
     double scale;
 } problem;
 
 static int valid_pair(const problem* p, int64_t i, int64_t j, int64_t lkv) {
     if (j >= lkv) return 0;
     if (p->causal && j > i) return 0;
+    if (p->window > 0 && (i - j >= p->window || j - i >= p->window)) return 0;
     return 1;
 }
 
@@ -240,6 +248,7 @@ static int check_problem(const problem* p) {
     if (p->act < ORACLE_GELU || p->act > ORACLE_IDENTITY) return 1;
     if (p->bias_len < 0 || (p->bias_len > 0 && (p->bias_len % 2) == 0)) return 1;
     if (p->bias_len > 0 && !p->bias) return 1;
+    if (p->window < 0) return 1;
     if (p->batch > 0 && (p->q_off[0] != 0 || p->kv_off[0] != 0)) return 1;
     for (int32_t b = 0; b < p->batch; ++b)
         if (p->q_off[b + 1] < p->q_off[b] || p->kv_off[b + 1] < p->kv_off[b]) return 1;
@@ -262,10 +271,11 @@ static void set_threads(int32_t threads) {
 int oracle_fwd(const double* q, const double* k, const double* v,
                const int32_t* q_off, const int32_t* kv_off, int32_t batch,
                int32_t heads, int32_t d, int32_t act, double scale,
-               const double* bias, int32_t bias_len, int32_t causal,
+               const double* bias, int32_t bias_len, int32_t causal, int32_t window,
                const int32_t* units, int32_t n_units, int32_t threads,
                double* out, double* lse) {
-    problem p = {q, k, v, NULL, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, scale};
+    problem p = {q, k, v, NULL, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, window,
+                 scale};
     if (check_problem(&p)) return 1;
     const int64_t total_q = batch > 0 ? q_off[batch] : 0;
     const int32_t n = units ? n_units : batch * heads;
@@ -285,10 +295,11 @@ int oracle_fwd(const double* q, const double* k, const double* v,
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
                const int32_t* q_off, const int32_t* kv_off, int32_t batch,
                int32_t heads, int32_t d, int32_t act, double scale,
-               const double* bias, int32_t bias_len, int32_t causal,
+               const double* bias, int32_t bias_len, int32_t causal, int32_t window,
                const int32_t* units, int32_t n_units, int32_t threads,
                double* dq, double* dk, double* dv, double* dbias) {
-    problem p = {q, k, v, dout, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, scale};
+    problem p = {q, k, v, dout, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, window,
+                 scale};
     if (check_problem(&p)) return 1;
     const int32_t n = units ? n_units : batch * heads;
     const int32_t t = bias_len > 0 ? bias_len : 1;

@@ -11,6 +11,9 @@ derivative, a missing mask) fails at least one of them:
 * the identity-activation associativity (s Q K^T) V = s Q (K^T V);
 * invariance under permutation of the segments;
 * softmax mode against torch.softmax per segment (a library routine);
+* sliding window: the dense references above with a band mask |i - j| < w,
+  a window of 1 against its closed form, a window no shorter than any
+  segment against the unwindowed oracle, and rows left without any key;
 * closed forms (tests/golden/activation_closed_forms.json and hand-derived
   single-key / zero-query cases).
 """
@@ -63,6 +66,8 @@ def dense_reference(x: workloads.Inputs, act: str = None):
     mask = (j[None] < x.lkv[:, None, None]) & (i[None] < x.lq[:, None, None])
     if x.causal:
         mask = mask & (j <= i)[None]
+    if x.window:
+        mask = mask & (np.abs(i - j) < x.window)[None]
     s = np.einsum("bihc,bjhc->bhij", qp, kp) * x.scale
     if x.bias is not None:
         t = x.bias.shape[1]
@@ -106,6 +111,8 @@ def dense_torch_grads(x: workloads.Inputs):
     mask = (j[None] < lkv[:, None, None]) & (i[None] < lq[:, None, None])
     if x.causal:
         mask = mask & (j <= i)[None]
+    if x.window:
+        mask = mask & ((i - j).abs() < x.window)[None]
     m4 = mask[:, None]
     s = torch.einsum("bihc,bjhc->bhij", qp, kp) * x.scale
     bias = None
@@ -353,9 +360,10 @@ def test_empty_segments():
 
 
 def test_workload_lengths_are_reproduced():
-    """The realized lengths of the five workloads and the offsets derived from them."""
+    """The realized lengths of the workloads and the offsets derived from them
+    (the sliding-window workload draws the long-tail batch)."""
     expect_tot = {1: (147, 22), 2: (133254, 133254), 3: (1054174, 82241),
-                  4: (8192, 1039300), 5: (147612, 147612)}
+                  4: (8192, 1039300), 5: (147612, 147612), 6: (147612, 147612)}
     for idx, w in workloads.WORKLOADS.items():
         lq, lkv = workloads.lengths_for(w)
         assert (int(lq.sum()), int(lkv.sum())) == expect_tot[idx]
@@ -383,3 +391,120 @@ def test_unit_subset_equals_full_run():
         assert np.array_equal(gq[qo[b]:qo[b + 1], h], dq[qo[b]:qo[b + 1], h])
         assert np.array_equal(gk[ko[b]:ko[b + 1], h], dk[ko[b]:ko[b + 1], h])
         assert np.array_equal(gv[ko[b]:ko[b + 1], h], dv[ko[b]:ko[b + 1], h])
+
+
+# ----------------------------------------------------------------------------
+# Sliding window (|i - j| < w, segment-local)
+# ----------------------------------------------------------------------------
+
+WINDOW_MODES = [(a, c, w) for a in ("gelu", "softmax") for c in (False, True) for w in (1, 3, 8)]
+
+
+@pytest.mark.parametrize("act,causal,window", WINDOW_MODES)
+def test_window_forward_matches_dense_bruteforce(act, causal, window):
+    for seed in range(8):
+        x = workloads.random_case(700 + seed, batch=1 + seed % 5, heads=1 + seed % 2,
+                                  head_dim=(4, 8)[seed % 2], act=act, lq_range=(1, 20),
+                                  lkv_range=(1, 20), causal=causal, bias_len=(0, 7)[seed % 2],
+                                  allow_empty=(seed % 4 == 3), window=window)
+        o, _ = oracle.fwd_inputs(x)
+        ref = dense_reference(x)
+        if o.size:
+            assert _rel(o, ref) <= 1e-12, (seed, _rel(o, ref))
+
+
+@pytest.mark.parametrize("act,causal,window", WINDOW_MODES)
+def test_window_backward_matches_torch_autograd(act, causal, window):
+    for seed in range(4):
+        x = workloads.random_case(800 + seed, batch=1 + seed % 3, heads=1 + seed % 2,
+                                  head_dim=4, act=act, lq_range=(1, 12), lkv_range=(1, 12),
+                                  causal=causal, bias_len=(0, 5)[seed % 2], window=window)
+        dq, dk, dv, db = oracle.bwd_inputs(x)
+        rq, rk, rv, rb = dense_torch_grads(x)
+        for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+            if ref.size and np.max(np.abs(ref)) > 0:
+                assert _rel(got, ref) <= 1e-10, (seed, _rel(got, ref))
+        if x.bias is not None:
+            assert _rel(db, rb) <= 1e-10
+
+
+def test_window_finite_differences():
+    """Central differences of L = sum(O * dO) under a window, GELU with bias."""
+    x = workloads.random_case(901, batch=2, heads=1, head_dim=3, act="gelu", lq_range=(2, 6),
+                              lkv_range=(2, 6), bias_len=5, window=2)
+    q, k, v = x.q.double().numpy(), x.k.double().numpy(), x.v.double().numpy()
+    do, bias = x.dout.double().numpy(), x.bias.double().numpy()
+
+    def loss(q_, k_, v_, b_):
+        o, _ = oracle.fwd(q_, k_, v_, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, "gelu",
+                          x.scale, bias=b_, window=x.window)
+        return float(np.sum(o * do))
+
+    dq, dk, dv, db = oracle.bwd(q, k, v, do, x.q_offsets, x.kv_offsets, x.heads, x.head_dim,
+                                "gelu", x.scale, bias=bias, window=x.window)
+    h = 1e-6
+    for arr, grad, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2), (bias, db, 3)):
+        num = np.zeros_like(arr)
+        flat, nflat = arr.reshape(-1), num.reshape(-1)
+        for e in range(flat.size):
+            keep = flat[e]
+            args = [q, k, v, bias]
+            flat[e] = keep + h
+            lp = loss(*args)
+            flat[e] = keep - h
+            lm = loss(*args)
+            flat[e] = keep
+            nflat[e] = (lp - lm) / (2 * h)
+        assert _rel(grad, num) <= 1e-6, (which, _rel(grad, num))
+
+
+@pytest.mark.parametrize("act", ["gelu", "silu", "softmax"])
+def test_window_of_one_closed_form(act):
+    """w = 1 leaves the diagonal only: O_i = act(s q_i.k_i + B[h][R]) v_i for
+    GELU / SiLU, and O_i = v_i with LSE_i = x_ii for softmax (Lq = Lkv)."""
+    lens = np.array([5, 1, 9])
+    x = workloads.make_inputs(lens, lens, 2, 8, act, bias_len=7, seed=31, window=1)
+    o, lse = oracle.fwd_inputs(x)
+    q, k, v = x.q.double().numpy(), x.k.double().numpy(), x.v.double().numpy()
+    bias = x.bias.double().numpy()
+    off = x.q_offsets.numpy()
+    for b in range(len(lens)):
+        for i in range(lens[b]):
+            r = off[b] + i
+            for h in range(2):
+                xi = x.scale * float(q[r, h] @ k[r, h]) + bias[h, 3]
+                if act == "softmax":
+                    assert np.allclose(o[r, h], v[r, h], rtol=0, atol=1e-12)
+                    assert abs(lse[h, r] - xi) <= 1e-12
+                else:
+                    a = xi * 0.5 * (1 + math.erf(xi / math.sqrt(2))) if act == "gelu" else xi * sps.expit(xi)
+                    assert np.allclose(o[r, h], a * v[r, h], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", ["gelu", "softmax"])
+def test_window_covering_every_pair_equals_no_window(act):
+    x = workloads.random_case(950, batch=4, heads=2, head_dim=8, act=act, lq_range=(1, 20),
+                              lkv_range=(1, 20), causal=(act == "softmax"), bias_len=7)
+    import dataclasses
+    y = dataclasses.replace(x, window=20)
+    o0, l0 = oracle.fwd_inputs(x)
+    o1, l1 = oracle.fwd_inputs(y)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    g0, g1 = oracle.bwd_inputs(x), oracle.bwd_inputs(y)
+    for a, b in zip(g0, g1):
+        assert np.array_equal(a, b)
+
+
+def test_window_rows_without_keys():
+    """Lq > Lkv + w - 1: rows i >= Lkv + w - 1 see no key: O_i = 0, LSE_i = -inf,
+    and those rows contribute nothing to any gradient."""
+    x = workloads.make_inputs([12], [3], 1, 4, "softmax", seed=5, window=2)
+    o, lse = oracle.fwd_inputs(x)
+    assert np.all(o[4:] == 0.0) and np.all(np.isneginf(lse[0, 4:]))
+    assert np.all(np.isfinite(lse[0, :4]))
+    dq, dk, dv, _ = oracle.bwd_inputs(x)
+    assert np.all(dq[4:] == 0.0)
+    y = workloads.make_inputs([4], [3], 1, 4, "softmax", seed=5, window=2)
+    y = type(y)(**{**y.__dict__, "q": x.q[:4], "dout": x.dout[:4], "k": x.k, "v": x.v})
+    _, dk4, dv4, _ = oracle.bwd_inputs(y)
+    assert np.allclose(dk, dk4, rtol=0, atol=1e-14) and np.allclose(dv, dv4, rtol=0, atol=1e-14)

@@ -12,6 +12,9 @@ watch": self-attention, PMA and cross-attention share one GDPA kernel;
 "Meta redesigns AI training infrastructure ...", section "Eliminating Compute
 Waste in Asymmetric Workloads": a production jagged sparsity of 0.5).  No
 dataset is named there, so these distributions stand in for production traffic.
+A sixth workload runs the long-tail batch under a sliding window of 1024
+(the same page, section "Custom Kernels and 5D Parallelism ...": sliding
+window attention for long sequences).
 
 Draw order for one workload, from ``numpy.random.default_rng(seed)``:
 query lengths, key/value lengths, Q, K, V (float32 standard normal), the bias
@@ -46,6 +49,7 @@ class Workload:
     lq: tuple              # ("uniform", lo, hi) inclusive, ("fixed", n), ("same",), ("lognormal", mu, sigma, lo, hi)
     lkv: tuple
     shared_q: int = 0      # >0: that many seed queries per head, shared by every segment (PMA)
+    window: int = 0        # >0: sliding window, pairs with |i - j| < window
 
 
 WORKLOADS = {
@@ -59,6 +63,9 @@ WORKLOADS = {
                 ("fixed", 16), ("uniform", 1, 4096), shared_q=16),
     5: Workload("long-tail jagged GDPA", 64, 8, 128, "gelu", False, 257, 4,
                 ("lognormal", math.log(1500.0), 1.0, 100, 16384), ("same",)),
+    # the long-tail batch (same seed, same draws) under a sliding window
+    6: Workload("long-tail jagged GDPA, sliding window 1024", 64, 8, 128, "gelu", False, 257, 4,
+                ("lognormal", math.log(1500.0), 1.0, 100, 16384), ("same",), window=1024),
 }
 
 
@@ -114,6 +121,7 @@ class Inputs:
     causal: bool
     scale: float               # float32 value 1/sqrt(d)
     q_seed: Optional[torch.Tensor] = None  # PMA: the shared bf16 [n_seed, H, d] queries
+    window: int = 0            # >0: only pairs with |i - j| < window (segment-local)
 
     @property
     def batch(self) -> int:
@@ -134,7 +142,7 @@ class Inputs:
 
 def make_inputs(lq, lkv, heads: int, head_dim: int, act: str, causal: bool = False,
                 bias_len: int = 0, seed: int = 0, rng: Optional[np.random.Generator] = None,
-                shared_q: int = 0) -> Inputs:
+                shared_q: int = 0, window: int = 0) -> Inputs:
     """Draw Q, K, V, bias and dO for given segment lengths (draw order in the module doc)."""
     if act not in ACTS:
         raise ValueError(f"act must be one of {ACTS}")
@@ -161,7 +169,8 @@ def make_inputs(lq, lkv, heads: int, head_dim: int, act: str, causal: bool = Fal
     scale = float(np.float32(1.0) / np.sqrt(np.float32(d)))
     return Inputs(q=q, k=k, v=v, dout=dout, q_offsets=offsets_from_lengths(lq),
                   kv_offsets=offsets_from_lengths(lkv), bias=bias, lq=lq, lkv=lkv,
-                  heads=h, head_dim=d, act=act, causal=causal, scale=scale, q_seed=q_seed)
+                  heads=h, head_dim=d, act=act, causal=causal, scale=scale, q_seed=q_seed,
+                  window=int(window))
 
 
 def select_segments(x: Inputs, segs) -> Inputs:
@@ -182,21 +191,21 @@ def select_segments(x: Inputs, segs) -> Inputs:
 
 
 def workload_inputs(index: int) -> Inputs:
-    """The full-size inputs of workload ``index`` (1..5)."""
+    """The full-size inputs of workload ``index`` (1..6)."""
     w = WORKLOADS[index]
     rng = np.random.default_rng(w.seed)
     lq, lkv = lengths_for(w, rng)
     return make_inputs(lq, lkv, w.heads, w.head_dim, w.act, w.causal, w.bias_len,
-                       rng=rng, shared_q=w.shared_q)
+                       rng=rng, shared_q=w.shared_q, window=w.window)
 
 
 def random_case(seed: int, batch: int, heads: int, head_dim: int, act: str,
                 lq_range=(1, 20), lkv_range=(1, 20), causal: bool = False,
-                bias_len: int = 0, allow_empty: bool = False) -> Inputs:
+                bias_len: int = 0, allow_empty: bool = False, window: int = 0) -> Inputs:
     """A small random jagged case; with ``allow_empty`` lengths may be 0."""
     rng = np.random.default_rng(seed)
     lo_q = 0 if allow_empty else lq_range[0]
     lo_k = 0 if allow_empty else lkv_range[0]
     lq = rng.integers(lo_q, lq_range[1] + 1, size=batch)
     lkv = rng.integers(lo_k, lkv_range[1] + 1, size=batch)
-    return make_inputs(lq, lkv, heads, head_dim, act, causal, bias_len, rng=rng)
+    return make_inputs(lq, lkv, heads, head_dim, act, causal, bias_len, rng=rng, window=window)
