@@ -41,19 +41,35 @@ WORKLOAD = 5
 METRIC = "jagged GDPA fwd/bwd TFLOPS over valid pairs; % of GB300 BF16 tensor peak"
 
 
-def valid_pairs(lq, lkv, causal: bool) -> int:
-    """Number of (i, j) pairs with j < Lkv (and j <= i when causal), per head."""
+def segment_pairs(lq, lkv, causal: bool, window: int = 0) -> np.ndarray:
+    """Valid (i, j) pairs of each segment, per head: j < Lkv, j <= i when
+    causal, |i - j| < window when window > 0."""
     lq = np.asarray(lq, dtype=np.int64)
     lkv = np.asarray(lkv, dtype=np.int64)
-    if not causal:
-        return int(np.sum(lq * lkv))
-    m = np.minimum(lq, lkv)
-    # rows i < m see i+1 keys; rows i >= m see all Lkv keys
-    return int(np.sum(m * (m + 1) // 2 + (lq - m) * lkv))
+    if window <= 0:
+        if not causal:
+            return lq * lkv
+        m = np.minimum(lq, lkv)
+        # rows i < m see i+1 keys; rows i >= m see all Lkv keys
+        return m * (m + 1) // 2 + (lq - m) * lkv
+    out = np.zeros(len(lq), dtype=np.int64)
+    for b, (a, n) in enumerate(zip(lq, lkv)):
+        i = np.arange(a, dtype=np.int64)
+        hi = np.minimum(n - 1, i + window - 1)
+        if causal:
+            hi = np.minimum(hi, i)
+        lo = np.maximum(0, i - window + 1)
+        out[b] = int(np.maximum(0, hi - lo + 1).sum())
+    return out
+
+
+def valid_pairs(lq, lkv, causal: bool, window: int = 0) -> int:
+    """Number of valid (i, j) pairs over all segments, per head."""
+    return int(segment_pairs(lq, lkv, causal, window).sum())
 
 
 def flops(x) -> tuple[float, float]:
-    p = valid_pairs(x.lq, x.lkv, x.causal) * x.heads
+    p = valid_pairs(x.lq, x.lkv, x.causal, x.window) * x.heads
     return 4.0 * p * x.head_dim, 10.0 * p * x.head_dim
 
 
@@ -78,6 +94,8 @@ WORKLOAD_TEXT = {
     4: "PMA-style pooling fwd+bwd: B=512, H=8, d=64, Lq=16 shared seed queries, Lkv~U[1,4096], SiLU, seed 3",
     5: "long-tail jagged GDPA fwd+bwd: B=64, H=8, d=128, L~round(LogNormal(ln 1500, 1)) clamped [100, 16384], "
        "GELU, rel-pos bias 257, seed 4",
+    6: "long-tail jagged GDPA fwd+bwd under a sliding window |i-j| < 1024: B=64, H=8, d=128, "
+       "L~round(LogNormal(ln 1500, 1)) clamped [100, 16384], GELU, rel-pos bias 257, seed 4",
 }
 
 
@@ -209,7 +227,7 @@ def oracle_sample(x, budget_s: float, seed: int = 0):
     rng = np.random.default_rng(seed)
     order = rng.permutation(x.batch)
     d = x.head_dim
-    pairs = x.lq.astype(np.int64) * x.lkv.astype(np.int64)
+    pairs = segment_pairs(x.lq, x.lkv, x.causal, x.window)
     threads = oracle.max_threads()
 
     def run(segs):
@@ -269,17 +287,17 @@ def run_native(args, world, rank, local):
     ws_b = torch.empty(jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, True),
                        dtype=torch.uint8, device=dev)
     # stored-dS backward: scratch sized from the (host) segment lengths
-    ds_scratch = torch.empty(max(1, jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, heads)),
+    ds_scratch = torch.empty(max(1, jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, heads, x.window)),
                              dtype=torch.uint8, device=dev)
 
     def fwd():
         jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
-                     causal=x.causal, out=out, lse=lse, workspace=ws_f)
+                     causal=x.causal, out=out, lse=lse, workspace=ws_f, window=x.window)
 
     def bwd(pass_events=None):
         jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
                      bias_table=d.bias, causal=x.causal, dq=dq, dk=dk, dv=dv, dbias=dbias, workspace=ws_b,
-                     ds_scratch=ds_scratch, pass_events=pass_events)
+                     ds_scratch=ds_scratch, pass_events=pass_events, window=x.window)
 
     # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, dQ, [dbias reduce])
     launches_per_step = 2 + 3 + int(softmax) + int(bias_len > 0)
@@ -336,10 +354,10 @@ def run_native(args, world, rank, local):
             dev_in[k].copy_(v, non_blocking=True)
         o, l2 = jg.jgdpa_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["q_offsets"], dev_in["kv_offsets"],
                              x.act, x.scale, bias_table=dev_in.get("bias"), causal=x.causal, out=out, lse=lse,
-                             workspace=ws_f)
+                             workspace=ws_f, window=x.window)
         jg.jgdpa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, l2, dev_in["dout"], dev_in["q_offsets"],
                      dev_in["kv_offsets"], x.act, x.scale, bias_table=dev_in.get("bias"), causal=x.causal, dq=dq,
-                     dk=dk, dv=dv, dbias=dbias, workspace=ws_b, ds_scratch=ds_scratch)
+                     dk=dk, dv=dv, dbias=dbias, workspace=ws_b, ds_scratch=ds_scratch, window=x.window)
         for k, t in results:
             host_out[k].copy_(t, non_blocking=True)
 
@@ -408,7 +426,7 @@ def run_native(args, world, rank, local):
             "batch_segments": x.batch,
             "total_q_tokens": int(total_q),
             "total_kv_tokens": int(total_kv),
-            "valid_pairs_x_heads": int(valid_pairs(x.lq, x.lkv, x.causal) * heads),
+            "valid_pairs_x_heads": int(valid_pairs(x.lq, x.lkv, x.causal, x.window) * heads),
             "fwd_tflop_per_step": f_fwd / 1e12,
             "bwd_tflop_per_step": f_bwd / 1e12,
             "fwd_algorithmic_gb_per_step": b_fwd / 1e9,

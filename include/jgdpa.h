@@ -123,6 +123,28 @@ JGDPA_API jgdpa_status jgdpa_fwd(const void* q, const void* k, const void* v,
                        void* workspace, size_t workspace_bytes, jgdpa_stream_t stream);
 
 /*
+ * Forward pass with a sliding window: the same computation, arguments and
+ * errors as jgdpa_fwd, plus
+ *   window   0 (no window, exactly jgdpa_fwd) or w >= 1: only pairs with
+ *            |i - j| < w (segment-local) are attended, on top of the
+ *            length and causal conditions; negative -> INVALID_ARGUMENT.
+ * Sliding window attention is named for long sequences in "Meta redesigns AI
+ * training infrastructure ..." (aiuniverse.news), section "Custom Kernels
+ * and 5D Parallelism ...", without a definition; this symmetric band, with
+ * the same segment-local indices as the bias and causal rules, is the reading
+ * taken.  Key/value tiles wholly outside the band are neither loaded nor
+ * computed, and the scheduler costs units by the tiles they visit.  A query
+ * row that meets no key gets O = 0 (and LSE = -inf in SOFTMAX mode).
+ */
+JGDPA_API jgdpa_status jgdpa_fwd_ex(const void* q, const void* k, const void* v,
+                       const int32_t* q_offsets, const int32_t* kv_offsets,
+                       int32_t batch, int64_t total_q, int64_t total_kv,
+                       int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
+                       const float* bias_table, int32_t bias_len, int32_t causal, int32_t window,
+                       void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, jgdpa_stream_t stream);
+
+/*
  * Backward pass: gradients of L = sum(O * dout) with respect to q, k, v and
  * the bias table.
  *   out, lse   the forward's O and LSE; read in SOFTMAX mode only (may be NULL
@@ -148,16 +170,22 @@ JGDPA_API jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v,
 
 /*
  * Bytes of stored-dS scratch that jgdpa_bwd_ex needs for these segment
- * lengths: heads * sum_b ceil(Lq_b/128) * ceil(Lkv_b/128) tiles of 32 KB.
- * q_offsets_host / kv_offsets_host are HOST copies of the offsets
- * ([batch + 1] each).  Returns 0 for invalid arguments (and for batch 0).
+ * lengths and window: heads * sum_b nk_b * span_b tiles of 32 KB, with
+ * nq_b = ceil(Lq_b/128), nk_b = ceil(Lkv_b/128), and span_b = nq_b, or under
+ * a window w > 0 the 2e + 1 query tiles one key tile can meet
+ * (e = ceil((w - 1)/128)) when that is fewer.  q_offsets_host /
+ * kv_offsets_host are HOST copies of the offsets ([batch + 1] each); window
+ * as in jgdpa_bwd_ex.  Returns 0 for invalid arguments (and for batch 0).
  */
 JGDPA_API size_t jgdpa_ds_scratch_bytes(const int32_t* q_offsets_host, const int32_t* kv_offsets_host,
-                                        int32_t batch, int32_t heads);
+                                        int32_t batch, int32_t heads, int32_t window);
 
 /*
  * Backward pass, extended.  The same computation, arguments and errors as
  * jgdpa_bwd, plus:
+ *   window
+ *       0 (no window) or w >= 1: the sliding window of jgdpa_fwd_ex; pass
+ *       the forward's window (and its out / lse in SOFTMAX mode).
  *   ds_scratch, ds_scratch_bytes
  *       optional caller-owned device scratch (256-byte aligned) for the
  *       stored-dS backward; NULL selects the recompute backward of
@@ -181,7 +209,7 @@ JGDPA_API jgdpa_status jgdpa_bwd_ex(const void* q, const void* k, const void* v,
                        const int32_t* q_offsets, const int32_t* kv_offsets,
                        int32_t batch, int64_t total_q, int64_t total_kv,
                        int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
-                       const float* bias_table, int32_t bias_len, int32_t causal,
+                       const float* bias_table, int32_t bias_len, int32_t causal, int32_t window,
                        void* dq, void* dk, void* dv, float* dbias,
                        void* workspace, size_t workspace_bytes,
                        void* ds_scratch, size_t ds_scratch_bytes, jgdpa_stream_t stream,

@@ -23,7 +23,8 @@ STATUS = {
     3: "JGDPA_ERR_MISALIGNED", 4: "JGDPA_ERR_WORKSPACE_TOO_SMALL", 5: "JGDPA_ERR_CUDA",
     6: "JGDPA_ERR_BAD_OFFSETS", 7: "JGDPA_ERR_DEVICE_TIMEOUT",
 }
-EXPORTS = ("jgdpa_workspace_bytes", "jgdpa_fwd", "jgdpa_bwd", "jgdpa_bwd_ex", "jgdpa_ds_scratch_bytes",
+EXPORTS = ("jgdpa_workspace_bytes", "jgdpa_fwd", "jgdpa_fwd_ex", "jgdpa_bwd", "jgdpa_bwd_ex",
+           "jgdpa_ds_scratch_bytes",
            "jgdpa_read_device_status", "jgdpa_status_string", "jgdpa_eval_activation", "jgdpa_fwd_noalloc")
 
 
@@ -50,12 +51,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.jgdpa_fwd.argtypes = [P, P, P, P, P, i32, i64, i64, i32, i32, ctypes.c_int, f32, P, i32, i32,
                               P, P, P, sz, P]
     lib.jgdpa_fwd.restype = ctypes.c_int
+    lib.jgdpa_fwd_ex.argtypes = lib.jgdpa_fwd.argtypes[:15] + [i32] + lib.jgdpa_fwd.argtypes[15:]
+    lib.jgdpa_fwd_ex.restype = ctypes.c_int
     lib.jgdpa_bwd.argtypes = [P, P, P, P, P, P, P, P, i32, i64, i64, i32, i32, ctypes.c_int, f32, P, i32,
                               i32, P, P, P, P, P, sz, P]
     lib.jgdpa_bwd.restype = ctypes.c_int
-    lib.jgdpa_bwd_ex.argtypes = lib.jgdpa_bwd.argtypes[:-1] + [P, sz, P, P]
+    lib.jgdpa_bwd_ex.argtypes = (lib.jgdpa_bwd.argtypes[:18] + [i32] + lib.jgdpa_bwd.argtypes[18:-1]
+                                 + [P, sz, P, P])
     lib.jgdpa_bwd_ex.restype = ctypes.c_int
-    lib.jgdpa_ds_scratch_bytes.argtypes = [P, P, i32, i32]
+    lib.jgdpa_ds_scratch_bytes.argtypes = [P, P, i32, i32, i32]
     lib.jgdpa_ds_scratch_bytes.restype = sz
     lib.jgdpa_read_device_status.argtypes = [P, P]
     lib.jgdpa_read_device_status.restype = ctypes.c_int
@@ -111,8 +115,9 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.
 
 
 def jgdpa_fwd(q, k, v, q_offsets, kv_offsets, act, scale: float, bias_table=None, causal: bool = False,
-              out=None, lse=None, workspace=None, stream=None):
-    """Forward pass; returns (out, lse) with lse None unless act == 'softmax'."""
+              out=None, lse=None, workspace=None, stream=None, window: int = 0):
+    """Forward pass; returns (out, lse) with lse None unless act == 'softmax'.
+    window > 0 takes the sliding-window entry point (jgdpa_fwd_ex)."""
     lib = load()
     total_q, heads, d = q.shape
     total_kv = k.shape[0]
@@ -125,30 +130,36 @@ def jgdpa_fwd(q, k, v, q_offsets, kv_offsets, act, scale: float, bias_table=None
         lse = torch.empty((heads, total_q), dtype=torch.float32, device=q.device)
     nbytes = jgdpa_workspace_bytes(batch, total_q, total_kv, heads, d, a, bias_len, False)
     ws = _workspace(nbytes, q.device, workspace)
-    rc = lib.jgdpa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(kv_offsets), batch, total_q,
-                       total_kv, heads, d, a, float(scale), _ptr(bias_table), bias_len, int(bool(causal)),
-                       _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
-    _check(rc, "jgdpa_fwd")
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(kv_offsets), batch, total_q, total_kv, heads, d,
+            a, float(scale), _ptr(bias_table), bias_len, int(bool(causal)))
+    tail = (_ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    if window:
+        rc = lib.jgdpa_fwd_ex(*head, int(window), *tail)
+        _check(rc, "jgdpa_fwd_ex")
+    else:
+        rc = lib.jgdpa_fwd(*head, *tail)
+        _check(rc, "jgdpa_fwd")
     return out, lse
 
 
-def jgdpa_ds_scratch_bytes(q_offsets, kv_offsets, heads: int) -> int:
+def jgdpa_ds_scratch_bytes(q_offsets, kv_offsets, heads: int, window: int = 0) -> int:
     """Stored-dS scratch bytes for these offsets (copied to the host here)."""
     lib = load()
     qo = q_offsets.detach().to("cpu", torch.int32).contiguous()
     ko = kv_offsets.detach().to("cpu", torch.int32).contiguous()
-    return int(lib.jgdpa_ds_scratch_bytes(qo.data_ptr(), ko.data_ptr(), qo.numel() - 1, int(heads)))
+    return int(lib.jgdpa_ds_scratch_bytes(qo.data_ptr(), ko.data_ptr(), qo.numel() - 1, int(heads), int(window)))
 
 
 def jgdpa_bwd(q, k, v, out, lse, dout, q_offsets, kv_offsets, act, scale: float, bias_table=None,
               causal: bool = False, dq=None, dk=None, dv=None, dbias=None, want_dbias: bool = True,
-              workspace=None, stream=None, ds_scratch=None, pass_events=None):
+              workspace=None, stream=None, ds_scratch=None, pass_events=None, window: int = 0):
     """Backward pass; returns (dq, dk, dv, dbias) with dbias None without a bias table.
 
     ds_scratch: optional uint8 device tensor of at least jgdpa_ds_scratch_bytes
     bytes -- selects the stored-dS backward (jgdpa_bwd_ex).  pass_events:
     optional three torch.cuda.Event (timing enabled, already recorded once),
-    recorded before the dK/dV pass, between the passes and after the dQ pass."""
+    recorded before the dK/dV pass, between the passes and after the dQ pass.
+    window: the forward's sliding window (jgdpa_bwd_ex); 0 for none."""
     lib = load()
     total_q, heads, d = q.shape
     total_kv = k.shape[0]
@@ -162,19 +173,19 @@ def jgdpa_bwd(q, k, v, out, lse, dout, q_offsets, kv_offsets, act, scale: float,
         dbias = torch.empty((heads, bias_len), dtype=torch.float32, device=q.device)
     nbytes = jgdpa_workspace_bytes(batch, total_q, total_kv, heads, d, a, bias_len, True)
     ws = _workspace(nbytes, q.device, workspace)
-    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(q_offsets),
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(q_offsets),
             _ptr(kv_offsets), batch, total_q, total_kv, heads, d, a, float(scale),
-            _ptr(bias_table), bias_len, int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
-            _ptr(dbias), _ptr(ws), ws.numel())
-    if ds_scratch is None and pass_events is None:
-        rc = lib.jgdpa_bwd(*args, _stream(stream))
+            _ptr(bias_table), bias_len, int(bool(causal)))
+    tail = (_ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(ws), ws.numel())
+    if ds_scratch is None and pass_events is None and not window:
+        rc = lib.jgdpa_bwd(*head, *tail, _stream(stream))
         _check(rc, "jgdpa_bwd")
     else:
         ev = None
         if pass_events is not None:
             ev = (ctypes.c_void_p * 3)(*[None if e is None else e.cuda_event for e in pass_events])
-        rc = lib.jgdpa_bwd_ex(*args, _ptr(ds_scratch), 0 if ds_scratch is None else ds_scratch.numel(),
-                              _stream(stream), ev)
+        rc = lib.jgdpa_bwd_ex(*head, int(window), *tail, _ptr(ds_scratch),
+                              0 if ds_scratch is None else ds_scratch.numel(), _stream(stream), ev)
         _check(rc, "jgdpa_bwd_ex")
     return dq, dk, dv, dbias
 

@@ -218,8 +218,8 @@ __global__ void eval_act_kernel(int act, int path, const float* x, int64_t n, fl
 }
 
 jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batch, int32_t heads,
-                          int64_t total_q, int64_t total_kv, int32_t causal, uint8_t* ws, const Layout& L,
-                          bool bwd, cudaStream_t stream, int64_t ds_capacity = -1) {
+                          int64_t total_q, int64_t total_kv, int32_t causal, int32_t window, uint8_t* ws,
+                          const Layout& L, bool bwd, cudaStream_t stream, int64_t ds_capacity = -1) {
   jg::SchedParams sp{};
   if (ds_capacity >= 0) {
     sp.ds_base = reinterpret_cast<int64_t*>(ws + L.ds_base);
@@ -232,6 +232,7 @@ jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batc
   sp.total_q = total_q;
   sp.total_kv = total_kv;
   sp.causal = causal;
+  sp.window = window;
   int* hdr = reinterpret_cast<int*>(ws + L.header);
   sp.status = hdr;
   sp.item_base = reinterpret_cast<int32_t*>(ws + L.item_base);
@@ -264,15 +265,20 @@ size_t jgdpa_workspace_bytes(int32_t batch, int64_t total_q, int64_t total_kv, i
   return L.total;
 }
 
-jgdpa_status jgdpa_fwd(const void* q, const void* k, const void* v, const int32_t* q_offsets,
-                       const int32_t* kv_offsets, int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
-                       int32_t head_dim, jgdpa_act act, float scale, const float* bias_table, int32_t bias_len,
-                       int32_t causal, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                       jgdpa_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t* q_offsets,
+                      const int32_t* kv_offsets, int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
+                      int32_t head_dim, jgdpa_act act, float scale, const float* bias_table, int32_t bias_len,
+                      int32_t causal, int32_t window, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, jgdpa_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   jgdpa_status st = check_common(batch, total_q, total_kv, heads, head_dim, act, scale, bias_table, bias_len,
                                  causal, q_offsets, kv_offsets);
   if (st != JGDPA_OK) return st;
+  if (window < 0) return JGDPA_ERR_INVALID_ARGUMENT;
   if ((act == JGDPA_ACT_SOFTMAX) != (lse != nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
   if (total_q > 0 && (q == nullptr || out == nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
   if (total_kv > 0 && (k == nullptr || v == nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
@@ -290,7 +296,7 @@ jgdpa_status jgdpa_fwd(const void* q, const void* k, const void* v, const int32_
     if (lse) JG_CUDA(fill_f32(lse, total_q * heads, -INFINITY, stream));
     return JGDPA_OK;
   }
-  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, ws, L, false, stream);
+  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, false, stream);
   if (st != JGDPA_OK) return st;
 
   jg::FwdParams p{};
@@ -310,10 +316,33 @@ jgdpa_status jgdpa_fwd(const void* q, const void* k, const void* v, const int32_
   p.heads = heads;
   p.bias_len = bias_len;
   p.causal = causal;
+  p.window = window;
   p.scale = act == JGDPA_ACT_SOFTMAX ? scale * jg::kLog2e : scale;
   const int grid = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max0)));
   JG_CUDA(jg::launch_fwd(p, head_dim, act, grid, stream));
   return JGDPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+jgdpa_status jgdpa_fwd(const void* q, const void* k, const void* v, const int32_t* q_offsets,
+                       const int32_t* kv_offsets, int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
+                       int32_t head_dim, jgdpa_act act, float scale, const float* bias_table, int32_t bias_len,
+                       int32_t causal, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       jgdpa_stream_t stream) {
+  return fwd_impl(q, k, v, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act, scale,
+                  bias_table, bias_len, causal, 0, out, lse, workspace, workspace_bytes, stream);
+}
+
+jgdpa_status jgdpa_fwd_ex(const void* q, const void* k, const void* v, const int32_t* q_offsets,
+                          const int32_t* kv_offsets, int32_t batch, int64_t total_q, int64_t total_kv,
+                          int32_t heads, int32_t head_dim, jgdpa_act act, float scale, const float* bias_table,
+                          int32_t bias_len, int32_t causal, int32_t window, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, jgdpa_stream_t stream) {
+  return fwd_impl(q, k, v, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act, scale,
+                  bias_table, bias_len, causal, window, out, lse, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
@@ -325,9 +354,9 @@ namespace {
 jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
                       const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
                       int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
-                      float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq, void* dk,
-                      void* dv, float* dbias, void* workspace, size_t workspace_bytes, jgdpa_stream_t stream_,
-                      void* ds_scratch, size_t ds_scratch_bytes, void* const* ev) {
+                      float scale, const float* bias_table, int32_t bias_len, int32_t causal, int32_t window,
+                      void* dq, void* dk, void* dv, float* dbias, void* workspace, size_t workspace_bytes,
+                      jgdpa_stream_t stream_, void* ds_scratch, size_t ds_scratch_bytes, void* const* ev) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   auto record = [&](int i) -> cudaError_t {
     return (ev != nullptr && ev[i] != nullptr) ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), stream)
@@ -336,6 +365,7 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   jgdpa_status st = check_common(batch, total_q, total_kv, heads, head_dim, act, scale, bias_table, bias_len,
                                  causal, q_offsets, kv_offsets);
   if (st != JGDPA_OK) return st;
+  if (window < 0) return JGDPA_ERR_INVALID_ARGUMENT;
   if (dbias != nullptr && bias_len == 0) return JGDPA_ERR_INVALID_ARGUMENT;
   if (total_q > 0 && (q == nullptr || dout == nullptr || dq == nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
   if (total_kv > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr))
@@ -367,7 +397,7 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     return JGDPA_OK;
   }
   const bool stored_ds = ds_scratch != nullptr && ds_tiles > 0;
-  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, ws, L, true, stream,
+  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, true, stream,
                  ds_scratch ? std::max<int64_t>(ds_tiles, 0) : -1);
   if (st != JGDPA_OK) return st;
 
@@ -393,6 +423,7 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   p.heads = heads;
   p.bias_len = bias_len;
   p.causal = causal;
+  p.window = window;
   p.scale = scale;
   if (act == JGDPA_ACT_SOFTMAX)
     JG_CUDA(jg::launch_softmax_delta(out, dout, const_cast<float*>(p.delta), total_q, heads, head_dim, hdr,
@@ -427,31 +458,34 @@ jgdpa_status jgdpa_bwd(const void* q, const void* k, const void* v, const void* 
                        float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq, void* dk,
                        void* dv, float* dbias, void* workspace, size_t workspace_bytes, jgdpa_stream_t stream) {
   return bwd_impl(q, k, v, out, lse, dout, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act,
-                  scale, bias_table, bias_len, causal, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
+                  scale, bias_table, bias_len, causal, 0, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
                   nullptr, 0, nullptr);
 }
 
 jgdpa_status jgdpa_bwd_ex(const void* q, const void* k, const void* v, const void* out, const float* lse,
                           const void* dout, const int32_t* q_offsets, const int32_t* kv_offsets, int32_t batch,
                           int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
-                          float scale, const float* bias_table, int32_t bias_len, int32_t causal, void* dq,
-                          void* dk, void* dv, float* dbias, void* workspace, size_t workspace_bytes,
-                          void* ds_scratch, size_t ds_scratch_bytes, jgdpa_stream_t stream,
+                          float scale, const float* bias_table, int32_t bias_len, int32_t causal,
+                          int32_t window, void* dq, void* dk, void* dv, float* dbias, void* workspace,
+                          size_t workspace_bytes, void* ds_scratch, size_t ds_scratch_bytes, jgdpa_stream_t stream,
                           void* const* pass_events) {
   return bwd_impl(q, k, v, out, lse, dout, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act,
-                  scale, bias_table, bias_len, causal, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
-                  ds_scratch, ds_scratch_bytes, pass_events);
+                  scale, bias_table, bias_len, causal, window, dq, dk, dv, dbias, workspace, workspace_bytes,
+                  stream, ds_scratch, ds_scratch_bytes, pass_events);
 }
 
 size_t jgdpa_ds_scratch_bytes(const int32_t* q_offsets_host, const int32_t* kv_offsets_host, int32_t batch,
-                              int32_t heads) {
-  if (batch < 0 || heads < 1 || (batch > 0 && (q_offsets_host == nullptr || kv_offsets_host == nullptr))) return 0;
+                              int32_t heads, int32_t window) {
+  if (batch < 0 || heads < 1 || window < 0 ||
+      (batch > 0 && (q_offsets_host == nullptr || kv_offsets_host == nullptr)))
+    return 0;
   uint64_t tiles = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const int64_t lq = static_cast<int64_t>(q_offsets_host[b + 1]) - q_offsets_host[b];
     const int64_t lkv = static_cast<int64_t>(kv_offsets_host[b + 1]) - kv_offsets_host[b];
     if (lq < 0 || lkv < 0) return 0;
-    tiles += static_cast<uint64_t>((lq + jg::kTile - 1) / jg::kTile) * ((lkv + jg::kTile - 1) / jg::kTile);
+    const int64_t nq = (lq + jg::kTile - 1) / jg::kTile, nk = (lkv + jg::kTile - 1) / jg::kTile;
+    tiles += static_cast<uint64_t>(nk) * static_cast<uint64_t>(jg::ds_span(nq, window));
   }
   return static_cast<size_t>(tiles * heads * jg::kDsTileBytes);
 }
@@ -535,6 +569,6 @@ extern "C" jgdpa_status jgdpa_fwd_noalloc(const void* q, const void* k, const vo
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != JGDPA_OK) return st;
-  return jgdpa_fwd(q, k, v, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act, scale,
-                   bias_table, bias_len, causal, out, lse, scratch, JGDPA_NOALLOC_SCRATCH_BYTES, stream);
+  return fwd_impl(q, k, v, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act, scale,
+                  bias_table, bias_len, causal, 0, out, lse, scratch, JGDPA_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -36,6 +36,7 @@ struct SchedParams {
   int64_t total_q;
   int64_t total_kv;
   int32_t causal;
+  int32_t window;       // > 0: sliding window |i - j| < window
   int* status;
   int32_t* item_base;   // scratch [batch + 1] per list
   SchedList list[2];
@@ -60,19 +61,35 @@ __device__ __forceinline__ Seg load_seg(const int32_t* q_off, const int32_t* kv_
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Number of key/value tiles that query tile t (128 rows) must visit.  With
-// top-left causal masking, query row i sees keys j <= i, so tile t needs kv
-// tiles 0..t.
-__device__ __forceinline__ int kv_tiles_for_q_tile(int t, int lkv, int causal) {
-  const int n = ceil_div(lkv, kTile);
-  return causal ? min(t + 1, n) : n;
+// The partner tiles [first, first + count) that one 128-row tile meets.
+// Query row i and key row j (segment-local) form a pair when j < Lkv and,
+// with top-left causal masking, j <= i, and with a sliding window w > 0,
+// |i - j| < w.
+struct TileSpan {
+  int first, count;
+};
+
+// Rows [128 t, 128 t + 127] reach partner rows [128 t - (w - 1), 128 t + 127 + (w - 1)].
+__device__ __forceinline__ void window_tiles(int t, int window, int& lo, int& hi) {
+  if (window <= 0) return;
+  const int64_t a = static_cast<int64_t>(t) * kTile - (window - 1);
+  const int64_t b = static_cast<int64_t>(t) * kTile + (kTile - 1) + (window - 1);
+  lo = max(lo, a <= 0 ? 0 : static_cast<int>(a / kTile));
+  hi = static_cast<int>(min(static_cast<int64_t>(hi), b / kTile + 1));
 }
-// Number of query tiles that key/value tile kt meets (same masking rule).
-__device__ __forceinline__ int q_tiles_for_kv_tile(int kt, int lq, int causal) {
-  const int n = ceil_div(lq, kTile);
-  return causal ? max(0, n - kt) : n;
+// Key/value tiles that query tile t visits (causal: tiles 0..t at most).
+__device__ __forceinline__ TileSpan kv_span_for_q_tile(int t, int lkv, int causal, int window) {
+  int lo = 0, hi = ceil_div(lkv, kTile);
+  if (causal) hi = min(hi, t + 1);
+  window_tiles(t, window, lo, hi);
+  return {lo, max(0, hi - lo)};
 }
-__device__ __forceinline__ int first_q_tile_for_kv_tile(int kt, int causal) { return causal ? kt : 0; }
+// Query tiles that key/value tile kt meets (causal: tiles kt.. at least).
+__device__ __forceinline__ TileSpan q_span_for_kv_tile(int kt, int lq, int causal, int window) {
+  int lo = causal ? kt : 0, hi = ceil_div(lq, kTile);
+  window_tiles(kt, window, lo, hi);
+  return {lo, max(0, hi - lo)};
+}
 
 // Index of the i-th unit processed by CTA c of G (serpentine over rounds, so
 // that each round's longest units are spread evenly).
@@ -96,6 +113,7 @@ struct FwdParams {
   int32_t heads;
   int32_t bias_len;
   int32_t causal;
+  int32_t window;         // > 0: sliding window |i - j| < window
   float scale;            // s (GELU/SiLU) or s * log2(e) (softmax)
 };
 
@@ -120,20 +138,42 @@ struct BwdParams {
   int32_t heads;
   int32_t bias_len;
   int32_t causal;
+  int32_t window;          // > 0: sliding window |i - j| < window
   float scale;             // s
   // Stored dS (optional): the dK/dV pass writes every bf16 dS^T tile to a
   // scratch array of [128 keys][128 queries] tiles; tile of (segment b, head
-  // h, key tile kt, query tile qt) = ds_base[b] + (h nk_b + kt) nq_b + qt.
+  // h, key tile kt, query tile qt) = ds_base[b] + (h nk_b + kt) span_b +
+  // slot (see ds_span / ds_slot).
   CUtensorMap tm_ds;       // 2-D over the scratch: 128 columns x (tiles * 128) rows
   const int64_t* ds_base;  // nullptr: no stored dS
 };
 
 constexpr int kDsTileBytes = kTile * kTile * 2;
 
+// Stored-dS slots per key tile of a segment with nq query tiles: nq, or
+// under a window short enough to pay, the 2e + 1 query tiles kt - e .. kt + e
+// that key tile kt can meet (e = ceil((w - 1) / 128)); the slot of query
+// tile qt is then qt - kt + e.
+__host__ __device__ __forceinline__ int64_t ds_band_reach(int window) {
+  return (static_cast<int64_t>(window) + kTile - 2) / kTile;
+}
+__host__ __device__ __forceinline__ int64_t ds_span(int64_t nq, int window) {
+  if (window <= 0) return nq;
+  const int64_t band = 2 * ds_band_reach(window) + 1;
+  return band < nq ? band : nq;
+}
+__device__ __forceinline__ int64_t ds_slot(int64_t nq, int window, int kt, int qt) {
+  if (window <= 0 || ds_span(nq, window) == nq) return qt;
+  return qt - kt + ds_band_reach(window);
+}
+
 // First row of a dS tile in the scratch's 2-D view.
-__device__ __forceinline__ int ds_row(const int64_t* ds_base, const Seg& s, int b, int h, int kt, int qt) {
+__device__ __forceinline__ int ds_row(const int64_t* ds_base, const Seg& s, int b, int h, int kt, int qt,
+                                      int window) {
   const int64_t nq = ceil_div(s.lq, kTile), nk = ceil_div(s.lkv, kTile);
-  return static_cast<int>((__ldg(ds_base + b) + (static_cast<int64_t>(h) * nk + kt) * nq + qt) * kTile);
+  const int64_t span = ds_span(nq, window);
+  return static_cast<int>(
+      (__ldg(ds_base + b) + (static_cast<int64_t>(h) * nk + kt) * span + ds_slot(nq, window, kt, qt)) * kTile);
 }
 
 }  // namespace jg

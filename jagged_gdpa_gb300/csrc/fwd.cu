@@ -77,34 +77,53 @@ struct FwdBars {
 };
 
 // Per-unit geometry shared by every role.
+// The unit streams key/value tiles k0 .. k0 + nkv - 1 once; query slot s
+// uses stream positions [beg_s, beg_s + nkv_s) of it (the two query tiles'
+// spans overlap or touch, so their union has no gap).
 struct FwdUnit {
   int b, h, pair;
   Seg seg;
+  int k0;         // first key/value tile of the stream
+  int nkv;        // tiles streamed
+  int beg_s[2];   // each query slot's first stream position
   int nkv_s[2];   // key/value tiles for each query slot (0 = slot idle)
   int rows_s[2];  // valid query rows in each slot's tile (<= 0: no tile)
-  int nkv;        // max of nkv_s
 };
 
+// WIN: the kernel is compiled for a sliding window (p.window > 0); the plain
+// kernels fold the window away.
+template <bool WIN>
 __device__ __forceinline__ FwdUnit fwd_unit(const FwdParams& p, int idx) {
+  const int window = WIN ? p.window : 0;
   FwdUnit u;
   const Unit w = p.units[idx];
   u.b = w.x;
   u.h = w.y;
   u.pair = w.z;
   u.seg = load_seg(p.q_off, p.kv_off, u.b);
-  u.nkv = 0;
+  int lo = 0x7fffffff, hi = 0;
+  int first[2];
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const int t = 2 * u.pair + s;
     u.rows_s[s] = u.seg.lq - t * kTile;
-    u.nkv_s[s] = u.rows_s[s] > 0 ? kv_tiles_for_q_tile(t, u.seg.lkv, p.causal) : 0;
-    u.nkv = max(u.nkv, u.nkv_s[s]);
+    const TileSpan sp = u.rows_s[s] > 0 ? kv_span_for_q_tile(t, u.seg.lkv, p.causal, window) : TileSpan{0, 0};
+    u.nkv_s[s] = sp.count;
+    first[s] = sp.first;
+    if (sp.count > 0) {
+      lo = min(lo, sp.first);
+      hi = max(hi, sp.first + sp.count);
+    }
   }
+  u.k0 = hi > 0 ? lo : 0;
+  u.nkv = hi > 0 ? hi - lo : 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) u.beg_s[s] = first[s] - u.k0;
   return u;
 }
 
 // --------------------------------------------------------------- producer
-template <int D>
+template <int D, bool WIN>
 __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, int n_units, Fail fail) {
   using C = FwdCfg<D>;
   uint32_t q_it[2] = {0, 0};
@@ -114,7 +133,7 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
   for (int r = 0;; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
     if (idx >= n_units) break;
-    const FwdUnit u = fwd_unit(p, idx);
+    const FwdUnit u = fwd_unit<WIN>(p, idx);
     if (u.nkv == 0) continue;
     for (int s = 0; s < 2 && ok; ++s) {
       if (u.nkv_s[s] == 0) continue;
@@ -136,7 +155,7 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
       const int st = kv_it % C::kStages;
       const uint32_t empty_phase = ((kv_it / C::kStages) & 1) ^ 1;
       if (!(ok = mbar_wait_warp(&bars->k_empty[st], empty_phase, fail))) break;
-      const int row = u.seg.k0 + kt * kTile;
+      const int row = u.seg.k0 + (u.k0 + kt) * kTile;
       if (leader) {
         mbar_arrive_tx(&bars->k_full[st], C::kTileBytes);
         uint8_t* kd = smem + C::kKOff + st * C::kTileBytes;
@@ -195,7 +214,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
   }
 }
 
-template <int D>
+template <int D, bool WIN>
 __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem, int n_units, Fail fail) {
   using C = FwdCfg<D>;
   const uint32_t q_addr[2] = {smem_u32(smem + C::kQOff), smem_u32(smem + C::kQOff + C::kTileBytes)};
@@ -211,7 +230,7 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
   for (int r = 0; ok; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
     if (idx >= n_units) break;
-    const FwdUnit u = fwd_unit(p, idx);
+    const FwdUnit u = fwd_unit<WIN>(p, idx);
     if (u.nkv == 0) continue;
     for (int s = 0; s < 2 && ok; ++s) {
       if (u.nkv_s[s] == 0) continue;
@@ -219,18 +238,21 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
       ++q_it[s];
     }
     if (!ok) break;
-    // S(0) for both slots
+    // slot s takes stream positions [b_s, e_s)
+    const int b0 = u.beg_s[0], e0 = b0 + u.nkv_s[0];
+    const int b1 = u.beg_s[1], e1 = b1 + u.nkv_s[1];
+    // S of stream position 0 for the slots that start there
     {
       const int st = kv_it % C::kStages;
       if (!(ok = mbar_wait_warp(&bars->k_full[st], (kv_it / C::kStages) & 1, fail))) break;
       tc_fence_after();
       for (int s = 0; s < 2; ++s) {
-        if (u.nkv_s[s] == 0) continue;
+        if (u.nkv_s[s] == 0 || u.beg_s[s] != 0) continue;
         issue_qk<D>(t_s[s], q_addr[s], k_base + st * C::kTileBytes, leader);
         if (leader) mma_commit(&bars->s_full[s]);
         if (u.nkv_s[s] == 1) if (leader) mma_commit(&bars->q_empty[s]);
       }
-      if (leader) mma_commit(&bars->k_empty[st]);  // both S of K(0) issued
+      if (leader) mma_commit(&bars->k_empty[st]);  // every S of stream position 0 issued
     }
     for (int kt = 0; kt < u.nkv && ok; ++kt) {
       const uint32_t it = kv_it + kt;
@@ -244,43 +266,43 @@ __device__ void fwd_mma(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
       // hide behind.  S_s(kt+1) overwrites the columns that PV_s(kt) reads;
       // it is issued after it, and MMAs execute in issue order.
       // slot 0: O0 += P0 V, then S0 of the next tile
-      if (kt < u.nkv_s[0]) {
-        if (kt == 0) {
+      if (kt >= b0 && kt < e0) {
+        if (kt == b0) {
           if (!(ok = mbar_wait_warp(&bars->o_empty[0], (o_it[0] & 1) ^ 1, fail))) break;
           ++o_it[0];
         }
         if (!(ok = mbar_wait_warp(&bars->p_full[0], p_it[0] & 1, fail))) break;
         ++p_it[0];
         tc_fence_after();
-        issue_pv<D>(t_o[0], t_s[0], v_addr, kt > 0, leader);
-        if (kt == u.nkv_s[0] - 1) if (leader) mma_commit(&bars->o_full[0]);
+        issue_pv<D>(t_o[0], t_s[0], v_addr, kt > b0, leader);
+        if (kt == e0 - 1) if (leader) mma_commit(&bars->o_full[0]);
       }
       if (more) {
         if (!(ok = mbar_wait_warp(&bars->k_full[st1], ((it + 1) / C::kStages) & 1, fail))) break;
         tc_fence_after();
-        if (kt + 1 < u.nkv_s[0]) {
+        if (kt + 1 >= b0 && kt + 1 < e0) {
           issue_qk<D>(t_s[0], q_addr[0], k_base + st1 * C::kTileBytes, leader);
           if (leader) mma_commit(&bars->s_full[0]);
-          if (kt + 1 == u.nkv_s[0] - 1) if (leader) mma_commit(&bars->q_empty[0]);
+          if (kt + 1 == e0 - 1) if (leader) mma_commit(&bars->q_empty[0]);
         }
       }
       // slot 1: O1 += P1 V, release V, then S1 of the next tile, release K
-      if (kt < u.nkv_s[1]) {
-        if (kt == 0) {
+      if (kt >= b1 && kt < e1) {
+        if (kt == b1) {
           if (!(ok = mbar_wait_warp(&bars->o_empty[1], (o_it[1] & 1) ^ 1, fail))) break;
           ++o_it[1];
         }
         if (!(ok = mbar_wait_warp(&bars->p_full[1], p_it[1] & 1, fail))) break;
         ++p_it[1];
         tc_fence_after();
-        issue_pv<D>(t_o[1], t_s[1], v_addr, kt > 0, leader);
-        if (kt == u.nkv_s[1] - 1) if (leader) mma_commit(&bars->o_full[1]);
+        issue_pv<D>(t_o[1], t_s[1], v_addr, kt > b1, leader);
+        if (kt == e1 - 1) if (leader) mma_commit(&bars->o_full[1]);
       }
       if (leader) mma_commit(&bars->v_empty[st]);  // every P V of V(kt) issued
-      if (more && kt + 1 < u.nkv_s[1]) {
+      if (more && kt + 1 >= b1 && kt + 1 < e1) {
         issue_qk<D>(t_s[1], q_addr[1], k_base + st1 * C::kTileBytes, leader);
         if (leader) mma_commit(&bars->s_full[1]);
-        if (kt + 1 == u.nkv_s[1] - 1) if (leader) mma_commit(&bars->q_empty[1]);
+        if (kt + 1 == e1 - 1) if (leader) mma_commit(&bars->q_empty[1]);
       }
       if (more) if (leader) mma_commit(&bars->k_empty[st1]);  // every S of K(kt+1) issued
     }
@@ -332,7 +354,8 @@ __device__ __forceinline__ float2 band_bias2(const TileBias& tb, int c, float mu
 // S (fp32, TMEM) -> P = act(s S + bias) (bf16, over the same TMEM columns)
 // for one 128 x 128 tile, GELU / SiLU, two columns per packed instruction.
 // The last NALU of the four 32-column chunks take the ALU route.  MASKED:
-// columns >= nvalid (the subtraction-scheme count) get P = act(0) = 0.
+// columns outside [lo, nvalid) (nvalid: the subtraction-scheme count; lo > 0
+// only under a sliding window) get P = act(0) = 0.
 // The four 32-column chunks are software-pipelined: the TMEM load of chunk
 // q + 1 is in flight while chunk q is computed and its P stored (P of chunk q
 // lands in columns [16q, 16q + 16), all read already).
@@ -340,7 +363,8 @@ __device__ __forceinline__ float2 band_bias2(const TileBias& tb, int c, float mu
 // key row of the segment; the rest are not computed, and their P is zero (the
 // PV product reads every column).
 template <int ACT, int NALU, bool BAND, bool MASKED>
-__device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias& tb, int nvalid, int nchunks) {
+__device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias& tb, int lo, int nvalid,
+                                         int nchunks) {
   const float hb = 0.5f * tb.value;
   uint32_t buf0[32], buf1[32];
   tmem_ld32(t_s, buf0);
@@ -362,8 +386,8 @@ __device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias&
         const float2 bias = BAND ? band_bias2(tb, c, 0.5f) : f2(hb);
         float2 hx = __ffma2_rn(sv, f2(hs), bias);  // x / 2
         if (MASKED) {
-          if (c >= nvalid) hx.x = 0.f;
-          if (c + 1 >= nvalid) hx.y = 0.f;
+          if (c < lo || c >= nvalid) hx.x = 0.f;
+          if (c + 1 < lo || c + 1 >= nvalid) hx.y = 0.f;
         }
         float2 y;
         if (q >= 4 - NALU) y = act2_route<ACT, 1>(hx);
@@ -382,7 +406,7 @@ __device__ __forceinline__ void tile_act(uint32_t t_s, float hs, const TileBias&
 // P = 2^(x2 - m) over the S columns, running row sum.
 template <int D, bool BAND, bool MASKED>
 __device__ __forceinline__ void tile_softmax(uint32_t t_s, uint32_t t_o, float scale2, const TileBias& tb,
-                                             int nvalid, bool first, float& m_run, float& l_run) {
+                                             int lo, int nvalid, bool first, float& m_run, float& l_run) {
   uint32_t a[32], b[32], c3[32], d4[32];
   tmem_ld32(t_s, a);
   tmem_ld32(t_s + 32, b);
@@ -399,8 +423,8 @@ __device__ __forceinline__ void tile_softmax(uint32_t t_s, uint32_t t_o, float s
     const float2 bias = BAND ? band_bias2(tb, c, kLog2e) : f2(b2);
     float2 x = __ffma2_rn(make_float2(__uint_as_float(r0), __uint_as_float(r1)), f2(scale2), bias);
     if (MASKED) {
-      if (c >= nvalid) x.x = -INFINITY;
-      if (c + 1 >= nvalid) x.y = -INFINITY;
+      if (c < lo || c >= nvalid) x.x = -INFINITY;
+      if (c + 1 < lo || c + 1 >= nvalid) x.y = -INFINITY;
     }
     r0 = __float_as_uint(x.x);
     r1 = __float_as_uint(x.y);
@@ -412,7 +436,9 @@ __device__ __forceinline__ void tile_softmax(uint32_t t_s, uint32_t t_o, float s
   l_run *= factor;
   m_run = m_new;
   float2 lsum = f2(0.f);
-  const float2 neg_m = f2(-m_run);
+  // a row with no key so far (a sliding window can leave whole tiles empty
+  // for it) keeps m = -inf; its x are all -inf and P must come out 0
+  const float2 neg_m = f2(m_run == -INFINITY ? 0.f : -m_run);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t(&src)[32] = q == 0 ? a : q == 1 ? b : q == 2 ? c3 : d4;
@@ -447,7 +473,7 @@ __device__ __forceinline__ void tile_softmax(uint32_t t_s, uint32_t t_o, float s
   }
 }
 
-template <int D, int ACT, int NALU>
+template <int D, int ACT, int NALU, bool WIN>
 __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int slot, int n_units, Fail fail) {
   constexpr bool kSoftmax = ACT == 2;
   const int warp = threadIdx.x >> 5;
@@ -462,7 +488,7 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
   for (int rr = 0;; ++rr) {
     const int idx = unit_index(rr, blockIdx.x, gridDim.x);
     if (idx >= n_units) break;
-    const FwdUnit u = fwd_unit(p, idx);
+    const FwdUnit u = fwd_unit<WIN>(p, idx);
     const int rows = u.rows_s[slot];
     if (rows <= 0) continue;
     const int t = 2 * u.pair + slot;
@@ -486,33 +512,44 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
       bc_hi = __ldg(brow + p.bias_len - 1);
     }
     bool ok = true;
-    for (int kt = 0; kt < nkv; ++kt) {
+    const int kfirst = u.k0 + u.beg_s[slot];  // this slot's key/value tiles: kfirst .. kend - 1
+    const int kend = kfirst + nkv;
+    for (int kt = kfirst; kt < kend; ++kt) {
       if (!(ok = mbar_wait(&bars->s_full[slot], s_it & 1, fail))) break;
       ++s_it;
       tc_fence_after();
       const int j0 = kt * kTile;
+      const int i_row = t * kTile + r;  // segment-local query row
+      // valid columns of this row: lo <= c < nvalid
       int nvalid = min(kTile, u.seg.lkv - j0);
-      if (p.causal) nvalid = min(nvalid, t * kTile + r - j0 + 1);
-      const bool tile_masked = (u.seg.lkv - j0 < kTile) || (p.causal && kt == t);
+      if (p.causal) nvalid = min(nvalid, i_row - j0 + 1);
+      int lo = 0;
+      bool tile_masked = (u.seg.lkv - j0 < kTile) || (p.causal && kt == t);
+      if constexpr (WIN) {  // j0 + c in (i - w, i + w); each bound is formed only where it binds
+        const int dj = i_row - j0;
+        if (p.window <= kTile - dj) nvalid = min(nvalid, dj + p.window);
+        if (dj >= p.window) lo = dj - p.window + 1;
+        tile_masked = tile_masked || abs(t - kt) * kTile + (kTile - 1) >= p.window;
+      }
       const int nchunks = (min(kTile, u.seg.lkv - j0) + 31) / 32;
       const TileBias tb = tile_bias(p, u.h, t * kTile, r, j0, bc_lo, bc_hi);
       if constexpr (!kSoftmax) {
         const float hs = 0.5f * p.scale;
         if (tb.band) {
-          if (tile_masked) tile_act<ACT, NALU, true, true>(t_s, hs, tb, nvalid, nchunks);
-          else tile_act<ACT, NALU, true, false>(t_s, hs, tb, nvalid, nchunks);
+          if (tile_masked) tile_act<ACT, NALU, true, true>(t_s, hs, tb, lo, nvalid, nchunks);
+          else tile_act<ACT, NALU, true, false>(t_s, hs, tb, lo, nvalid, nchunks);
         } else {
-          if (tile_masked) tile_act<ACT, NALU, false, true>(t_s, hs, tb, nvalid, nchunks);
-          else tile_act<ACT, NALU, false, false>(t_s, hs, tb, nvalid, nchunks);
+          if (tile_masked) tile_act<ACT, NALU, false, true>(t_s, hs, tb, lo, nvalid, nchunks);
+          else tile_act<ACT, NALU, false, false>(t_s, hs, tb, lo, nvalid, nchunks);
         }
       } else {
-        const bool first = kt == 0;
+        const bool first = kt == kfirst;
         if (tb.band) {
-          if (tile_masked) tile_softmax<D, true, true>(t_s, t_o, p.scale, tb, nvalid, first, m_run, l_run);
-          else tile_softmax<D, true, false>(t_s, t_o, p.scale, tb, nvalid, first, m_run, l_run);
+          if (tile_masked) tile_softmax<D, true, true>(t_s, t_o, p.scale, tb, lo, nvalid, first, m_run, l_run);
+          else tile_softmax<D, true, false>(t_s, t_o, p.scale, tb, lo, nvalid, first, m_run, l_run);
         } else {
-          if (tile_masked) tile_softmax<D, false, true>(t_s, t_o, p.scale, tb, nvalid, first, m_run, l_run);
-          else tile_softmax<D, false, false>(t_s, t_o, p.scale, tb, nvalid, first, m_run, l_run);
+          if (tile_masked) tile_softmax<D, false, true>(t_s, t_o, p.scale, tb, lo, nvalid, first, m_run, l_run);
+          else tile_softmax<D, false, false>(t_s, t_o, p.scale, tb, lo, nvalid, first, m_run, l_run);
         }
       }
       tmem_st_wait();
@@ -524,7 +561,9 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
     if (!mbar_wait(&bars->o_full[slot], o_it & 1, fail)) break;
     ++o_it;
     tc_fence_after();
-    const float inv_l = kSoftmax ? 1.0f / l_run : 1.0f;
+    // softmax: a row that met no key (possible under a sliding window) has
+    // l = 0 and O = 0; it keeps O = 0 and gets LSE = -inf
+    const float inv_l = kSoftmax ? (l_run > 0.f ? 1.0f / l_run : 0.f) : 1.0f;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t o[32];
@@ -544,12 +583,12 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
     tc_fence_before();
     mbar_arrive_warp(&bars->o_empty[slot]);
     if (kSoftmax && row_ok && p.lse)
-      p.lse[static_cast<int64_t>(u.h) * p.total_q + grow] = (m_run + __log2f(l_run)) * kLn2;
+      p.lse[static_cast<int64_t>(u.h) * p.total_q + grow] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
   }
 }
 
 // ----------------------------------------------------------------- kernel
-template <int D, int ACT, int NALU>
+template <int D, int ACT, int NALU, bool WIN>
 __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -589,11 +628,11 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   Fail fail{&bars->abort, p.status};
 
   if (warp == 0) {
-    fwd_producer<D>(p, smem, bars, n_units, fail);
+    fwd_producer<D, WIN>(p, smem, bars, n_units, fail);
   } else if (warp == 1) {
-    fwd_mma<D>(p, smem, bars, tmem, n_units, fail);
+    fwd_mma<D, WIN>(p, smem, bars, tmem, n_units, fail);
   } else if (warp >= 4) {
-    fwd_act<D, ACT, NALU>(p, bars, tmem, (warp - 4) >> 2, n_units, fail);
+    fwd_act<D, ACT, NALU, WIN>(p, bars, tmem, (warp - 4) >> 2, n_units, fail);
   }
   tc_fence_before();
   __syncthreads();
@@ -605,7 +644,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
 template <int D, int ACT>
 static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = gdpa_fwd_kernel<D, ACT, kFwdAluChunks>;
+  auto kern = p.window > 0 ? gdpa_fwd_kernel<D, ACT, kFwdAluChunks, true> : gdpa_fwd_kernel<D, ACT, kFwdAluChunks, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, C::kSmemBytes, stream>>>(p);

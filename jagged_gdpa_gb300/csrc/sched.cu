@@ -25,15 +25,15 @@ __device__ int items_of_segment(int kind, const Seg& s) {
   return ceil_div(s.lq, kTile);
 }
 
-__device__ int cost_of_item(int kind, const Seg& s, int tile, int causal) {
+__device__ int cost_of_item(int kind, const Seg& s, int tile, int causal, int window) {
   if (kind == kUnitsFwd) {
     const int t0 = 2 * tile, t1 = 2 * tile + 1;
-    int c = kv_tiles_for_q_tile(t0, s.lkv, causal) + 1;
-    if (s.lq > t1 * kTile) c += kv_tiles_for_q_tile(t1, s.lkv, causal) + 1;
+    int c = kv_span_for_q_tile(t0, s.lkv, causal, window).count + 1;
+    if (s.lq > t1 * kTile) c += kv_span_for_q_tile(t1, s.lkv, causal, window).count + 1;
     return c;
   }
-  if (kind == kUnitsKv) return q_tiles_for_kv_tile(tile, s.lq, causal) + 1;
-  return kv_tiles_for_q_tile(tile, s.lkv, causal) + 1;
+  if (kind == kUnitsKv) return q_span_for_kv_tile(tile, s.lq, causal, window).count + 1;
+  return kv_span_for_q_tile(tile, s.lkv, causal, window).count + 1;
 }
 
 // Inclusive scan of one value per thread over the whole block.
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
     return;
   }
 
-  // ---- stored dS (backward): first scratch tile of each segment, H nq nk
-  // tiles per segment, checked against the caller's capacity
+  // ---- stored dS (backward): first scratch tile of each segment, H nk span
+  // tiles per segment (span: ds_span), checked against the caller's capacity
   if (p.ds_base != nullptr && blockIdx.x == 0) {
     __shared__ long long warp_tot64[32];
     __shared__ long long carry64;
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
       long long v = 0;
       if (b < p.batch) {
         const Seg sg = load_seg(p.q_off, p.kv_off, b);
-        v = static_cast<long long>(p.heads) * ceil_div(sg.lq, kTile) * ceil_div(sg.lkv, kTile);
+        v = static_cast<long long>(p.heads) * ceil_div(sg.lkv, kTile) * ds_span(ceil_div(sg.lq, kTile), p.window);
       }
       const long long incl = block_inclusive_scan64(v, warp_tot64);
       if (b < p.batch) p.ds_base[b] = carry64 + incl - v;
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
   for (int it = tid; it < n_items; it += kSchedThreads) {
     int b, tile;
     locate(it, b, tile);
-    const int cost = cost_of_item(L.kind, load_seg(p.q_off, p.kv_off, b), tile, p.causal);
+    const int cost = cost_of_item(L.kind, load_seg(p.q_off, p.kv_off, b), tile, p.causal, p.window);
     atomicAdd(&hist[kCostBuckets - 1 - min(cost, kCostBuckets - 1)], 1);
   }
   __syncthreads();
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
   for (int it = tid; it < n_items; it += kSchedThreads) {
     int b, tile;
     locate(it, b, tile);
-    const int cost = cost_of_item(L.kind, load_seg(p.q_off, p.kv_off, b), tile, p.causal);
+    const int cost = cost_of_item(L.kind, load_seg(p.q_off, p.kv_off, b), tile, p.causal, p.window);
     const int pos = atomicAdd(&hist[kCostBuckets - 1 - min(cost, kCostBuckets - 1)], 1);
     for (int h = 0; h < p.heads; ++h)
       L.units[static_cast<int64_t>(pos) * p.heads + h] = make_int4(b, h, tile, cost);

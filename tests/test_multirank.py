@@ -58,3 +58,8 @@ def test_valid_pair_count_matches_brute_force():
         brute = sum(int(((np.arange(b)[None, :] <= np.arange(a)[:, None]) | (not causal)).sum())
                     for a, b in zip(lq, lkv))
         assert bench.valid_pairs(lq, lkv, causal) == brute
+        for window in (1, 3, 17):
+            brute_w = sum(int((((np.arange(b)[None, :] <= np.arange(a)[:, None]) | (not causal))
+                               & (np.abs(np.arange(a)[:, None] - np.arange(b)[None, :]) < window)).sum())
+                          for a, b in zip(lq, lkv))
+            assert bench.valid_pairs(lq, lkv, causal, window) == brute_w

@@ -2,7 +2,7 @@
 
 Bar (per output tensor): max|gpu - oracle| <= 2e-2 * max|oracle|; offsets
 and lengths are integers and must be reproduced exactly.  Small cases run the
-oracle on everything; the five named workloads run at full size on the GPU
+oracle on everything; the named workloads run at full size on the GPU
 and the oracle recomputes a sample of (segment, head) units, whose rows are
 compared (each unit is independent of the others).
 """
@@ -28,7 +28,7 @@ def jg():
 def run_fwd(jg, x):
     d = x.to("cuda")
     out, lse = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale,
-                            bias_table=d.bias, causal=x.causal)
+                            bias_table=d.bias, causal=x.causal, window=x.window)
     torch.cuda.synchronize()
     return out.cpu(), (None if lse is None else lse.cpu())
 
@@ -39,15 +39,16 @@ def run_bwd(jg, x, out=None, lse=None, stored=False):
     d = x.to("cuda")
     if x.act == "softmax":
         out, lse = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale,
-                                bias_table=d.bias, causal=x.causal)
+                                bias_table=d.bias, causal=x.causal, window=x.window)
     scratch = None
     if stored:
-        nbytes = jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, x.heads)
+        nbytes = jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, x.heads, x.window)
         scratch = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
     ws = torch.empty(jg.jgdpa_workspace_bytes(x.batch, x.q.shape[0], x.k.shape[0], x.heads, x.head_dim, x.act,
                                               x.bias_len, True), dtype=torch.uint8, device="cuda")
     dq, dk, dv, db = jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act,
-                                  x.scale, bias_table=d.bias, causal=x.causal, workspace=ws, ds_scratch=scratch)
+                                  x.scale, bias_table=d.bias, causal=x.causal, workspace=ws, ds_scratch=scratch,
+                                  window=x.window)
     torch.cuda.synchronize()
     assert jg.jgdpa_read_device_status(ws) == 0, "device status"
     return dq.cpu(), dk.cpu(), dv.cpu(), (None if db is None else db.cpu())
@@ -115,6 +116,60 @@ def test_edge_lengths(jg, act):
     check_bwd_full(jg, x, "edge bwd causal", stored=True)
 
 
+# ------------------------------------------------------------ sliding window
+WINDOW_FWD = [(d, act, causal, w) for d in (64, 128) for act in ("gelu", "silu", "softmax")
+              for causal in (False, True) for w in (1, 129, 300)]
+WINDOW_BWD = [(d, act, causal, w) for d in (64, 128) for act in ("gelu", "softmax")
+              for causal in (False, True) for w in (1, 129, 300)]
+
+
+def _window_case(seed, d, act, causal, w, batch):
+    # lengths up to ~5.5 tiles, so that whole tiles fall outside the band
+    return workloads.random_case(seed, batch=batch, heads=2, head_dim=d, act=act, lq_range=(1, 700),
+                                 lkv_range=(1, 700), causal=causal, bias_len=257, window=w)
+
+
+@pytest.mark.parametrize("d,act,causal,w", WINDOW_FWD)
+def test_forward_window(jg, d, act, causal, w):
+    x = _window_case(3000 + d + w + int(causal), d, act, causal, w, batch=5)
+    check_fwd_full(jg, x, f"d={d} {act} causal={causal} window={w}")
+
+
+@pytest.mark.parametrize("stored", [False, True])
+@pytest.mark.parametrize("d,act,causal,w", WINDOW_BWD)
+def test_backward_window(jg, d, act, causal, w, stored):
+    x = _window_case(4000 + d + w + int(causal), d, act, causal, w, batch=4)
+    check_bwd_full(jg, x, f"d={d} {act} causal={causal} window={w}", stored=stored)
+
+
+@pytest.mark.parametrize("act", ["gelu", "softmax"])
+def test_window_rows_without_keys(jg, act):
+    """Lq far beyond Lkv + w: the later query rows (and whole query tiles)
+    meet no key: O = 0, LSE = -inf, no gradient from them."""
+    lq = [600, 300, 1, 129]
+    lkv = [40, 1, 5, 129]
+    rng = np.random.default_rng(21)
+    for w in (1, 7, 130):
+        x = workloads.make_inputs(lq, lkv, 2, 128, act, bias_len=257, rng=rng, window=w)
+        check_fwd_full(jg, x, f"no-key rows fwd window={w}")
+        check_bwd_full(jg, x, f"no-key rows bwd window={w}")
+        check_bwd_full(jg, x, f"no-key rows bwd window={w}", stored=True)
+
+
+def test_window_covering_every_pair_equals_no_window(jg):
+    """A window at least as long as every segment changes nothing (bitwise)."""
+    x = workloads.random_case(77, batch=4, heads=2, head_dim=128, act="gelu", lq_range=(1, 400),
+                              lkv_range=(1, 400), bias_len=257)
+    import dataclasses
+    y = dataclasses.replace(x, window=400)
+    o0, _ = run_fwd(jg, x)
+    o1, _ = run_fwd(jg, y)
+    assert torch.equal(o0, o1)
+    g0, g1 = run_bwd(jg, x), run_bwd(jg, y)
+    for a, b in zip(g0[:3], g1[:3]):
+        assert torch.equal(a, b)
+
+
 def test_workload_1_tiny_full(jg):
     x = workloads.workload_inputs(1)
     check_fwd_full(jg, x, "w1")
@@ -163,6 +218,7 @@ def check_sampled(jg, x, units_fwd, units_bwd, tag, stored=False):
     (3, 6, None, None),
     (4, 6, None, None),
     (5, 4, None, 3e7),
+    (6, 4, 4e7, 4e7),
 ])
 def test_full_size_workloads_sampled(jg, idx, n_random, max_pairs_fwd, max_pairs_bwd):
     x = workloads.workload_inputs(idx)
