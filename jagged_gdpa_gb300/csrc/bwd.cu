@@ -486,7 +486,11 @@ __device__ void bwd_ds_store(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
         const int row = ds_row(p.ds_base, u.seg, u.b, u.h, u.tile, u.first + i, WIN ? p.window : 0);
         const uint8_t* src = x_base + xs * C::kXBytes;
         tma_store_2d_hint(&p.tm_ds, src, 0, row, policy);
-        tma_store_2d_hint(&p.tm_ds, src + C::kXBytes / 2, kTile / 2, row, policy);
+        // at d <= 64, the upper 64 query columns only where a query row of
+        // the segment reaches them (the dQ pass never reads them otherwise;
+        // at d = 128 the branch measured slower in this pass)
+        if (D == 128 || u.seg.lq - (u.first + i) * kTile > kTile / 2)
+          tma_store_2d_hint(&p.tm_ds, src + C::kXBytes / 2, kTile / 2, row, policy);
         bulk_commit();
         bulk_wait_read_all();
         mbar_arrive(&bars->x_empty[xs]);
@@ -1101,10 +1105,13 @@ __global__ void __launch_bounds__(256, 1) gdpa_dq_ds_kernel(const __grid_constan
         if (!(ok = mbar_wait_warp(&bars->empty[st], ((it / C::kStages) & 1) ^ 1, fail))) break;
         if (leader) {
           uint8_t* dst = smem + st * C::kStageBytes;
-          mbar_arrive_tx(&bars->full[st], C::kStageBytes);
+          // query rows 64..127 of a tile that ends before them were not
+          // stored; their stale half only feeds dQ rows that are not written
+          const bool upper = u.rows > kTile / 2;
+          mbar_arrive_tx(&bars->full[st], C::kStageBytes - (upper ? 0 : kDsTileBytes / 2));
           const int row = ds_row(p.ds_base, u.seg, u.b, u.h, kt, u.tile, p.window);
           tma_load_2d_hint(dst, &p.tm_ds, &bars->full[st], 0, row, policy);
-          tma_load_2d_hint(dst + kDsTileBytes / 2, &p.tm_ds, &bars->full[st], kTile / 2, row, policy);
+          if (upper) tma_load_2d_hint(dst + kDsTileBytes / 2, &p.tm_ds, &bars->full[st], kTile / 2, row, policy);
 #pragma unroll
           for (int cb = 0; cb < C::kNumBlocks; ++cb)
             tma_load_3d(dst + kDsTileBytes + cb * C::kBlockBytes, &p.tm_k, &bars->full[st], cb * C::kBlockCols,
