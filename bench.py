@@ -103,9 +103,9 @@ WORKLOAD_TEXT = {
 # long-tail workload, from a one-pass ncu capture of the current kernels at
 # that size; emptied whenever a kernel changes after the capture.
 TRAFFIC = {
-    "gdpa_fwd_kernel": 1.419974e9 + 0.343300e9,
-    "gdpa_bwd_kernel (dK/dV pass)": 2.221351e9 + 13.152255e9,
-    "gdpa_bwd_kernel (dQ pass)": 12.910343e9 + 0.262154e9,
+    "gdpa_fwd_kernel": 1.462840e9 + 0.334485e9,
+    "gdpa_bwd_kernel (dK/dV pass)": 2.257031e9 + 13.151038e9,
+    "gdpa_bwd_kernel (dQ pass)": 12.911199e9 + 0.264141e9,
 }
 
 

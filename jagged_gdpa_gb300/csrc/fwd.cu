@@ -62,9 +62,20 @@ struct FwdCfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+  static constexpr int kEpiOff = kVOff + kStages * kTileBytes;  // epilogue staging, if any
   static constexpr int kTmemCols = 512;
+};
+
+// The rest of the layout depends on the activation: GELU / SiLU at d >= 64
+// stage the O epilogue (4 KB per activation warp).  Softmax does not: its
+// kernel spills more, spills go through L1, and L1 is what shared memory
+// leaves over (the staged softmax forward measured 8% slower).
+template <int D, int ACT>
+struct FwdSmem {
+  static constexpr bool kStage = D >= 64 && ACT != 2;
+  static constexpr int kBarOff = FwdCfg<D>::kEpiOff + (kStage ? 8 * 4096 : 0);
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct FwdBars {
@@ -474,7 +485,9 @@ __device__ __forceinline__ void tile_softmax(uint32_t t_s, uint32_t t_o, float s
 }
 
 template <int D, int ACT, int NALU, bool WIN>
-__device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int slot, int n_units, Fail fail) {
+__device__ void fwd_act(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32_t tmem, int slot, int n_units,
+                        Fail fail) {
+  using C = FwdCfg<D>;
   constexpr bool kSoftmax = ACT == 2;
   const int warp = threadIdx.x >> 5;
   const int quad = warp & 3;
@@ -564,19 +577,58 @@ __device__ void fwd_act(const FwdParams& p, FwdBars* bars, uint32_t tmem, int sl
     // softmax: a row that met no key (possible under a sliding window) has
     // l = 0 and O = 0; it keeps O = 0 and gets LSE = -inf
     const float inv_l = kSoftmax ? (l_run > 0.f ? 1.0f / l_run : 0.f) : 1.0f;
+    if constexpr (FwdSmem<D, ACT>::kStage) {
+      // A thread owns one row and rows lie H D 2 bytes apart, so plain stores
+      // would touch 32 lines per instruction.  Each 64-column half of the
+      // warp's 32 rows is staged in the warp's own 4 KB of shared memory
+      // (XOR-swizzled 16-byte chunks), then stored four whole 128-byte rows
+      // per instruction.
+      const int lr = threadIdx.x & 31;
+      const uint32_t stg = smem_u32(smem + C::kEpiOff) + (warp - 4) * 4096;
+      const int64_t row0 = grow - lr;  // global row of the warp's first row
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t o[32];
-      tmem_ld32(t_o + c0, o);
-      tmem_ld_wait(o);
-      if (row_ok) {
+      for (int hb = 0; hb < D / 64; ++hb) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 8) {
-          uint32_t w[4];
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + 64 * hb + c0, o);
+          tmem_ld_wait(o);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * inv_l, __uint_as_float(o[c + 2 * e + 1]) * inv_l);
-          st_global_v4(out_row + c0 + c, w[0], w[1], w[2], w[3]);
+          for (int c = 0; c < 32; c += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * inv_l, __uint_as_float(o[c + 2 * e + 1]) * inv_l);
+            const int j = (c0 + c) >> 3;
+            st_shared_v4(stg + lr * 128 + ((j ^ (lr & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rr = 4 * k + (lr >> 3), j = lr & 7;
+          uint32_t a, b2, c2, d2;
+          ld_shared_v4(stg + rr * 128 + ((j ^ (rr & 7)) << 4), a, b2, c2, d2);
+          if (quad * 32 + rr < rows)
+            st_global_v4(p.out + ((row0 + rr) * H + u.h) * D + 64 * hb + 8 * j, a, b2, c2, d2);
+        }
+        __syncwarp();
+      }
+    } else {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c0, o);
+        tmem_ld_wait(o);
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * inv_l, __uint_as_float(o[c + 2 * e + 1]) * inv_l);
+            st_global_v4(out_row + c0 + c, w[0], w[1], w[2], w[3]);
+          }
         }
       }
     }
@@ -593,7 +645,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::kBarOff);
+  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + FwdSmem<D, ACT>::kBarOff);
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -632,7 +684,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   } else if (warp == 1) {
     fwd_mma<D, WIN>(p, smem, bars, tmem, n_units, fail);
   } else if (warp >= 4) {
-    fwd_act<D, ACT, NALU, WIN>(p, bars, tmem, (warp - 4) >> 2, n_units, fail);
+    fwd_act<D, ACT, NALU, WIN>(p, smem, bars, tmem, (warp - 4) >> 2, n_units, fail);
   }
   tc_fence_before();
   __syncthreads();
@@ -643,11 +695,11 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
 // ------------------------------------------------------------------ launch
 template <int D, int ACT>
 static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
-  using C = FwdCfg<D>;
   auto kern = p.window > 0 ? gdpa_fwd_kernel<D, ACT, kFwdAluChunks, true> : gdpa_fwd_kernel<D, ACT, kFwdAluChunks, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  constexpr int kSmemBytes = FwdSmem<D, ACT>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 384, C::kSmemBytes, stream>>>(p);
+  kern<<<grid, 384, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
