@@ -344,39 +344,75 @@ def run_native(args, world, rank, local):
     ms_step, value = aggregate(world, f_fwd + f_bwd, ms_total / args.steps)
 
     # end to end through the public API: pinned host inputs -> device, step,
-    # results -> pinned host
+    # results -> pinned host, every step.  Double-buffered as an input
+    # pipeline would be: a copy stream loads step i+1's inputs into the other
+    # input set while step i computes, and a second copy stream reads step
+    # i's results from its own output set while step i+1 computes.
     in_names = ["q", "k", "v", "dout", "q_offsets", "kv_offsets"] + (["bias"] if bias_len else [])
     host_in = {k: getattr(x, k).pin_memory() for k in in_names}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    results = [("out", out), ("dq", dq), ("dk", dk), ("dv", dv)] + ([("dbias", dbias)] if bias_len else [])
-    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in results}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
-
-    def e2e_step():
-        for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        o, l2 = jg.jgdpa_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["q_offsets"], dev_in["kv_offsets"],
-                             x.act, x.scale, bias_table=dev_in.get("bias"), causal=x.causal, out=out, lse=lse,
-                             workspace=ws_f, window=x.window)
-        jg.jgdpa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, l2, dev_in["dout"], dev_in["q_offsets"],
-                     dev_in["kv_offsets"], x.act, x.scale, bias_table=dev_in.get("bias"), causal=x.causal, dq=dq,
-                     dk=dk, dv=dv, dbias=dbias, workspace=ws_b, ds_scratch=ds_scratch, window=x.window)
-        for k, t in results:
-            host_out[k].copy_(t, non_blocking=True)
-
     ms_e2e = float("nan")
+    d2h = 0
     if not args.no_e2e:
-        for _ in range(max(1, args.warmup // 2)):
-            e2e_step()
+        dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
+        res = [{"out": out, "dq": dq, "dk": dk, "dv": dv}, {"out": torch.empty_like(out), "dq": torch.empty_like(dq),
+                                                            "dk": torch.empty_like(dk), "dv": torch.empty_like(dv)}]
+        if bias_len:
+            res[0]["dbias"], res[1]["dbias"] = dbias, torch.empty_like(dbias)
+        lse2 = [lse, None if lse is None else torch.empty_like(lse)]
+        host_out = [{k: torch.empty_like(t, device="cpu").pin_memory() for k, t in r.items()} for r in res]
+        d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+        comp = torch.cuda.current_stream()
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        in_free = [torch.cuda.Event() for _ in range(2)]
+        out_ready = [torch.cuda.Event() for _ in range(2)]
+        out_free = [torch.cuda.Event() for _ in range(2)]
+
+        def load(i):
+            bi = i % 2
+            s_in.wait_event(in_free[bi])
+            with torch.cuda.stream(s_in):
+                for k, v in host_in.items():
+                    dev_in[bi][k].copy_(v, non_blocking=True)
+            in_ready[bi].record(s_in)
+
+        def run(n):
+            for e in in_free + out_free:
+                e.record(comp)
+            load(0)
+            for i in range(n):
+                bi = i % 2
+                if i + 1 < n:
+                    load(i + 1)
+                comp.wait_event(in_ready[bi])
+                comp.wait_event(out_free[bi])
+                di, r = dev_in[bi], res[bi]
+                o, l2 = jg.jgdpa_fwd(di["q"], di["k"], di["v"], di["q_offsets"], di["kv_offsets"], x.act, x.scale,
+                                     bias_table=di.get("bias"), causal=x.causal, out=r["out"], lse=lse2[bi],
+                                     workspace=ws_f, window=x.window)
+                jg.jgdpa_bwd(di["q"], di["k"], di["v"], o, l2, di["dout"], di["q_offsets"], di["kv_offsets"],
+                             x.act, x.scale, bias_table=di.get("bias"), causal=x.causal, dq=r["dq"], dk=r["dk"],
+                             dv=r["dv"], dbias=r.get("dbias"), workspace=ws_b, ds_scratch=ds_scratch,
+                             window=x.window)
+                in_free[bi].record(comp)
+                out_ready[bi].record(comp)
+                s_out.wait_event(out_ready[bi])
+                with torch.cuda.stream(s_out):
+                    for k, t in r.items():
+                        host_out[bi][k].copy_(t, non_blocking=True)
+                out_free[bi].record(s_out)
+            for e in out_free:  # every read-back has landed
+                comp.wait_event(e)
+
+        run(max(1, args.warmup // 2))
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(comp)
+        run(args.steps)
+        e1.record(comp)
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
         barrier(world)
@@ -462,6 +498,8 @@ def run_native(args, world, rank, local):
             "ms_per_step": round(ms_e2e, 4),
             "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h),
+            "copies": "every step's inputs in and results out; step i+1's copy in and step i-1's copy out "
+                      "overlap step i on two copy streams (double-buffered inputs and results)",
         },
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
