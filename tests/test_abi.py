@@ -79,3 +79,37 @@ def test_workspace_query_rejects_invalid_sizes(lib):
     import jagged_gdpa_gb300 as jg
     assert jg.jgdpa_workspace_bytes(1, 4, 4, 1, 48, "gelu") == 0
     assert jg.jgdpa_workspace_bytes(-1, 4, 4, 1, 64, "gelu") == 0
+
+
+@pytest.mark.parametrize("window,code", [(-1, 1), (-1000, 1)])
+def test_fwd_ex_rejects_a_negative_window_without_a_launch(lib, window, code):
+    args = _fwd_args()
+    args.insert(15, window)  # after causal
+    assert lib.jgdpa_fwd_ex(*args) == code
+    # a valid window still meets the other checks first: bad head_dim
+    args = _fwd_args(d=48)
+    args.insert(15, 5)
+    assert lib.jgdpa_fwd_ex(*args) == 2
+
+
+def test_ds_scratch_size_follows_the_band(lib):
+    """Stored-dS scratch: heads * sum_b nk_b * span_b tiles of 32 KB, span = nq
+    without a window, else min(nq, 2e + 1) with e = ceil((w - 1) / 128)."""
+    import numpy as np
+    import torch
+    import jagged_gdpa_gb300 as jg
+    import workloads
+    rng = np.random.default_rng(3)
+    lq = rng.integers(0, 3000, size=9)
+    lkv = rng.integers(0, 3000, size=9)
+    qo, ko = workloads.offsets_from_lengths(lq), workloads.offsets_from_lengths(lkv)
+    for heads in (1, 3):
+        for w in (0, 1, 2, 128, 129, 300, 1000, 5000):
+            nq, nk = -(-lq // 128), -(-lkv // 128)
+            e = -(-(w - 1) // 128) if w > 0 else 0
+            span = nq if w == 0 else np.minimum(nq, 2 * e + 1)
+            want = int(heads * np.sum(nk * span)) * 32768
+            assert jg.jgdpa_ds_scratch_bytes(qo, ko, heads, w) == want, (heads, w)
+    assert jg.jgdpa_ds_scratch_bytes(qo, ko, 1, -1) == 0
+    # the band never holds more than the unwindowed scratch
+    assert jg.jgdpa_ds_scratch_bytes(qo, ko, 2, 300) <= jg.jgdpa_ds_scratch_bytes(qo, ko, 2, 0)
