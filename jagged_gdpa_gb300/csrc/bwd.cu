@@ -863,45 +863,49 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     if (!mbar_wait(&bars->acc_full, acc_it & 1, fail)) break;
     ++acc_it;
     tc_fence_after();
-    if constexpr (KV_MAJOR && D == 64) {
+    if constexpr (KV_MAJOR && D >= 64) {
       // warpgroup 0 stores dV, warpgroup 1 stores dK (scaled by s).  A thread
-      // owns one 128-byte row and rows lie H D 2 bytes apart, so plain stores
-      // would touch 32 lines per instruction.  The warp stages its 32 rows in
-      // its own block of the next X slot (the rows and columns it writes dS to
-      // in phase B, free once that slot is empty), then stores four whole rows
-      // per instruction.
+      // owns one row and rows lie H D 2 bytes apart, so plain stores would
+      // touch 32 lines per instruction.  The warp stages 64 columns of its 32
+      // rows at a time in its own 4 KB block of the next X slot (the rows and
+      // columns it writes dS to in phase B, free once that slot is empty),
+      // then stores four whole 128-byte row pieces per instruction.
       const uint32_t t_acc = tmem + lane_off + 256 + D * half;
       const float mul = half == 0 ? 1.0f : p.scale;
       const int xs = x.slot<C::kNumX>();
       if (!mbar_wait(&bars->x_empty[xs], x.empty_parity<C::kNumX>(), fail)) break;
       const int lr = threadIdx.x & 31;
       const uint32_t blk = x_base + xs * C::kXBytes + half * (kTile * 128) + quad * 32 * 128;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(t_acc + c0, o);
-        tmem_ld_wait(o);
-#pragma unroll
-        for (int c = 0; c < 32; c += 8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * mul, __uint_as_float(o[c + 2 * e + 1]) * mul);
-          const int j = (c0 + c) >> 3;  // 16-byte chunk of the row
-          st_shared_v4(blk + lr * 128 + ((j ^ (lr & 7)) << 4), w[0], w[1], w[2], w[3]);
-        }
-      }
-      __syncwarp();
       __nv_bfloat16* base = half == 0 ? p.dv : p.dk;
       const int64_t row0 = grow - lr;  // global row of the warp's first row
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int rr = 4 * k + (lr >> 3), j = lr & 7;
-        uint32_t a, b2, c2, d2;
-        ld_shared_v4(blk + rr * 128 + ((j ^ (rr & 7)) << 4), a, b2, c2, d2);
-        if (quad * 32 + rr < u.rows) st_global_v4(base + ((row0 + rr) * H + u.h) * D + 8 * j, a, b2, c2, d2);
+      for (int hb = 0; hb < D / 64; ++hb) {
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_acc + 64 * hb + c0, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * mul, __uint_as_float(o[c + 2 * e + 1]) * mul);
+            const int j = (c0 + c) >> 3;  // 16-byte chunk of the 128-byte piece
+            st_shared_v4(blk + lr * 128 + ((j ^ (lr & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rr = 4 * k + (lr >> 3), j = lr & 7;
+          uint32_t a, b2, c2, d2;
+          ld_shared_v4(blk + rr * 128 + ((j ^ (rr & 7)) << 4), a, b2, c2, d2);
+          if (quad * 32 + rr < u.rows)
+            st_global_v4(base + ((row0 + rr) * H + u.h) * D + 64 * hb + 8 * j, a, b2, c2, d2);
+        }
+        __syncwarp();
       }
-      __syncwarp();
     } else if constexpr (KV_MAJOR) {
       // warpgroup 0 stores dV, warpgroup 1 stores dK (scaled by s)
       const uint32_t t_acc = tmem + lane_off + 256 + D * half;
