@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     jgdpa_ds_scratch_bytes,
     jgdpa_eval_activation,
     jgdpa_fwd,
+    jgdpa_fwd_noalloc,
     jgdpa_read_device_status,
     jgdpa_status_string,
     jgdpa_workspace_bytes,
