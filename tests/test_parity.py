@@ -226,3 +226,14 @@ def test_full_size_workloads_sampled(jg, idx, n_random, max_pairs_fwd, max_pairs
     ub = sample_units(x, n_random, seed=100 + idx, max_pairs=max_pairs_bwd)
     check_sampled(jg, x, uf, ub, f"w{idx}")
     check_sampled(jg, x, uf, ub, f"w{idx}", stored=True)
+
+
+def test_largest_bias_table_and_more_heads(jg):
+    """The largest accepted bias table (4095 entries, R = 2047) on segments
+    longer than R, so both clamped ends and the band are hit, with 16 heads."""
+    lq = [2600, 5, 300]
+    lkv = [2500, 2100, 1]
+    rng = np.random.default_rng(41)
+    x = workloads.make_inputs(lq, lkv, 16, 64, "gelu", bias_len=4095, rng=rng)
+    check_fwd_full(jg, x, "bias 4095, H=16")
+    check_bwd_full(jg, x, "bias 4095, H=16", stored=True)
