@@ -46,10 +46,10 @@ def _load():
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-        lib.oracle_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32, i32,
+        lib.oracle_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32, i32, i32,
                                    P, i32, i32, P, P]
         lib.oracle_fwd.restype = ctypes.c_int
-        lib.oracle_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32, i32,
+        lib.oracle_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32, i32, i32,
                                    P, i32, i32, P, P, P, P]
         lib.oracle_bwd.restype = ctypes.c_int
         lib.oracle_act_eval.argtypes = [i32, P, i64, P, P]
@@ -98,10 +98,12 @@ def _units(units: Optional[Sequence[int]]):
 
 def fwd(q, k, v, q_offsets, kv_offsets, heads: int, head_dim: int, act: str, scale: float,
         bias=None, causal: bool = False, units: Optional[Sequence[int]] = None,
-        threads: int = 0, window: int = 0):
+        threads: int = 0, window: int = 0, q_shared: int = 0):
     """O (float64 [total_q, H, d]) and LSE (float64 [H, total_q]).
 
     ``window`` > 0 keeps only the pairs with |i - j| < window (segment-local).
+    ``q_shared`` = S > 0: q is [S, H, d], read by every segment as its query
+    rows (each segment has Lq = S; q_offsets still place O and LSE).
 
     ``units`` restricts the work to (segment, head) units b*H + h; rows of
     other units are returned as NaN.
@@ -116,8 +118,8 @@ def fwd(q, k, v, q_offsets, kv_offsets, heads: int, head_dim: int, act: str, sca
     u, nu = _units(units)
     rc = _load().oracle_fwd(_ptr(qf), _ptr(kf), _ptr(vf), _ptr(qo), _ptr(ko), len(qo) - 1,
                             heads, head_dim, ACT_CODE[act], float(scale), _ptr(bf), bias_len,
-                            int(bool(causal)), int(window), _ptr(u), nu, int(threads), _ptr(out),
-                            _ptr(lse))
+                            int(bool(causal)), int(window), int(q_shared), _ptr(u), nu, int(threads),
+                            _ptr(out), _ptr(lse))
     if rc:
         raise ValueError("oracle_fwd rejected its arguments")
     return out, lse
@@ -125,8 +127,10 @@ def fwd(q, k, v, q_offsets, kv_offsets, heads: int, head_dim: int, act: str, sca
 
 def bwd(q, k, v, dout, q_offsets, kv_offsets, heads: int, head_dim: int, act: str,
         scale: float, bias=None, causal: bool = False,
-        units: Optional[Sequence[int]] = None, threads: int = 0, window: int = 0):
-    """dQ, dK, dV (float64, layouts of q/k/v) and dbias (float64 [H, T] or None)."""
+        units: Optional[Sequence[int]] = None, threads: int = 0, window: int = 0,
+        q_shared: int = 0):
+    """dQ, dK, dV (float64, layouts of q/k/v) and dbias (float64 [H, T] or None).
+    With ``q_shared`` = S > 0, dQ is [S, H, d]: the sum over segments."""
     qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(dout)
     qo, ko = _i32(q_offsets), _i32(kv_offsets)
     bf = None if bias is None else _f64(bias)
@@ -138,7 +142,8 @@ def bwd(q, k, v, dout, q_offsets, kv_offsets, heads: int, head_dim: int, act: st
     u, nu = _units(units)
     rc = _load().oracle_bwd(_ptr(qf), _ptr(kf), _ptr(vf), _ptr(dof), _ptr(qo), _ptr(ko),
                             len(qo) - 1, heads, head_dim, ACT_CODE[act], float(scale), _ptr(bf),
-                            bias_len, int(bool(causal)), int(window), _ptr(u), nu, int(threads),
+                            bias_len, int(bool(causal)), int(window), int(q_shared), _ptr(u), nu,
+                            int(threads),
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias))
     if rc:
         raise ValueError("oracle_bwd rejected its arguments")

@@ -40,7 +40,13 @@
  *     short attention windows) keeps the pairs with |i - j| < window, again
  *     with segment-local indices; window = 0 means no window, and with causal
  *     masking the two conditions combine (i - window < j <= i);
- *   - a row with no valid key gives O_i = 0 (and LSE_i = -inf in softmax mode).
+ *   - a row with no valid key gives O_i = 0 (and LSE_i = -inf in softmax mode);
+ *   - PMA-style pooling ("GEM Training ...", section "What to watch": learned
+ *     seed queries shared across the batch): with q_shared = S > 0, q holds S
+ *     rows that every segment reads as its query rows 0..S-1 (each segment
+ *     then has Lq = S, and q_off still places its O, dO and LSE rows); the
+ *     gradient of the shared rows is the sum over segments of each segment's
+ *     dQ, added in segment order.
  *
  * The backward pass is the analytic gradient of L = sum O * dO:
  *   dP_ij = <dO_i, v_j>
@@ -100,9 +106,16 @@ int oracle_act_eval(int32_t act, const double* x, int64_t n, double* y, double* 
 typedef struct {
     const double *q, *k, *v, *dout, *bias;
     const int32_t *q_off, *kv_off;
-    int32_t batch, heads, d, act, bias_len, causal, window;
+    int32_t batch, heads, d, act, bias_len, causal, window, q_shared;
     double scale;
 } problem;
+
+/* Query row i of segment b, head h (the shared rows when q_shared > 0). */
+static const double* q_row(const problem* p, int32_t b, int64_t i, int32_t h) {
+    const int64_t hd = (int64_t)p->heads * p->d;
+    const int64_t row = p->q_shared > 0 ? i : (int64_t)p->q_off[b] + i;
+    return p->q + row * hd + (int64_t)h * p->d;
+}
 
 static int valid_pair(const problem* p, int64_t i, int64_t j, int64_t lkv) {
     if (j >= lkv) return 0;
@@ -123,7 +136,7 @@ static int64_t bias_index(const problem* p, int64_t i, int64_t j) {
 /* x_ij = s <q_i, k_j> + bias. */
 static double logit(const problem* p, int32_t b, int32_t h, int64_t i, int64_t j) {
     const int64_t hd = (int64_t)p->heads * p->d;
-    const double* qi = p->q + ((int64_t)p->q_off[b] + i) * hd + (int64_t)h * p->d;
+    const double* qi = q_row(p, b, i, h);
     const double* kj = p->k + ((int64_t)p->kv_off[b] + j) * hd + (int64_t)h * p->d;
     double dot = 0.0;
     for (int32_t c = 0; c < p->d; ++c) dot += qi[c] * kj[c];
@@ -167,7 +180,8 @@ static void fwd_unit(const problem* p, int32_t b, int32_t h, double* out, double
 }
 
 /* Backward of one unit.  dq/dk/dv rows of the unit are overwritten; the
- * unit's dbias contribution is written to dbias_unit[T] (zeroed here). */
+ * unit's dbias contribution is written to dbias_unit[T] (zeroed here).  With
+ * shared queries dq is the unit's own [S][d] buffer instead. */
 static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double* dk,
                      double* dv, double* dbias_unit) {
     const int64_t lq = p->q_off[b + 1] - p->q_off[b];
@@ -176,8 +190,9 @@ static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double*
     const int64_t hd = (int64_t)p->heads * d;
     const int64_t q0 = p->q_off[b], k0 = p->kv_off[b];
     if (dbias_unit) memset(dbias_unit, 0, sizeof(double) * (size_t)p->bias_len);
+    const int shared = p->q_shared > 0;
     for (int64_t i = 0; i < lq; ++i) {
-        double* dqi = dq + (q0 + i) * hd + (int64_t)h * d;
+        double* dqi = shared ? dq + i * d : dq + (q0 + i) * hd + (int64_t)h * d;
         for (int32_t c = 0; c < d; ++c) dqi[c] = 0.0;
     }
     for (int64_t j = 0; j < lkv; ++j) {
@@ -193,7 +208,8 @@ static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double*
         int32_t qoff2[2] = {0, (int32_t)lq};
         int32_t koff2[2] = {0, (int32_t)lkv};
         problem sub = *p;
-        sub.q = p->q + q0 * hd;
+        sub.q = shared ? p->q : p->q + q0 * hd;
+        sub.q_shared = 0;
         sub.k = p->k + k0 * hd;
         sub.v = p->v + k0 * hd;
         sub.q_off = qoff2;
@@ -204,9 +220,9 @@ static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double*
         fwd_unit(&sub, 0, h, o, lse, lq);
     }
     for (int64_t i = 0; i < lq; ++i) {
-        const double* qi = p->q + (q0 + i) * hd + (int64_t)h * d;
+        const double* qi = q_row(p, b, i, h);
         const double* doi = p->dout + (q0 + i) * hd + (int64_t)h * d;
-        double* dqi = dq + (q0 + i) * hd + (int64_t)h * d;
+        double* dqi = shared ? dq + i * d : dq + (q0 + i) * hd + (int64_t)h * d;
         double di = 0.0, lse_i = 0.0;
         if (o) {
             const double* oi = o + i * hd + (int64_t)h * d;
@@ -252,6 +268,10 @@ static int check_problem(const problem* p) {
     if (p->batch > 0 && (p->q_off[0] != 0 || p->kv_off[0] != 0)) return 1;
     for (int32_t b = 0; b < p->batch; ++b)
         if (p->q_off[b + 1] < p->q_off[b] || p->kv_off[b + 1] < p->kv_off[b]) return 1;
+    if (p->q_shared < 0) return 1;
+    if (p->q_shared > 0)  /* every segment reads the S shared rows */
+        for (int32_t b = 0; b < p->batch; ++b)
+            if (p->q_off[b + 1] - p->q_off[b] != p->q_shared) return 1;
     return 0;
 }
 
@@ -272,10 +292,10 @@ int oracle_fwd(const double* q, const double* k, const double* v,
                const int32_t* q_off, const int32_t* kv_off, int32_t batch,
                int32_t heads, int32_t d, int32_t act, double scale,
                const double* bias, int32_t bias_len, int32_t causal, int32_t window,
-               const int32_t* units, int32_t n_units, int32_t threads,
+               int32_t q_shared, const int32_t* units, int32_t n_units, int32_t threads,
                double* out, double* lse) {
     problem p = {q, k, v, NULL, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, window,
-                 scale};
+                 q_shared, scale};
     if (check_problem(&p)) return 1;
     const int64_t total_q = batch > 0 ? q_off[batch] : 0;
     const int32_t n = units ? n_units : batch * heads;
@@ -296,20 +316,36 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                const int32_t* q_off, const int32_t* kv_off, int32_t batch,
                int32_t heads, int32_t d, int32_t act, double scale,
                const double* bias, int32_t bias_len, int32_t causal, int32_t window,
-               const int32_t* units, int32_t n_units, int32_t threads,
+               int32_t q_shared, const int32_t* units, int32_t n_units, int32_t threads,
                double* dq, double* dk, double* dv, double* dbias) {
     problem p = {q, k, v, dout, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, window,
-                 scale};
+                 q_shared, scale};
     if (check_problem(&p)) return 1;
     const int32_t n = units ? n_units : batch * heads;
     const int32_t t = bias_len > 0 ? bias_len : 1;
     double* part = (dbias && bias_len > 0)
                        ? (double*)calloc((size_t)n * (size_t)t, sizeof(double)) : NULL;
+    /* shared queries: each unit's dQ in its own [S][d] buffer, summed per
+       head in unit (segment) order below */
+    const int64_t sq = (int64_t)q_shared * d;
+    double* dq_part = q_shared > 0 ? (double*)calloc((size_t)n * (size_t)(sq > 0 ? sq : 1), sizeof(double))
+                                   : NULL;
     set_threads(threads);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t u = 0; u < n; ++u) {
         int32_t id = units ? units[u] : u;
-        bwd_unit(&p, id / heads, id % heads, dq, dk, dv, part ? part + (int64_t)u * t : NULL);
+        bwd_unit(&p, id / heads, id % heads, dq_part ? dq_part + (int64_t)u * sq : dq, dk, dv,
+                 part ? part + (int64_t)u * t : NULL);
+    }
+    if (dq_part) {
+        memset(dq, 0, sizeof(double) * (size_t)q_shared * (size_t)heads * (size_t)d);
+        for (int32_t u = 0; u < n; ++u) {
+            int32_t h = (units ? units[u] : u) % heads;
+            for (int64_t i = 0; i < q_shared; ++i)
+                for (int32_t c = 0; c < d; ++c)
+                    dq[(i * heads + h) * d + c] += dq_part[(int64_t)u * sq + i * d + c];
+        }
+        free(dq_part);
     }
     if (part) {
         memset(dbias, 0, sizeof(double) * (size_t)heads * (size_t)bias_len);

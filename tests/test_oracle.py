@@ -508,3 +508,73 @@ def test_window_rows_without_keys():
     y = type(y)(**{**y.__dict__, "q": x.q[:4], "dout": x.dout[:4], "k": x.k, "v": x.v})
     _, dk4, dv4, _ = oracle.bwd_inputs(y)
     assert np.allclose(dk, dk4, rtol=0, atol=1e-14) and np.allclose(dv, dv4, rtol=0, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# Shared query rows (PMA-style pooling): q_shared = S
+# ----------------------------------------------------------------------------
+
+def _shared_case(seed, act, batch=4, s=5, heads=2, d=8, bias_len=7, causal=False):
+    rng = np.random.default_rng(seed)
+    lkv = rng.integers(0, 14, size=batch)
+    return workloads.make_inputs(np.full(batch, s), lkv, heads, d, act, causal=causal, bias_len=bias_len,
+                                 rng=rng, shared_q=s)
+
+
+@pytest.mark.parametrize("act,causal", [("gelu", False), ("silu", True), ("softmax", False), ("softmax", True)])
+def test_shared_queries_equal_the_expanded_batch(act, causal):
+    """Shared rows read by every segment give the expanded batch's O, LSE, dK,
+    dV exactly, and dQ equal to the expanded dQ summed over segments."""
+    x = _shared_case(60 + len(act) + int(causal), act, causal=causal)
+    s = x.q_seed.shape[0]
+    o_e, l_e = oracle.fwd_inputs(x)
+    dq_e, dk_e, dv_e, db_e = oracle.bwd_inputs(x)
+    args = (x.k, x.v)
+    o_s, l_s = oracle.fwd(x.q_seed, *args, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, act, x.scale,
+                          bias=x.bias, causal=causal, q_shared=s)
+    dq_s, dk_s, dv_s, db_s = oracle.bwd(x.q_seed, *args, x.dout, x.q_offsets, x.kv_offsets, x.heads,
+                                        x.head_dim, act, x.scale, bias=x.bias, causal=causal, q_shared=s)
+    assert np.array_equal(o_s, o_e) and np.array_equal(l_s, l_e)
+    assert np.array_equal(dk_s, dk_e) and np.array_equal(dv_s, dv_e)
+    assert np.allclose(db_s, db_e, rtol=1e-13, atol=1e-15)
+    want = dq_e.reshape(x.batch, s, x.heads, x.head_dim).sum(axis=0)
+    assert dq_s.shape == (s, x.heads, x.head_dim)
+    assert _rel(dq_s, want) <= 1e-12
+
+
+@pytest.mark.parametrize("act", ["gelu", "softmax"])
+def test_shared_query_gradient_matches_autograd_through_the_broadcast(act):
+    """dQ of the shared rows against torch autograd on a dense formulation in
+    which one [S, H, d] leaf is broadcast to every segment."""
+    x = _shared_case(71, act, batch=3, s=4, d=4, bias_len=5)
+    s, b = x.q_seed.shape[0], x.batch
+    lkm = max(1, int(x.lkv.max()))
+    ko = x.kv_offsets.numpy().astype(np.int64)
+    qs = torch.tensor(x.q_seed.double().numpy(), requires_grad=True)            # [S, H, d]
+    kp = torch.tensor(_pad(x.k.double().numpy(), ko, lkm))
+    vp = torch.tensor(_pad(x.v.double().numpy(), ko, lkm))
+    dop = torch.tensor(x.dout.double().numpy().reshape(b, s, x.heads, x.head_dim))
+    i = torch.arange(s)[:, None]
+    j = torch.arange(lkm)[None, :]
+    mask = (j[None] < torch.tensor(x.lkv)[:, None, None]).expand(b, s, lkm)
+    m4 = mask[:, None]
+    sc = torch.einsum("ihc,bjhc->bhij", qs, kp) * x.scale
+    r = (x.bias.shape[1] - 1) // 2
+    sc = sc + x.bias.double()[:, torch.clamp(i - j, -r, r) + r][None]
+    if act == "softmax":
+        sm = torch.where(m4, sc, torch.full_like(sc, -torch.inf))
+        sm = torch.where(m4.any(-1, keepdim=True), sm, torch.zeros_like(sm))
+        p = torch.where(m4, torch.softmax(sm, dim=-1), torch.zeros_like(sm))
+    else:
+        p = torch.where(m4, torch.nn.functional.gelu(sc), torch.zeros_like(sc))
+    o = torch.einsum("bhij,bjhc->bihc", p, vp)
+    (o * dop).sum().backward()
+    dq_s, _, _, _ = oracle.bwd(x.q_seed, x.k, x.v, x.dout, x.q_offsets, x.kv_offsets, x.heads, x.head_dim,
+                               act, x.scale, bias=x.bias, q_shared=s)
+    assert _rel(dq_s, qs.grad.numpy()) <= 1e-10
+
+
+def test_shared_queries_need_equal_segment_lengths():
+    x = workloads.make_inputs([3, 4], [5, 5], 1, 4, "gelu", seed=2)
+    with pytest.raises(ValueError):
+        oracle.fwd(x.q[:3], x.k, x.v, x.q_offsets, x.kv_offsets, 1, 4, "gelu", x.scale, q_shared=3)
