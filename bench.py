@@ -118,7 +118,7 @@ def peaks():
 
 
 class Clocks:
-    """Samples nvidia-smi every 200 ms while the timed region runs."""
+    """Samples nvidia-smi every 50 ms while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -134,7 +134,7 @@ class Clocks:
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -431,8 +431,14 @@ def run_native(args, world, rank, local):
         "gdpa_bwd_kernel (dK/dV pass)": (statistics.mean(ms_kv), 2.0 * f_fwd),
         "gdpa_bwd_kernel (dQ pass)": (statistics.mean(ms_q), 0.5 * f_fwd),
     }
+    # The kernels are timed in a region of well under a second at full clock,
+    # so the denominator is the measured burst GEMM rate; the fraction of the
+    # measured sustained rate (a seconds-long GEMM loop under the power cap)
+    # is reported beside it.
     per_kernel = {k: {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
-                      "frac": round(fl / (ms * 1e-3) / 1e12 / bf16_sust, 4)} for k, (ms, fl) in kernels.items()}
+                      "frac": round(fl / (ms * 1e-3) / 1e12 / bf16_burst, 4),
+                      "frac_of_sustained": round(fl / (ms * 1e-3) / 1e12 / bf16_sust, 4)}
+                  for k, (ms, fl) in kernels.items()}
     # dram bytes per launch from the ncu capture above, valid for the full
     # long-tail workload only; with them each kernel also reports its DRAM
     # throughput against the measured copy bandwidth (the dQ pass streams the
@@ -479,16 +485,19 @@ def run_native(args, world, rank, local):
         "bwd_gbs": round(b_bwd / (statistics.mean(ms_bwd) * 1e-3) / 1e9, 1),
         "fwd_ms": round(fwd_ms, 4),
         "bwd_ms": round(bwd_ms, 4),
+        "step_ms_median": round(statistics.median(a + b for a, b in zip(ms_fwd, ms_bwd)), 4),
         "fwd_tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
         "bwd_tflops": round(f_bwd / (bwd_ms * 1e-3) / 1e12, 2),
         "roofline": {
             "kernel": dom,
             "bound": "tensor",
             "achieved": round(dom_fl / (dom_ms * 1e-3) / 1e12, 2),
-            "peak": bf16_sust,
+            "peak": bf16_burst,
             "unit": "TFLOP/s",
-            "frac": round(dom_fl / (dom_ms * 1e-3) / 1e12 / bf16_sust, 4),
-            "peak_kind": f"{peak_kind} bf16 sustained",
+            "frac": round(dom_fl / (dom_ms * 1e-3) / 1e12 / bf16_burst, 4),
+            "peak_kind": f"{peak_kind} bf16 burst (kernels timed in a {ms_total / 1e3:.2f} s region)",
+            "frac_of_sustained": round(dom_fl / (dom_ms * 1e-3) / 1e12 / bf16_sust, 4),
+            "peak_sustained": bf16_sust,
             "traffic": traffic,
         },
         "kernels": per_kernel,

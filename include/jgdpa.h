@@ -233,7 +233,9 @@ JGDPA_API jgdpa_status jgdpa_bwd_ex(const void* q, const void* k, const void* v,
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  No call allocates or frees memory.  All calls
+ * before any stream capture.  The address is kept for the life of the
+ * process, so a device reset (cudaDeviceReset) after the first call on that
+ * device is not supported: later calls would launch on the old address.  No call allocates or frees memory.  All calls
  * on a device share the one array and it keeps the previous call's contents
  * (the parts that must start at zero are cleared on the stream by each call):
  * calls that overlap in time on the GPU -- on different streams, or from
@@ -269,6 +271,20 @@ JGDPA_API const char* jgdpa_status_string(jgdpa_status s);
  */
 JGDPA_API jgdpa_status jgdpa_eval_activation(jgdpa_act act, int32_t path, const float* x, int64_t n,
                                    float* y, float* dy, jgdpa_stream_t stream);
+
+/*
+ * Test hook: sets how long one internal device wait of the kernels may take
+ * before it gives up, for every kernel launched after this call in this
+ * process (any device, any stream); 0 restores the default of 2 s.  A wait
+ * that gives up records JGDPA_ERR_DEVICE_TIMEOUT in the workspace status word;
+ * the CTA then waits (at most 200 ms each) for its copies and tensor-core
+ * operations in flight, releases its Tensor Memory and exits, and the later
+ * kernels of the call do nothing.  A limit of a few nanoseconds makes the
+ * waits of any multi-tile call run out, which is how the timeout path is
+ * tested without faulting or hanging a GPU.  Not thread-safe with respect to
+ * calls in flight on other host threads (they may see either value).
+ */
+JGDPA_API void jgdpa_set_wait_limit_ns(uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

@@ -6,6 +6,8 @@ under csrc/).  This package only builds and binds it.
 
 from ._lib import (  # noqa: F401
     ACT,
+    ALU_LIB_PATH,
+    LIB_PATH,
     EXPORTS,
     JgdpaError,
     jgdpa_bwd,
@@ -14,6 +16,7 @@ from ._lib import (  # noqa: F401
     jgdpa_fwd,
     jgdpa_fwd_noalloc,
     jgdpa_read_device_status,
+    jgdpa_set_wait_limit_ns,
     jgdpa_status_string,
     jgdpa_workspace_bytes,
     load,

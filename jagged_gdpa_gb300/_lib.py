@@ -16,6 +16,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libjgdpa.so")
+# the same library with GELU/SiLU on the ALU-only polynomial route everywhere
+ALU_LIB_PATH = os.path.join(_HERE, "_build", "alu", "libjgdpa.so")
 
 ACT = {"gelu": 0, "silu": 1, "softmax": 2}
 STATUS = {
@@ -25,7 +27,8 @@ STATUS = {
 }
 EXPORTS = ("jgdpa_workspace_bytes", "jgdpa_fwd", "jgdpa_fwd_ex", "jgdpa_bwd", "jgdpa_bwd_ex",
            "jgdpa_ds_scratch_bytes",
-           "jgdpa_read_device_status", "jgdpa_status_string", "jgdpa_eval_activation", "jgdpa_fwd_noalloc")
+           "jgdpa_read_device_status", "jgdpa_status_string", "jgdpa_eval_activation", "jgdpa_fwd_noalloc",
+           "jgdpa_set_wait_limit_ns")
 
 
 class JgdpaError(RuntimeError):
@@ -34,14 +37,14 @@ class JgdpaError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(code, code)}")
 
 
-_lib = None
+_libs: dict = {}
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libjgdpa.so (raises if it has not been built)."""
-    global _lib
-    if _lib is not None:
-        return _lib
+    """Load libjgdpa.so (raises if it has not been built).  Each path is
+    loaded once; the wrappers below take ``lib=`` to use another build."""
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with jagged_gdpa_gb300.build.build()")
     lib = ctypes.CDLL(path)
@@ -70,8 +73,56 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.jgdpa_fwd_noalloc.argtypes = [P, P, P, P, P, i32, i64, i64, i32, i32, ctypes.c_int, f32, P, i32, i32,
                                       P, P, P]
     lib.jgdpa_fwd_noalloc.restype = ctypes.c_int
-    _lib = lib
+    lib.jgdpa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.jgdpa_set_wait_limit_ns.restype = None
+    _libs[path] = lib
     return lib
+
+
+def _check(t, name: str, dtype, shape, device=None, optional: bool = False):
+    """Raise ValueError unless t is a tensor of this dtype and shape (None
+    entries of shape match any size) on `device`.  Run before any pointer is
+    taken: the library builds its TMA maps from the shapes it is given, so a
+    short tensor would be read past its end."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if t.dim() != len(shape) or any(w is not None and g != w for g, w in zip(t.shape, shape)):
+        want = "[" + ", ".join("*" if w is None else str(w) for w in shape) + "]"
+        raise ValueError(f"{name} must have shape {want}, got {list(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _check_common(q, k, v, q_offsets, kv_offsets, bias_table):
+    """Shapes and dtypes shared by the forward and backward wrappers; returns
+    (total_q, heads, head_dim, total_kv, batch, bias_len)."""
+    if not isinstance(q, torch.Tensor) or q.dim() != 3:
+        raise ValueError("q must be a bf16 tensor [total_q, heads, head_dim]")
+    total_q, heads, d = q.shape
+    _check(q, "q", torch.bfloat16, (None, None, None))
+    _check(k, "k", torch.bfloat16, (None, heads, d), q.device)
+    total_kv = k.shape[0]
+    _check(v, "v", torch.bfloat16, (total_kv, heads, d), q.device)
+    _check(q_offsets, "q_offsets", torch.int32, (None,), q.device)
+    batch = q_offsets.numel() - 1
+    if batch < 0:
+        raise ValueError("q_offsets must hold batch + 1 >= 1 entries")
+    _check(kv_offsets, "kv_offsets", torch.int32, (batch + 1,), q.device)
+    _check(bias_table, "bias_table", torch.float32, (heads, None), q.device, optional=True)
+    bias_len = 0 if bias_table is None else int(bias_table.shape[1])
+    return total_q, heads, d, total_kv, batch, bias_len
+
+
+def _check_bytes(t, name: str, device):
+    if t is None:
+        return
+    _check(t, name, torch.uint8, (None,), device)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -89,7 +140,7 @@ def _stream(stream: Optional[torch.cuda.Stream]):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _check(rc: int, where: str):
+def _rc(rc: int, where: str):
     if rc != 0:
         raise JgdpaError(rc, where)
 
@@ -98,14 +149,14 @@ def _act(act) -> int:
     return ACT[act] if isinstance(act, str) else int(act)
 
 
-def jgdpa_status_string(code: int) -> str:
-    return load().jgdpa_status_string(int(code)).decode()
+def jgdpa_status_string(code: int, lib=None) -> str:
+    return (lib or load()).jgdpa_status_string(int(code)).decode()
 
 
 def jgdpa_workspace_bytes(batch: int, total_q: int, total_kv: int, heads: int, head_dim: int, act,
-                          bias_len: int = 0, for_backward: bool = False) -> int:
-    return int(load().jgdpa_workspace_bytes(batch, total_q, total_kv, heads, head_dim, _act(act),
-                                            bias_len, int(bool(for_backward))))
+                          bias_len: int = 0, for_backward: bool = False, lib=None) -> int:
+    return int((lib or load()).jgdpa_workspace_bytes(batch, total_q, total_kv, heads, head_dim, _act(act),
+                                                     bias_len, int(bool(for_backward))))
 
 
 def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
@@ -115,36 +166,41 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.
 
 
 def jgdpa_fwd(q, k, v, q_offsets, kv_offsets, act, scale: float, bias_table=None, causal: bool = False,
-              out=None, lse=None, workspace=None, stream=None, window: int = 0):
+              out=None, lse=None, workspace=None, stream=None, window: int = 0, lib=None):
     """Forward pass; returns (out, lse) with lse None unless act == 'softmax'.
-    window > 0 takes the sliding-window entry point (jgdpa_fwd_ex)."""
-    lib = load()
-    total_q, heads, d = q.shape
-    total_kv = k.shape[0]
-    batch = q_offsets.numel() - 1
+    window > 0 takes the sliding-window entry point (jgdpa_fwd_ex).  Shapes
+    and dtypes are checked here (ValueError) before the library sees any
+    pointer."""
+    lib = lib or load()
+    total_q, heads, d, total_kv, batch, bias_len = _check_common(q, k, v, q_offsets, kv_offsets, bias_table)
     a = _act(act)
-    bias_len = 0 if bias_table is None else int(bias_table.shape[1])
     if out is None:
         out = torch.empty_like(q)
     if lse is None and a == ACT["softmax"]:
         lse = torch.empty((heads, total_q), dtype=torch.float32, device=q.device)
-    nbytes = jgdpa_workspace_bytes(batch, total_q, total_kv, heads, d, a, bias_len, False)
+    _check(out, "out", torch.bfloat16, (total_q, heads, d), q.device)
+    if a == ACT["softmax"]:
+        _check(lse, "lse", torch.float32, (heads, total_q), q.device)
+    elif lse is not None:
+        raise ValueError("lse is written in softmax mode only; pass None")
+    _check_bytes(workspace, "workspace", q.device)
+    nbytes = jgdpa_workspace_bytes(batch, total_q, total_kv, heads, d, a, bias_len, False, lib=lib)
     ws = _workspace(nbytes, q.device, workspace)
     head = (_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(kv_offsets), batch, total_q, total_kv, heads, d,
             a, float(scale), _ptr(bias_table), bias_len, int(bool(causal)))
     tail = (_ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     if window:
         rc = lib.jgdpa_fwd_ex(*head, int(window), *tail)
-        _check(rc, "jgdpa_fwd_ex")
+        _rc(rc, "jgdpa_fwd_ex")
     else:
         rc = lib.jgdpa_fwd(*head, *tail)
-        _check(rc, "jgdpa_fwd")
+        _rc(rc, "jgdpa_fwd")
     return out, lse
 
 
-def jgdpa_ds_scratch_bytes(q_offsets, kv_offsets, heads: int, window: int = 0) -> int:
+def jgdpa_ds_scratch_bytes(q_offsets, kv_offsets, heads: int, window: int = 0, lib=None) -> int:
     """Stored-dS scratch bytes for these offsets (copied to the host here)."""
-    lib = load()
+    lib = lib or load()
     qo = q_offsets.detach().to("cpu", torch.int32).contiguous()
     ko = kv_offsets.detach().to("cpu", torch.int32).contiguous()
     return int(lib.jgdpa_ds_scratch_bytes(qo.data_ptr(), ko.data_ptr(), qo.numel() - 1, int(heads), int(window)))
@@ -152,26 +208,41 @@ def jgdpa_ds_scratch_bytes(q_offsets, kv_offsets, heads: int, window: int = 0) -
 
 def jgdpa_bwd(q, k, v, out, lse, dout, q_offsets, kv_offsets, act, scale: float, bias_table=None,
               causal: bool = False, dq=None, dk=None, dv=None, dbias=None, want_dbias: bool = True,
-              workspace=None, stream=None, ds_scratch=None, pass_events=None, window: int = 0):
+              workspace=None, stream=None, ds_scratch=None, pass_events=None, window: int = 0, lib=None):
     """Backward pass; returns (dq, dk, dv, dbias) with dbias None without a bias table.
 
     ds_scratch: optional uint8 device tensor of at least jgdpa_ds_scratch_bytes
     bytes -- selects the stored-dS backward (jgdpa_bwd_ex).  pass_events:
     optional three torch.cuda.Event (timing enabled, already recorded once),
     recorded before the dK/dV pass, between the passes and after the dQ pass.
-    window: the forward's sliding window (jgdpa_bwd_ex); 0 for none."""
-    lib = load()
-    total_q, heads, d = q.shape
-    total_kv = k.shape[0]
-    batch = q_offsets.numel() - 1
+    window: the forward's sliding window (jgdpa_bwd_ex); 0 for none.  Shapes
+    and dtypes are checked here (ValueError) before the library sees any
+    pointer."""
+    lib = lib or load()
+    total_q, heads, d, total_kv, batch, bias_len = _check_common(q, k, v, q_offsets, kv_offsets, bias_table)
     a = _act(act)
-    bias_len = 0 if bias_table is None else int(bias_table.shape[1])
+    _check(dout, "dout", torch.bfloat16, (total_q, heads, d), q.device)
+    if a == ACT["softmax"]:
+        _check(out, "out", torch.bfloat16, (total_q, heads, d), q.device)
+        _check(lse, "lse", torch.float32, (heads, total_q), q.device)
+    else:
+        _check(out, "out", torch.bfloat16, (total_q, heads, d), q.device, optional=True)
+        _check(lse, "lse", torch.float32, (heads, total_q), q.device, optional=True)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     if dbias is None and bias_len and want_dbias:
         dbias = torch.empty((heads, bias_len), dtype=torch.float32, device=q.device)
-    nbytes = jgdpa_workspace_bytes(batch, total_q, total_kv, heads, d, a, bias_len, True)
+    _check(dq, "dq", torch.bfloat16, (total_q, heads, d), q.device)
+    _check(dk, "dk", torch.bfloat16, (total_kv, heads, d), q.device)
+    _check(dv, "dv", torch.bfloat16, (total_kv, heads, d), q.device)
+    if dbias is not None:
+        if not bias_len:
+            raise ValueError("dbias needs a bias table")
+        _check(dbias, "dbias", torch.float32, (heads, bias_len), q.device)
+    _check_bytes(workspace, "workspace", q.device)
+    _check_bytes(ds_scratch, "ds_scratch", q.device)
+    nbytes = jgdpa_workspace_bytes(batch, total_q, total_kv, heads, d, a, bias_len, True, lib=lib)
     ws = _workspace(nbytes, q.device, workspace)
     head = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(q_offsets),
             _ptr(kv_offsets), batch, total_q, total_kv, heads, d, a, float(scale),
@@ -179,48 +250,57 @@ def jgdpa_bwd(q, k, v, out, lse, dout, q_offsets, kv_offsets, act, scale: float,
     tail = (_ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(ws), ws.numel())
     if ds_scratch is None and pass_events is None and not window:
         rc = lib.jgdpa_bwd(*head, *tail, _stream(stream))
-        _check(rc, "jgdpa_bwd")
+        _rc(rc, "jgdpa_bwd")
     else:
         ev = None
         if pass_events is not None:
             ev = (ctypes.c_void_p * 3)(*[None if e is None else e.cuda_event for e in pass_events])
         rc = lib.jgdpa_bwd_ex(*head, int(window), *tail, _ptr(ds_scratch),
                               0 if ds_scratch is None else ds_scratch.numel(), _stream(stream), ev)
-        _check(rc, "jgdpa_bwd_ex")
+        _rc(rc, "jgdpa_bwd_ex")
     return dq, dk, dv, dbias
 
 
 def jgdpa_fwd_noalloc(q, k, v, q_offsets, kv_offsets, act, scale: float, bias_table=None,
-                      causal: bool = False, out=None, lse=None, stream=None):
+                      causal: bool = False, out=None, lse=None, stream=None, lib=None):
     """Forward pass using the library's built-in scratch (no workspace
     argument; for callers that cannot allocate device memory at call time).
     out / lse must be passed by such callers; they are created here only for
     convenience when omitted.  Returns (out, lse)."""
-    lib = load()
-    total_q, heads, d = q.shape
+    lib = lib or load()
+    total_q, heads, d, total_kv, batch, bias_len = _check_common(q, k, v, q_offsets, kv_offsets, bias_table)
     a = _act(act)
-    bias_len = 0 if bias_table is None else int(bias_table.shape[1])
     if out is None:
         out = torch.empty_like(q)
     if lse is None and a == ACT["softmax"]:
         lse = torch.empty((heads, total_q), dtype=torch.float32, device=q.device)
+    _check(out, "out", torch.bfloat16, (total_q, heads, d), q.device)
+    if a == ACT["softmax"]:
+        _check(lse, "lse", torch.float32, (heads, total_q), q.device)
     rc = lib.jgdpa_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(kv_offsets),
                                q_offsets.numel() - 1, total_q, k.shape[0], heads, d, a, float(scale),
                                _ptr(bias_table), bias_len, int(bool(causal)), _ptr(out), _ptr(lse),
                                _stream(stream))
-    _check(rc, "jgdpa_fwd_noalloc")
+    _rc(rc, "jgdpa_fwd_noalloc")
     return out, lse
 
 
-def jgdpa_read_device_status(workspace, stream=None) -> int:
-    return int(load().jgdpa_read_device_status(_ptr(workspace), _stream(stream)))
+def jgdpa_read_device_status(workspace, stream=None, lib=None) -> int:
+    return int((lib or load()).jgdpa_read_device_status(_ptr(workspace), _stream(stream)))
 
 
-def jgdpa_eval_activation(act, x, path: int = 0, stream=None):
+def jgdpa_eval_activation(act, x, path: int = 0, stream=None, lib=None):
     """Device act(x), act'(x) for fp32 x (test hook); path 0 = SFU route, 1 = ALU route."""
+    _check(x, "x", torch.float32, (None,))
     y = torch.empty_like(x)
     dy = torch.empty_like(x)
-    rc = load().jgdpa_eval_activation(_act(act), int(path), _ptr(x), x.numel(), _ptr(y), _ptr(dy),
+    rc = (lib or load()).jgdpa_eval_activation(_act(act), int(path), _ptr(x), x.numel(), _ptr(y), _ptr(dy),
                                       _stream(stream))
-    _check(rc, "jgdpa_eval_activation")
+    _rc(rc, "jgdpa_eval_activation")
     return y, dy
+
+
+def jgdpa_set_wait_limit_ns(limit_ns: int, lib=None) -> None:
+    """Test hook: limit of one internal device wait for later launches (0 =
+    the default of 2 s)."""
+    (lib or load()).jgdpa_set_wait_limit_ns(int(limit_ns))

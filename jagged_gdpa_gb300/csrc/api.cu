@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -12,16 +13,48 @@
 #include "../../include/jgdpa.h"
 #include "act.cuh"
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace jg {
-cudaError_t launch_fwd(const FwdParams& p, int head_dim, int act, int grid, cudaStream_t stream);
-cudaError_t launch_bwd_pass(const BwdParams& p, int head_dim, int act, bool kv_major, int grid,
-                            cudaStream_t stream);
-cudaError_t launch_softmax_delta(const void* out, const void* dout, float* delta, int64_t total_q, int heads,
-                                 int head_dim, const int* status, cudaStream_t stream);
-cudaError_t launch_dbias_reduce(const float* part, float* dbias, int n_parts, int n, cudaStream_t stream);
+// Per-head-dimension launchers, one object file per head dimension.
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, int act, int grid, cudaStream_t stream);
+template <int D>
+cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream);
+template <int D>
+cudaError_t launch_dq_ds_d(const BwdParams& p, int grid, cudaStream_t stream);
+template <int D>
+cudaError_t launch_softmax_delta_d(const void* out, const void* dout, float* delta, int64_t total_q, int heads,
+                                   const int* status, cudaStream_t stream);
+cudaError_t launch_dbias_reduce(const unsigned long long* part, float* dbias, int n_parts, int n,
+                                cudaStream_t stream);
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t stream);
-cudaError_t launch_dq_ds(const BwdParams& p, int head_dim, int grid, cudaStream_t stream);
+
+cudaError_t launch_fwd(const FwdParams& p, int head_dim, int act, int grid, cudaStream_t stream) {
+  if (head_dim == 128) return launch_fwd_d<128>(p, act, grid, stream);
+  if (head_dim == 64) return launch_fwd_d<64>(p, act, grid, stream);
+  if (head_dim == 32) return launch_fwd_d<32>(p, act, grid, stream);
+  return cudaErrorInvalidValue;
+}
+cudaError_t launch_bwd_pass(const BwdParams& p, int head_dim, int act, bool kv_major, int grid,
+                            cudaStream_t stream) {
+  if (head_dim == 128) return launch_bwd_pass_d<128>(p, act, kv_major, grid, stream);
+  if (head_dim == 64) return launch_bwd_pass_d<64>(p, act, kv_major, grid, stream);
+  if (head_dim == 32) return launch_bwd_pass_d<32>(p, act, kv_major, grid, stream);
+  return cudaErrorInvalidValue;
+}
+cudaError_t launch_dq_ds(const BwdParams& p, int head_dim, int grid, cudaStream_t stream) {
+  if (head_dim == 128) return launch_dq_ds_d<128>(p, grid, stream);
+  if (head_dim == 64) return launch_dq_ds_d<64>(p, grid, stream);
+  if (head_dim == 32) return launch_dq_ds_d<32>(p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+cudaError_t launch_softmax_delta(const void* out, const void* dout, float* delta, int64_t total_q, int heads,
+                                 int head_dim, const int* status, cudaStream_t stream) {
+  if (head_dim == 128) return launch_softmax_delta_d<128>(out, dout, delta, total_q, heads, status, stream);
+  if (head_dim == 64) return launch_softmax_delta_d<64>(out, dout, delta, total_q, heads, status, stream);
+  return launch_softmax_delta_d<32>(out, dout, delta, total_q, heads, status, stream);
+}
 }  // namespace jg
 
 namespace {
@@ -30,6 +63,14 @@ using jg::kTile;
 
 constexpr size_t kAlign = 256;
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Limit of one internal device wait for the kernels launched from now on
+// (jgdpa_set_wait_limit_ns; 0 = the default).
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+unsigned long long wait_limit_ns() {
+  const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : jg::kWaitLimitNs;
+}
 
 // ----------------------------------------------------------- device facts
 int sm_count() {
@@ -104,7 +145,7 @@ struct Layout {
   size_t units0 = 0;      // fwd units, or dkdv units
   size_t units1 = 0;      // dq units (bwd)
   size_t delta = 0;       // softmax bwd: [H][total_q]
-  size_t dbias = 0;       // bwd with dbias: [grid][H][T]
+  size_t dbias = 0;       // bwd with dbias: [grid][H][T] 64-bit fixed-point partial sums
   size_t ds_base = 0;     // bwd: first stored-dS tile per segment, int64 [batch + 1]
   size_t total = 0;
   int max0 = 0, max1 = 0;
@@ -142,7 +183,7 @@ bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
   L->delta = off;
   if (bwd && act == JGDPA_ACT_SOFTMAX) off += up(static_cast<size_t>(heads) * total_q * sizeof(float));
   L->dbias = off;
-  if (bwd && bias_len > 0) off += up(static_cast<size_t>(sms) * heads * bias_len * sizeof(float));
+  if (bwd && bias_len > 0) off += up(static_cast<size_t>(sms) * heads * bias_len * sizeof(unsigned long long));
   L->ds_base = off;
   if (bwd) off += up((static_cast<size_t>(batch) + 1) * sizeof(int64_t));
   L->total = off;
@@ -318,6 +359,7 @@ jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t
   p.causal = causal;
   p.window = window;
   p.scale = act == JGDPA_ACT_SOFTMAX ? scale * jg::kLog2e : scale;
+  p.wait_limit_ns = wait_limit_ns();
   const int grid = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max0)));
   JG_CUDA(jg::launch_fwd(p, head_dim, act, grid, stream));
   return JGDPA_OK;
@@ -425,13 +467,15 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   p.causal = causal;
   p.window = window;
   p.scale = scale;
+  p.wait_limit_ns = wait_limit_ns();
   if (act == JGDPA_ACT_SOFTMAX)
     JG_CUDA(jg::launch_softmax_delta(out, dout, const_cast<float*>(p.delta), total_q, heads, head_dim, hdr,
                                      stream));
   const int grid_kv = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max0)));
   const int grid_q = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max1)));
-  float* part = dbias ? reinterpret_cast<float*>(ws + L.dbias) : nullptr;
-  if (part) JG_CUDA(cudaMemsetAsync(part, 0, static_cast<size_t>(grid_kv) * heads * bias_len * sizeof(float), stream));
+  auto* part = dbias ? reinterpret_cast<unsigned long long*>(ws + L.dbias) : nullptr;
+  if (part)
+    JG_CUDA(cudaMemsetAsync(part, 0, static_cast<size_t>(grid_kv) * heads * bias_len * sizeof(*part), stream));
   p.dbias_part = part;
   p.units = reinterpret_cast<const jg::Unit*>(ws + L.units0);
   p.n_units = hdr + 1;
@@ -513,6 +557,8 @@ const char* jgdpa_status_string(jgdpa_status s) {
   }
   return "unknown status";
 }
+
+void jgdpa_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed); }
 
 jgdpa_status jgdpa_eval_activation(jgdpa_act act, int32_t path, const float* x, int64_t n, float* y, float* dy,
                                    jgdpa_stream_t stream_) {

@@ -677,7 +677,8 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     const bool row_ok = r < u.rows;
     const int64_t grow = static_cast<int64_t>(KV_MAJOR ? u.seg.k0 : u.seg.q0) + u.tile * kTile + r;
     const float* brow = p.bias_len ? p.bias + static_cast<int64_t>(u.h) * p.bias_len : nullptr;
-    float* part = want_dbias ? p.dbias_part + (static_cast<int64_t>(blockIdx.x) * H + u.h) * p.bias_len : nullptr;
+    unsigned long long* part =
+        want_dbias ? p.dbias_part + (static_cast<int64_t>(blockIdx.x) * H + u.h) * p.bias_len : nullptr;
     float acc_lo = 0.f, acc_hi = 0.f;  // dbias mass clamped to the table's ends
     const float bc_lo = brow ? __ldg(brow) : 0.f, bc_hi = brow ? __ldg(brow + 2 * R) : 0.f;
 
@@ -853,7 +854,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
           const int rel = rel1 + 32 * (k - 1);
           if (rel >= R) acc_hi += dacc[k];
           else if (rel <= -R) acc_lo += dacc[k];
-          else atomicAdd(part + rel + R, dacc[k]);
+          else atomicAdd(part + rel + R, dbias_fixed(dacc[k]));
         }
       }
     }
@@ -953,16 +954,16 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     mbar_arrive_warp(&bars->acc_empty);
 
     if (want_dbias) {
-      // the clamped mass of this unit: one red per warp and table end into
-      // this CTA's private slice
+      // the clamped mass of this unit: one fixed-point red per warp and table
+      // end into this CTA's private slice
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         acc_lo += __shfl_xor_sync(0xffffffffu, acc_lo, o);
         acc_hi += __shfl_xor_sync(0xffffffffu, acc_hi, o);
       }
       if ((threadIdx.x & 31) == 0) {
-        atomicAdd(part, acc_lo);
-        atomicAdd(part + 2 * R, acc_hi);
+        atomicAdd(part, dbias_fixed(acc_lo));
+        atomicAdd(part + 2 * R, dbias_fixed(acc_hi));
       }
     }
   }
@@ -1013,7 +1014,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
   const uint32_t tmem = bars->tmem_base;
   int n_units = *p.n_units;
   if (*reinterpret_cast<volatile int*>(p.status) != kOk) n_units = 0;
-  Fail fail{&bars->abort, p.status};
+  Fail fail{&bars->abort, p.status, p.wait_limit_ns};
   if (warp == 0) {
     bwd_producer<D, KV_MAJOR, 0, WIN>(p, smem, bars, n_units, fail);
   } else if (warp == 2) {
@@ -1091,7 +1092,7 @@ __global__ void __launch_bounds__(256, 1) gdpa_dq_ds_kernel(const __grid_constan
   const uint32_t tmem = bars->tmem_base;
   int n_units = *p.n_units;
   if (*reinterpret_cast<volatile int*>(p.status) != kOk) n_units = 0;
-  Fail fail{&bars->abort, p.status};
+  Fail fail{&bars->abort, p.status, p.wait_limit_ns};
 
   if (warp == 0) {  // ---- producer
     const bool leader = elect_one();
@@ -1235,16 +1236,28 @@ __global__ void softmax_delta_kernel(const __nv_bfloat16* __restrict__ out, cons
   delta[h * total_q + t] = acc;
 }
 
-// dbias[h][e] = sum over CTAs of the per-CTA partial sums, in CTA order.
-__global__ void dbias_reduce_kernel(const float* __restrict__ part, float* __restrict__ dbias, int n_parts, int n) {
+#if JGDPA_HEAD_DIM == 128
+// dbias[h][e] = sum over CTAs of the per-CTA fixed-point partial sums
+// (exact integer additions), converted to fp32 once.
+__global__ void dbias_reduce_kernel(const unsigned long long* __restrict__ part, float* __restrict__ dbias,
+                                    int n_parts, int n) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n) return;
-  float acc = 0.f;
+  unsigned long long acc = 0;
   for (int c = 0; c < n_parts; ++c) acc += part[static_cast<int64_t>(c) * n + e];
-  dbias[e] = acc;
+  dbias[e] = static_cast<float>(static_cast<double>(static_cast<long long>(acc)) *
+                                (1.0 / static_cast<double>(1ll << kDbiasFracBits)));
 }
+#endif
 
 // ------------------------------------------------------------------- launch
+// Each object file holds the kernels of one head dimension (JGDPA_HEAD_DIM),
+// so that the build compiles the head dimensions in parallel; the
+// head-dimension-free dbias reduction lives in the d = 128 object.
+#ifndef JGDPA_HEAD_DIM
+#error "compile bwd.cu with -DJGDPA_HEAD_DIM=32, 64 or 128"
+#endif
+
 template <int D, int ACT, bool KV_MAJOR>
 static cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t stream) {
   using C = BwdCfg<D, KV_MAJOR>;
@@ -1255,28 +1268,21 @@ static cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t strea
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pass(const BwdParams& p, int head_dim, int act, bool kv_major, int grid,
-                            cudaStream_t stream) {
-#define JG_BWD_CASE(DD)                                                                         \
-  if (head_dim == DD) {                                                                         \
-    if (kv_major) {                                                                             \
-      if (act == 0) return launch_bwd_t<DD, 0, true>(p, grid, stream);                          \
-      if (act == 1) return launch_bwd_t<DD, 1, true>(p, grid, stream);                          \
-      return launch_bwd_t<DD, 2, true>(p, grid, stream);                                        \
-    }                                                                                           \
-    if (act == 0) return launch_bwd_t<DD, 0, false>(p, grid, stream);                           \
-    if (act == 1) return launch_bwd_t<DD, 1, false>(p, grid, stream);                           \
-    return launch_bwd_t<DD, 2, false>(p, grid, stream);                                         \
+template <int D>
+cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream) {
+  if (kv_major) {
+    if (act == 0) return launch_bwd_t<D, 0, true>(p, grid, stream);
+    if (act == 1) return launch_bwd_t<D, 1, true>(p, grid, stream);
+    return launch_bwd_t<D, 2, true>(p, grid, stream);
   }
-  JG_BWD_CASE(128)
-  JG_BWD_CASE(64)
-  JG_BWD_CASE(32)
-#undef JG_BWD_CASE
-  return cudaErrorInvalidValue;
+  if (act == 0) return launch_bwd_t<D, 0, false>(p, grid, stream);
+  if (act == 1) return launch_bwd_t<D, 1, false>(p, grid, stream);
+  return launch_bwd_t<D, 2, false>(p, grid, stream);
 }
+template cudaError_t launch_bwd_pass_d<JGDPA_HEAD_DIM>(const BwdParams&, int, bool, int, cudaStream_t);
 
 template <int D>
-static cudaError_t launch_dq_ds_t(const BwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_dq_ds_d(const BwdParams& p, int grid, cudaStream_t stream) {
   using C = DqCfg<D>;
   auto kern = gdpa_dq_ds_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -1284,32 +1290,30 @@ static cudaError_t launch_dq_ds_t(const BwdParams& p, int grid, cudaStream_t str
   kern<<<grid, 256, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
+template cudaError_t launch_dq_ds_d<JGDPA_HEAD_DIM>(const BwdParams&, int, cudaStream_t);
 
-cudaError_t launch_dq_ds(const BwdParams& p, int head_dim, int grid, cudaStream_t stream) {
-  if (head_dim == 128) return launch_dq_ds_t<128>(p, grid, stream);
-  if (head_dim == 64) return launch_dq_ds_t<64>(p, grid, stream);
-  if (head_dim == 32) return launch_dq_ds_t<32>(p, grid, stream);
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_softmax_delta(const void* out, const void* dout, float* delta, int64_t total_q, int heads,
-                                 int head_dim, const int* status, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_softmax_delta_d(const void* out, const void* dout, float* delta, int64_t total_q, int heads,
+                                   const int* status, cudaStream_t stream) {
   const int64_t rows = total_q * heads;
   if (rows == 0) return cudaSuccess;
   const int threads = 256;
   const unsigned blocks = static_cast<unsigned>((rows + threads - 1) / threads);
-  const auto* o = static_cast<const __nv_bfloat16*>(out);
-  const auto* d = static_cast<const __nv_bfloat16*>(dout);
-  if (head_dim == 128) softmax_delta_kernel<128><<<blocks, threads, 0, stream>>>(o, d, delta, total_q, heads, status);
-  else if (head_dim == 64) softmax_delta_kernel<64><<<blocks, threads, 0, stream>>>(o, d, delta, total_q, heads, status);
-  else softmax_delta_kernel<32><<<blocks, threads, 0, stream>>>(o, d, delta, total_q, heads, status);
+  softmax_delta_kernel<D><<<blocks, threads, 0, stream>>>(static_cast<const __nv_bfloat16*>(out),
+                                                          static_cast<const __nv_bfloat16*>(dout), delta, total_q,
+                                                          heads, status);
   return cudaGetLastError();
 }
+template cudaError_t launch_softmax_delta_d<JGDPA_HEAD_DIM>(const void*, const void*, float*, int64_t, int,
+                                                            const int*, cudaStream_t);
 
-cudaError_t launch_dbias_reduce(const float* part, float* dbias, int n_parts, int n, cudaStream_t stream) {
+#if JGDPA_HEAD_DIM == 128
+cudaError_t launch_dbias_reduce(const unsigned long long* part, float* dbias, int n_parts, int n,
+                                cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
   dbias_reduce_kernel<<<(n + 255) / 256, 256, 0, stream>>>(part, dbias, n_parts, n);
   return cudaGetLastError();
 }
+#endif
 
 }  // namespace jg

@@ -115,6 +115,7 @@ struct FwdParams {
   int32_t causal;
   int32_t window;         // > 0: sliding window |i - j| < window
   float scale;            // s (GELU/SiLU) or s * log2(e) (softmax)
+  unsigned long long wait_limit_ns;  // limit of one internal wait
 };
 
 struct BwdParams {
@@ -133,7 +134,7 @@ struct BwdParams {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* dbias_part;       // [gridDim.x][H][bias_len] per-CTA partial sums, or nullptr
+  unsigned long long* dbias_part;  // [gridDim.x][H][bias_len] per-CTA fixed-point partial sums, or nullptr
   int64_t total_q;
   int32_t heads;
   int32_t bias_len;
@@ -146,9 +147,20 @@ struct BwdParams {
   // slot (see ds_span / ds_slot).
   CUtensorMap tm_ds;       // 2-D over the scratch: 128 columns x (tiles * 128) rows
   const int64_t* ds_base;  // nullptr: no stored dS
+  unsigned long long wait_limit_ns;  // limit of one internal wait
 };
 
 constexpr int kDsTileBytes = kTile * kTile * 2;
+
+// dbias partial sums are 64-bit two's-complement fixed point with this many
+// fraction bits (resolution 2^-24, range +-2^39).  Integer additions are exact
+// and commute, so the sums do not depend on the order in which the CTAs' warps
+// add their contributions or on which CTA ran which unit: dbias is the same
+// bit for bit on every run.
+constexpr int kDbiasFracBits = 24;
+__device__ __forceinline__ unsigned long long dbias_fixed(float v) {
+  return static_cast<unsigned long long>(__float2ll_rn(v * static_cast<float>(1 << kDbiasFracBits)));
+}
 
 // Stored-dS slots per key tile of a segment with nq query tiles: nq, or
 // under a window short enough to pay, the 2e + 1 query tiles kt - e .. kt + e

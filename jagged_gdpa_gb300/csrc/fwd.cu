@@ -138,7 +138,8 @@ template <int D, bool WIN>
 __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, int n_units, Fail fail) {
   using C = FwdCfg<D>;
   uint32_t q_it[2] = {0, 0};
-  uint32_t kv_it = 0;
+  uint32_t kv_it = 0;  // K/V stream positions whose V load was issued
+  uint32_t k_it = 0;   // K loads issued (one ahead of kv_it if a V wait failed)
   const bool leader = elect_one();
   bool ok = true;
   for (int r = 0;; ++r) {
@@ -174,6 +175,7 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
         for (int cb = 0; cb < C::kNumBlocks; ++cb)
           tma_load_3d(kd + cb * C::kBlockBytes, &p.tm_k, &bars->k_full[st], cb * C::kBlockCols, u.h, row);
       }
+      ++k_it;
       if (!(ok = mbar_wait_warp(&bars->v_empty[st], empty_phase, fail))) break;
       if (leader) {
         mbar_arrive_tx(&bars->v_full[st], C::kTileBytes);
@@ -190,10 +192,10 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
     // Let copies already issued land before the CTA exits.
     for (int s = 0; s < 2; ++s)
       if (q_it[s]) mbar_wait_drain(&bars->q_full[s], (q_it[s] - 1) & 1);
-    for (uint32_t i = kv_it > C::kStages ? kv_it - C::kStages : 0; i < kv_it; ++i) {
+    for (uint32_t i = k_it > C::kStages ? k_it - C::kStages : 0; i < k_it; ++i)
       mbar_wait_drain(&bars->k_full[i % C::kStages], (i / C::kStages) & 1);
+    for (uint32_t i = kv_it > C::kStages ? kv_it - C::kStages : 0; i < kv_it; ++i)
       mbar_wait_drain(&bars->v_full[i % C::kStages], (i / C::kStages) & 1);
-    }
   }
 }
 
@@ -677,7 +679,7 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   const uint32_t tmem = bars->tmem_base;
   int n_units = *p.n_units;
   if (*reinterpret_cast<volatile int*>(p.status) != kOk) n_units = 0;
-  Fail fail{&bars->abort, p.status};
+  Fail fail{&bars->abort, p.status, p.wait_limit_ns};
 
   if (warp == 0) {
     fwd_producer<D, WIN>(p, smem, bars, n_units, fail);
@@ -693,6 +695,12 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
 }
 
 // ------------------------------------------------------------------ launch
+// Each object file holds the kernels of one head dimension (JGDPA_HEAD_DIM),
+// so that the build compiles the head dimensions in parallel.
+#ifndef JGDPA_HEAD_DIM
+#error "compile fwd.cu with -DJGDPA_HEAD_DIM=32, 64 or 128"
+#endif
+
 template <int D, int ACT>
 static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
   auto kern = p.window > 0 ? gdpa_fwd_kernel<D, ACT, kFwdAluChunks, true> : gdpa_fwd_kernel<D, ACT, kFwdAluChunks, false>;
@@ -703,18 +711,12 @@ static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t strea
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int head_dim, int act, int grid, cudaStream_t stream) {
-#define JG_FWD_CASE(DD)                                              \
-  if (head_dim == DD) {                                              \
-    if (act == 0) return launch_fwd_t<DD, 0>(p, grid, stream);       \
-    if (act == 1) return launch_fwd_t<DD, 1>(p, grid, stream);       \
-    return launch_fwd_t<DD, 2>(p, grid, stream);                     \
-  }
-  JG_FWD_CASE(128)
-  JG_FWD_CASE(64)
-  JG_FWD_CASE(32)
-#undef JG_FWD_CASE
-  return cudaErrorInvalidValue;
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, int act, int grid, cudaStream_t stream) {
+  if (act == 0) return launch_fwd_t<D, 0>(p, grid, stream);
+  if (act == 1) return launch_fwd_t<D, 1>(p, grid, stream);
+  return launch_fwd_t<D, 2>(p, grid, stream);
 }
+template cudaError_t launch_fwd_d<JGDPA_HEAD_DIM>(const FwdParams&, int, int, cudaStream_t);
 
 }  // namespace jg

@@ -12,8 +12,9 @@ namespace jg {
 // Status codes shared with the C ABI (same values as jgdpa_status).
 enum : int { kOk = 0, kErrScratchTooSmall = 4, kErrBadOffsets = 6, kErrTimeout = 7 };
 
-// A single wait gives up after this long; no legitimate wait in these kernels
-// comes anywhere near it.
+// By default a single wait gives up after this long; no legitimate wait in
+// these kernels comes anywhere near it.  The launcher passes the limit in the
+// kernel parameters (a test hook can shorten it).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // While shutting down after a failure, waits for copies in flight are shorter.
 constexpr unsigned long long kDrainLimitNs = 200000000ull;
@@ -56,8 +57,9 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
 
 // Per-CTA failure state: `abort` lives in shared memory, `status` in global.
 struct Fail {
-  volatile int* abort;  // shared: nonzero once any role of this CTA gave up
-  int* status;          // global status word of the workspace
+  volatile int* abort;          // shared: nonzero once any role of this CTA gave up
+  int* status;                  // global status word of the workspace
+  unsigned long long limit_ns;  // how long one wait may take
 };
 
 // Wait for completion of the phase with the given parity; false = gave up.
@@ -66,12 +68,14 @@ struct Fail {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Fail f) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
+  // a short limit (the test hook) is checked after every try
+  const int tries = f.limit_ns < 1000000ull ? 1 : 64;
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < tries; ++i)
       if (mbar_try(bar, parity)) return true;
     if (*f.abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > f.limit_ns) {
       *f.abort = 1;
       atomicCAS(f.status, kOk, kErrTimeout);
       return false;

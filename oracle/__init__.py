@@ -52,6 +52,9 @@ def _load():
         lib.oracle_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32, i32, i32,
                                    P, i32, i32, P, P, P, P]
         lib.oracle_bwd.restype = ctypes.c_int
+        lib.oracle_bwd_rows.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, i32, i32,
+                                        i32, i32, P, i32, P, i32, i32, P, P, P]
+        lib.oracle_bwd_rows.restype = ctypes.c_int
         lib.oracle_act_eval.argtypes = [i32, P, i64, P, P]
         lib.oracle_act_eval.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -121,7 +124,7 @@ def fwd(q, k, v, q_offsets, kv_offsets, heads: int, head_dim: int, act: str, sca
                             int(bool(causal)), int(window), int(q_shared), _ptr(u), nu, int(threads),
                             _ptr(out), _ptr(lse))
     if rc:
-        raise ValueError("oracle_fwd rejected its arguments")
+        raise ValueError("oracle_fwd rejected its arguments" if rc == 1 else "oracle_fwd: out of memory")
     return out, lse
 
 
@@ -146,8 +149,35 @@ def bwd(q, k, v, dout, q_offsets, kv_offsets, heads: int, head_dim: int, act: st
                             int(threads),
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias))
     if rc:
-        raise ValueError("oracle_bwd rejected its arguments")
+        raise ValueError("oracle_bwd rejected its arguments" if rc == 1 else "oracle_bwd: out of memory")
     return dq, dk, dv, dbias
+
+
+def bwd_rows(q, k, v, dout, q_offsets, kv_offsets, heads: int, head_dim: int, act: str,
+             scale: float, segment: int, head: int, q_rows, kv_rows, bias=None,
+             causal: bool = False, window: int = 0, threads: int = 0):
+    """The backward of one (segment, head) unit restricted to some of its rows:
+    dQ of the segment-local query rows ``q_rows`` ([n_q, d]) and dK, dV of the
+    key rows ``kv_rows`` ([n_kv, d]), equal to those rows of ``bwd``.  The work
+    is O(rows x partner length), spread over threads, so single rows of very
+    long segments can be checked."""
+    qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(dout)
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    bf = None if bias is None else _f64(bias)
+    bias_len = 0 if bf is None else int(bf.shape[1])
+    qr = np.ascontiguousarray(q_rows, dtype=np.int32)
+    kr = np.ascontiguousarray(kv_rows, dtype=np.int32)
+    dq = np.full((qr.size, head_dim), np.nan)
+    dk = np.full((kr.size, head_dim), np.nan)
+    dv = np.full((kr.size, head_dim), np.nan)
+    rc = _load().oracle_bwd_rows(_ptr(qf), _ptr(kf), _ptr(vf), _ptr(dof), _ptr(qo), _ptr(ko),
+                                 len(qo) - 1, heads, head_dim, ACT_CODE[act], float(scale), _ptr(bf),
+                                 bias_len, int(bool(causal)), int(window), int(segment), int(head),
+                                 _ptr(qr), int(qr.size), _ptr(kr), int(kr.size), int(threads),
+                                 _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc:
+        raise ValueError("oracle_bwd_rows rejected its arguments" if rc == 1 else "oracle_bwd_rows: out of memory")
+    return dq, dk, dv
 
 
 def fwd_inputs(x, units=None, threads: int = 0):
@@ -160,3 +190,10 @@ def bwd_inputs(x, units=None, threads: int = 0):
     """``bwd`` on a ``workloads.Inputs`` bundle."""
     return bwd(x.q, x.k, x.v, x.dout, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, x.act,
                x.scale, bias=x.bias, causal=x.causal, units=units, threads=threads, window=x.window)
+
+
+def bwd_rows_inputs(x, segment: int, head: int, q_rows, kv_rows, threads: int = 0):
+    """``bwd_rows`` on a ``workloads.Inputs`` bundle."""
+    return bwd_rows(x.q, x.k, x.v, x.dout, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, x.act,
+                    x.scale, segment, head, q_rows, kv_rows, bias=x.bias, causal=x.causal,
+                    window=x.window, threads=threads)

@@ -145,45 +145,77 @@ static double logit(const problem* p, int32_t b, int32_t h, int64_t i, int64_t j
     return x;
 }
 
-/* Forward of one (segment, head) unit: O rows and LSE of that unit. */
-static void fwd_unit(const problem* p, int32_t b, int32_t h, double* out, double* lse,
+/* Forward of query row i of segment b, head h: writes O_i (d values at oi)
+ * and returns LSE_i.  x is scratch for the row's Lkv logits. */
+static double fwd_row(const problem* p, int32_t b, int32_t h, int64_t i, double* x, double* oi) {
+    const int64_t lkv = p->kv_off[b + 1] - p->kv_off[b];
+    const int64_t hd = (int64_t)p->heads * p->d;
+    for (int32_t c = 0; c < p->d; ++c) oi[c] = 0.0;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < lkv; ++j) {
+        if (!valid_pair(p, i, j, lkv)) continue;
+        x[j] = logit(p, b, h, i, j);
+        if (x[j] > m) m = x[j];
+    }
+    double l = 0.0;
+    if (p->act == ORACLE_SOFTMAX) {
+        for (int64_t j = 0; j < lkv; ++j)
+            if (valid_pair(p, i, j, lkv)) l += exp(x[j] - m);
+    }
+    for (int64_t j = 0; j < lkv; ++j) {
+        if (!valid_pair(p, i, j, lkv)) continue;
+        double w, dw;
+        if (p->act == ORACLE_SOFTMAX) w = exp(x[j] - m) / l;
+        else act_eval(p->act, x[j], &w, &dw);
+        const double* vj = p->v + ((int64_t)p->kv_off[b] + j) * hd + (int64_t)h * p->d;
+        for (int32_t c = 0; c < p->d; ++c) oi[c] += w * vj[c];
+    }
+    return (l > 0.0) ? m + log(l) : -INFINITY;
+}
+
+/* Forward of one (segment, head) unit: O rows and LSE of that unit.
+ * Returns nonzero if its scratch cannot be allocated. */
+static int fwd_unit(const problem* p, int32_t b, int32_t h, double* out, double* lse,
                      int64_t total_q) {
     const int64_t lq = p->q_off[b + 1] - p->q_off[b];
     const int64_t lkv = p->kv_off[b + 1] - p->kv_off[b];
     const int64_t hd = (int64_t)p->heads * p->d;
     double* x = (double*)malloc(sizeof(double) * (size_t)(lkv > 0 ? lkv : 1));
+    if (!x) return 1;
     for (int64_t i = 0; i < lq; ++i) {
         double* oi = out + ((int64_t)p->q_off[b] + i) * hd + (int64_t)h * p->d;
-        for (int32_t c = 0; c < p->d; ++c) oi[c] = 0.0;
-        double m = -INFINITY;
-        for (int64_t j = 0; j < lkv; ++j) {
-            if (!valid_pair(p, i, j, lkv)) continue;
-            x[j] = logit(p, b, h, i, j);
-            if (x[j] > m) m = x[j];
-        }
-        double l = 0.0;
-        if (p->act == ORACLE_SOFTMAX) {
-            for (int64_t j = 0; j < lkv; ++j)
-                if (valid_pair(p, i, j, lkv)) l += exp(x[j] - m);
-        }
-        for (int64_t j = 0; j < lkv; ++j) {
-            if (!valid_pair(p, i, j, lkv)) continue;
-            double w, dw;
-            if (p->act == ORACLE_SOFTMAX) w = exp(x[j] - m) / l;
-            else act_eval(p->act, x[j], &w, &dw);
-            const double* vj = p->v + ((int64_t)p->kv_off[b] + j) * hd + (int64_t)h * p->d;
-            for (int32_t c = 0; c < p->d; ++c) oi[c] += w * vj[c];
-        }
-        if (lse) lse[(int64_t)h * total_q + p->q_off[b] + i] = (l > 0.0) ? m + log(l) : -INFINITY;
+        const double l = fwd_row(p, b, h, i, x, oi);
+        if (lse) lse[(int64_t)h * total_q + p->q_off[b] + i] = l;
     }
     free(x);
+    return 0;
+}
+
+/* Backward quantities of one valid pair (i, j): P_ij (the act value, or the
+ * softmax probability exp(x_ij - LSE_i)) and dS_ij = dP_ij act'(x_ij), or
+ * P_ij (dP_ij - D_i) in softmax mode, with dP_ij = <dO_i, v_j>. */
+static void pair_grad(const problem* p, int32_t b, int32_t h, int64_t i, int64_t j,
+                      const double* doi, double lse_i, double di, double* pij, double* ds) {
+    const int64_t hd = (int64_t)p->heads * p->d;
+    const double* vj = p->v + ((int64_t)p->kv_off[b] + j) * hd + (int64_t)h * p->d;
+    double x = logit(p, b, h, i, j);
+    double dp = 0.0;
+    for (int32_t c = 0; c < p->d; ++c) dp += doi[c] * vj[c];
+    if (p->act == ORACLE_SOFTMAX) {
+        *pij = exp(x - lse_i);
+        *ds = *pij * (dp - di);
+    } else {
+        double da;
+        act_eval(p->act, x, pij, &da);
+        *ds = dp * da;
+    }
 }
 
 /* Backward of one unit.  dq/dk/dv rows of the unit are overwritten; the
  * unit's dbias contribution is written to dbias_unit[T] (zeroed here).  With
  * shared queries dq is the unit's own [S][d] buffer instead. */
-static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double* dk,
-                     double* dv, double* dbias_unit) {
+static int bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double* dk,
+                    double* dv, double* dbias_unit) {
     const int64_t lq = p->q_off[b + 1] - p->q_off[b];
     const int64_t lkv = p->kv_off[b + 1] - p->kv_off[b];
     const int32_t d = p->d;
@@ -217,7 +249,11 @@ static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double*
         sub.batch = 1;
         o = (double*)calloc((size_t)(lq * hd), sizeof(double));
         lse = (double*)calloc((size_t)(lq * p->heads), sizeof(double));
-        fwd_unit(&sub, 0, h, o, lse, lq);
+        if (!o || !lse || fwd_unit(&sub, 0, h, o, lse, lq)) {
+            free(o);
+            free(lse);
+            return 1;
+        }
     }
     for (int64_t i = 0; i < lq; ++i) {
         const double* qi = q_row(p, b, i, h);
@@ -232,21 +268,10 @@ static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double*
         for (int64_t j = 0; j < lkv; ++j) {
             if (!valid_pair(p, i, j, lkv)) continue;
             const double* kj = p->k + (k0 + j) * hd + (int64_t)h * d;
-            const double* vj = p->v + (k0 + j) * hd + (int64_t)h * d;
             double* dkj = dk + (k0 + j) * hd + (int64_t)h * d;
             double* dvj = dv + (k0 + j) * hd + (int64_t)h * d;
-            double x = logit(p, b, h, i, j);
-            double dp = 0.0;
-            for (int32_t c = 0; c < d; ++c) dp += doi[c] * vj[c];
             double pij, ds;
-            if (p->act == ORACLE_SOFTMAX) {
-                pij = exp(x - lse_i);
-                ds = pij * (dp - di);
-            } else {
-                double da;
-                act_eval(p->act, x, &pij, &da);
-                ds = dp * da;
-            }
+            pair_grad(p, b, h, i, j, doi, lse_i, di, &pij, &ds);
             for (int32_t c = 0; c < d; ++c) {
                 dvj[c] += pij * doi[c];
                 dqi[c] += p->scale * ds * kj[c];
@@ -257,6 +282,7 @@ static void bwd_unit(const problem* p, int32_t b, int32_t h, double* dq, double*
     }
     free(o);
     free(lse);
+    return 0;
 }
 
 static int check_problem(const problem* p) {
@@ -286,7 +312,8 @@ static void set_threads(int32_t threads) {
 /*
  * Forward.  units/n_units select (segment, head) units as b*H + h; units ==
  * NULL means all of them.  Only the selected units' rows of out and lse are
- * written.  lse may be NULL.  Returns 0, or 1 on invalid arguments.
+ * written.  lse may be NULL.  Returns 0, 1 on invalid arguments, or 2 if
+ * scratch memory cannot be allocated.
  */
 int oracle_fwd(const double* q, const double* k, const double* v,
                const int32_t* q_off, const int32_t* kv_off, int32_t batch,
@@ -299,18 +326,24 @@ int oracle_fwd(const double* q, const double* k, const double* v,
     if (check_problem(&p)) return 1;
     const int64_t total_q = batch > 0 ? q_off[batch] : 0;
     const int32_t n = units ? n_units : batch * heads;
+    int failed = 0;
     set_threads(threads);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t u = 0; u < n; ++u) {
         int32_t id = units ? units[u] : u;
-        fwd_unit(&p, id / heads, id % heads, out, lse, total_q);
+        if (fwd_unit(&p, id / heads, id % heads, out, lse, total_q)) {
+#pragma omp atomic write
+            failed = 1;
+        }
     }
-    return 0;
+    return failed ? 2 : 0;
 }
 
 /*
  * Backward.  Overwrites the selected units' rows of dq, dk, dv; dbias (may be
  * NULL) receives the sum over the selected units, reduced in unit order.
+ * Returns 0, 1 on invalid arguments, or 2 if scratch memory cannot be
+ * allocated (the outputs are then incomplete).
  */
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
                const int32_t* q_off, const int32_t* kv_off, int32_t batch,
@@ -330,12 +363,26 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
     const int64_t sq = (int64_t)q_shared * d;
     double* dq_part = q_shared > 0 ? (double*)calloc((size_t)n * (size_t)(sq > 0 ? sq : 1), sizeof(double))
                                    : NULL;
+    if ((dbias && bias_len > 0 && !part) || (q_shared > 0 && !dq_part)) {
+        free(part);
+        free(dq_part);
+        return 2;
+    }
+    int failed = 0;
     set_threads(threads);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t u = 0; u < n; ++u) {
         int32_t id = units ? units[u] : u;
-        bwd_unit(&p, id / heads, id % heads, dq_part ? dq_part + (int64_t)u * sq : dq, dk, dv,
-                 part ? part + (int64_t)u * t : NULL);
+        if (bwd_unit(&p, id / heads, id % heads, dq_part ? dq_part + (int64_t)u * sq : dq, dk, dv,
+                     part ? part + (int64_t)u * t : NULL)) {
+#pragma omp atomic write
+            failed = 1;
+        }
+    }
+    if (failed) {
+        free(part);
+        free(dq_part);
+        return 2;
     }
     if (dq_part) {
         memset(dq, 0, sizeof(double) * (size_t)q_shared * (size_t)heads * (size_t)d);
@@ -357,6 +404,115 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
         }
         free(part);
     }
+    return 0;
+}
+
+/*
+ * Backward of one (segment b, head h) unit restricted to some of its rows:
+ * dQ_i for the segment-local query rows q_rows[0..n_q) and dK_j, dV_j for
+ * the key rows kv_rows[0..n_kv), each an explicit sum over its valid
+ * partners with the per-pair quantities of the full backward, taken in the
+ * same order (ascending j for dQ_i, ascending i for dK_j and dV_j), so the
+ * rows equal those of oracle_bwd.  In softmax mode LSE_i and D_i = <dO_i, O_i>
+ * come from the forward of each query row involved.  dq_rows is [n_q][d],
+ * dk_rows and dv_rows are [n_kv][d].  OpenMP runs over the selected rows.
+ * Returns 0, 1 on invalid arguments (including a row outside the segment,
+ * or shared queries, which this entry point does not take), or 2 if scratch
+ * memory cannot be allocated.
+ */
+int oracle_bwd_rows(const double* q, const double* k, const double* v, const double* dout,
+                    const int32_t* q_off, const int32_t* kv_off, int32_t batch,
+                    int32_t heads, int32_t d, int32_t act, double scale,
+                    const double* bias, int32_t bias_len, int32_t causal, int32_t window,
+                    int32_t b, int32_t h, const int32_t* q_rows, int32_t n_q,
+                    const int32_t* kv_rows, int32_t n_kv, int32_t threads,
+                    double* dq_rows, double* dk_rows, double* dv_rows) {
+    problem p = {q, k, v, dout, bias, q_off, kv_off, batch, heads, d, act, bias_len, causal, window,
+                 0, scale};
+    if (check_problem(&p)) return 1;
+    if (b < 0 || b >= batch || h < 0 || h >= heads || n_q < 0 || n_kv < 0) return 1;
+    const int64_t lq = q_off[b + 1] - q_off[b];
+    const int64_t lkv = kv_off[b + 1] - kv_off[b];
+    for (int32_t r = 0; r < n_q; ++r)
+        if (q_rows[r] < 0 || q_rows[r] >= lq) return 1;
+    for (int32_t r = 0; r < n_kv; ++r)
+        if (kv_rows[r] < 0 || kv_rows[r] >= lkv) return 1;
+    const int64_t hd = (int64_t)heads * d;
+    const int64_t q0 = q_off[b], k0 = kv_off[b];
+    const int softmax = act == ORACLE_SOFTMAX;
+    /* softmax: LSE_i and D_i of every query row (the key rows meet them all) */
+    double* lse = NULL;
+    double* dd = NULL;
+    int failed = 0;
+    set_threads(threads);
+    if (softmax && lq > 0) {
+        lse = (double*)malloc(sizeof(double) * (size_t)lq);
+        dd = (double*)malloc(sizeof(double) * (size_t)lq);
+        if (!lse || !dd) {
+            free(lse);
+            free(dd);
+            return 2;
+        }
+#pragma omp parallel
+        {
+            double* x = (double*)malloc(sizeof(double) * (size_t)(lkv > 0 ? lkv : 1));
+            double* oi = (double*)malloc(sizeof(double) * (size_t)d);
+            if (!x || !oi) {
+#pragma omp atomic write
+                failed = 1;
+            }
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t i = 0; i < lq; ++i) {
+                if (!x || !oi) continue;
+                lse[i] = fwd_row(&p, b, h, i, x, oi);
+                const double* doi = dout + (q0 + i) * hd + (int64_t)h * d;
+                double di = 0.0;
+                for (int32_t c = 0; c < d; ++c) di += doi[c] * oi[c];
+                dd[i] = di;
+            }
+            free(x);
+            free(oi);
+        }
+        if (failed) {
+            free(lse);
+            free(dd);
+            return 2;
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t r = 0; r < n_q; ++r) {
+        const int64_t i = q_rows[r];
+        const double* doi = dout + (q0 + i) * hd + (int64_t)h * d;
+        double* dqi = dq_rows + (int64_t)r * d;
+        for (int32_t c = 0; c < d; ++c) dqi[c] = 0.0;
+        for (int64_t j = 0; j < lkv; ++j) {
+            if (!valid_pair(&p, i, j, lkv)) continue;
+            const double* kj = k + (k0 + j) * hd + (int64_t)h * d;
+            double pij, ds;
+            pair_grad(&p, b, h, i, j, doi, softmax ? lse[i] : 0.0, softmax ? dd[i] : 0.0, &pij, &ds);
+            for (int32_t c = 0; c < d; ++c) dqi[c] += scale * ds * kj[c];
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t r = 0; r < n_kv; ++r) {
+        const int64_t j = kv_rows[r];
+        double* dkj = dk_rows + (int64_t)r * d;
+        double* dvj = dv_rows + (int64_t)r * d;
+        for (int32_t c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+        for (int64_t i = 0; i < lq; ++i) {
+            if (!valid_pair(&p, i, j, lkv)) continue;
+            const double* qi = q + (q0 + i) * hd + (int64_t)h * d;
+            const double* doi = dout + (q0 + i) * hd + (int64_t)h * d;
+            double pij, ds;
+            pair_grad(&p, b, h, i, j, doi, softmax ? lse[i] : 0.0, softmax ? dd[i] : 0.0, &pij, &ds);
+            for (int32_t c = 0; c < d; ++c) {
+                dvj[c] += pij * doi[c];
+                dkj[c] += scale * ds * qi[c];
+            }
+        }
+    }
+    free(lse);
+    free(dd);
     return 0;
 }
 

@@ -2,10 +2,14 @@
 
 from __future__ import annotations
 
+import dataclasses
+import functools
+
 import numpy as np
 import torch
 
 import oracle
+import workloads
 
 # Per-output-tensor bar: max|gpu - ref| <= TOL * max|ref| (bf16 inputs, fp32
 # accumulation, bf16 P / dS operands).
@@ -100,3 +104,16 @@ def sampled_oracle(x, units, backward: bool):
             o, lse = res
             out.append((b, h, q_rows, kv_rows, (o[sq, h], lse[h, sq])))
     return out
+
+
+@functools.lru_cache(maxsize=2)
+def _workload(idx: int):
+    return workloads.workload_inputs(idx)
+
+
+def full_workload(idx: int):
+    """The full-size inputs of a named workload, generated once per process
+    (the sliding-window workload 6 reuses the draws of workload 5)."""
+    if idx == 6:
+        return dataclasses.replace(_workload(5), window=workloads.WORKLOADS[6].window)
+    return _workload(idx)

@@ -113,3 +113,116 @@ def test_ds_scratch_size_follows_the_band(lib):
     assert jg.jgdpa_ds_scratch_bytes(qo, ko, 1, -1) == 0
     # the band never holds more than the unwindowed scratch
     assert jg.jgdpa_ds_scratch_bytes(qo, ko, 2, 300) <= jg.jgdpa_ds_scratch_bytes(qo, ko, 2, 0)
+
+
+# ---------------------------------------------------------------- binding checks
+# The Python wrappers check dtypes and shapes before any pointer reaches the
+# library (the library builds V's tensor map from K's row count and dO's from
+# Q's, so a short tensor would be read past its end).  These run on the CPU:
+# the checks come before the device check.
+
+def _bundle(tq=10, tkv=7, h=2, d=64, bias=5):
+    import torch
+    return dict(q=torch.zeros(tq, h, d, dtype=torch.bfloat16), k=torch.zeros(tkv, h, d, dtype=torch.bfloat16),
+                v=torch.zeros(tkv, h, d, dtype=torch.bfloat16), q_offsets=torch.tensor([0, tq], dtype=torch.int32),
+                kv_offsets=torch.tensor([0, tkv], dtype=torch.int32),
+                bias_table=torch.zeros(h, bias, dtype=torch.float32) if bias else None)
+
+
+@pytest.mark.parametrize("field,bad,match", [
+    ("q", "float32", "q must have dtype"),
+    ("k", "float16", "k must have dtype"),
+    ("v", "short", "v must have shape"),
+    ("k", "heads", "k must have shape"),
+    ("q_offsets", "int64", "q_offsets must have dtype"),
+    ("kv_offsets", "long", "kv_offsets must have shape"),
+    ("bias_table", "float64", "bias_table must have dtype"),
+    ("bias_table", "heads", "bias_table must have shape"),
+])
+def test_forward_wrapper_rejects_bad_tensors(lib, field, bad, match):
+    import torch
+    import jagged_gdpa_gb300 as jg
+    b = _bundle()
+    t = b[field]
+    if bad in ("float32", "float16", "int64", "float64"):
+        b[field] = t.to(getattr(torch, bad))
+    elif bad == "short":
+        b[field] = t[:-1]
+    elif bad == "heads":  # one head too many: dimension 1 of [rows, H, d], dimension 0 of [H, T]
+        shape = list(t.shape)
+        shape[1 if t.dim() == 3 else 0] += 1
+        b[field] = torch.zeros(shape, dtype=t.dtype)
+    elif bad == "long":
+        b[field] = torch.zeros(t.numel() + 1, dtype=t.dtype)
+    with pytest.raises(ValueError, match=match):
+        jg.jgdpa_fwd(b["q"], b["k"], b["v"], b["q_offsets"], b["kv_offsets"], "gelu", 0.125,
+                     bias_table=b["bias_table"])
+
+
+def test_forward_wrapper_rejects_bad_outputs(lib):
+    import torch
+    import jagged_gdpa_gb300 as jg
+    b = _bundle()
+    args = (b["q"], b["k"], b["v"], b["q_offsets"], b["kv_offsets"])
+    with pytest.raises(ValueError, match="out must have shape"):
+        jg.jgdpa_fwd(*args, "gelu", 0.125, out=torch.zeros(9, 2, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="out must have dtype"):
+        jg.jgdpa_fwd(*args, "gelu", 0.125, out=torch.zeros(10, 2, 64, dtype=torch.float32))
+    with pytest.raises(ValueError, match="lse must have shape"):
+        jg.jgdpa_fwd(*args, "softmax", 0.125, lse=torch.zeros(2, 9, dtype=torch.float32))
+    with pytest.raises(ValueError, match="lse is written in softmax mode only"):
+        jg.jgdpa_fwd(*args, "gelu", 0.125, lse=torch.zeros(2, 10, dtype=torch.float32))
+    with pytest.raises(ValueError, match="workspace must have dtype"):
+        jg.jgdpa_fwd(*args, "gelu", 0.125, workspace=torch.zeros(1024, dtype=torch.float32))
+    # everything valid: the wrapper gets as far as the device check
+    with pytest.raises(ValueError, match="CUDA device"):
+        jg.jgdpa_fwd(*args, "gelu", 0.125, bias_table=b["bias_table"])
+
+
+@pytest.mark.parametrize("field,shape,dtype,match", [
+    ("dout", (9, 2, 64), "bfloat16", "dout must have shape"),
+    ("dq", (10, 2, 64), "float32", "dq must have dtype"),
+    ("dk", (6, 2, 64), "bfloat16", "dk must have shape"),
+    ("dv", (7, 2, 32), "bfloat16", "dv must have shape"),
+    ("dbias", (2, 4), "float32", "dbias must have shape"),
+    ("lse", (2, 11), "float32", "lse must have shape"),
+    ("out", (10, 2, 64), "float16", "out must have dtype"),
+    ("ds_scratch", (64,), "int32", "ds_scratch must have dtype"),
+])
+def test_backward_wrapper_rejects_bad_tensors(lib, field, shape, dtype, match):
+    import torch
+    import jagged_gdpa_gb300 as jg
+    b = _bundle()
+    kw = dict(dq=None, dk=None, dv=None, dbias=None, ds_scratch=None)
+    out = torch.zeros(10, 2, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(2, 10, dtype=torch.float32)
+    dout = torch.zeros(10, 2, 64, dtype=torch.bfloat16)
+    bad = torch.zeros(shape, dtype=getattr(torch, dtype))
+    if field == "dout":
+        dout = bad
+    elif field == "lse":
+        lse = bad
+    elif field == "out":
+        out = bad
+    else:
+        kw[field] = bad
+    with pytest.raises(ValueError, match=match):
+        jg.jgdpa_bwd(b["q"], b["k"], b["v"], out, lse, dout, b["q_offsets"], b["kv_offsets"], "softmax", 0.125,
+                     bias_table=b["bias_table"], **kw)
+
+
+def test_backward_wrapper_rejects_dbias_without_a_table(lib):
+    import torch
+    import jagged_gdpa_gb300 as jg
+    b = _bundle(bias=0)
+    with pytest.raises(ValueError, match="dbias needs a bias table"):
+        jg.jgdpa_bwd(b["q"], b["k"], b["v"], None, None, torch.zeros(10, 2, 64, dtype=torch.bfloat16),
+                     b["q_offsets"], b["kv_offsets"], "gelu", 0.125, dbias=torch.zeros(2, 5))
+
+
+def test_alu_route_library_is_built_and_exports_the_same_symbols(lib):
+    import jagged_gdpa_gb300 as jg
+    alu = jg.load(jg.ALU_LIB_PATH)
+    assert alu is not lib
+    for n in declared_functions():
+        assert hasattr(alu, n), n

@@ -111,3 +111,54 @@ def test_stored_ds_scratch_too_small_is_reported(jg):
                                  workspace=ws, ds_scratch=enough)
     assert jg.jgdpa_read_device_status(ws) == 0
     assert torch.isfinite(dq.float()).all() and torch.isfinite(dk.float()).all()
+
+
+def test_device_wait_timeout_is_reported_and_the_next_call_recovers(jg):
+    """Every internal wait of the kernels is bounded.  With the limit set to
+    1 ns through the test hook, the waits of a multi-tile call run out: the
+    kernels record JGDPA_ERR_DEVICE_TIMEOUT (7), drain their copies and
+    tensor-core work in flight, free Tensor Memory and exit.  With the
+    default limit back, the next call on the same GPU and workspace returns
+    status 0 and matches the oracle.  Nothing here waits without a limit."""
+    import oracle
+    from tests._util import assert_close
+    # several long units per CTA, so producers wait on slots held for many tiles
+    x = workloads.random_case(31, batch=16, heads=4, head_dim=128, act="gelu", lq_range=(3000, 4096),
+                              lkv_range=(3000, 4096), bias_len=257)
+    d = x.to("cuda")
+    tq, tkv = x.q.shape[0], x.k.shape[0]
+    ws_f = torch.empty(jg.jgdpa_workspace_bytes(x.batch, tq, tkv, x.heads, x.head_dim, x.act, x.bias_len, False),
+                       dtype=torch.uint8, device="cuda")
+    ws_b = torch.empty(jg.jgdpa_workspace_bytes(x.batch, tq, tkv, x.heads, x.head_dim, x.act, x.bias_len, True),
+                       dtype=torch.uint8, device="cuda")
+    scratch = torch.empty(jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, x.heads), dtype=torch.uint8,
+                          device="cuda")
+    out = torch.empty_like(d.q)
+    try:
+        jg.jgdpa_set_wait_limit_ns(1)
+        jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias, out=out,
+                     workspace=ws_f)
+        assert jg.jgdpa_read_device_status(ws_f) == 7
+        for sc in (scratch, None):  # stored-dS and recompute backward
+            jg.jgdpa_bwd(d.q, d.k, d.v, out, None, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
+                         bias_table=d.bias, workspace=ws_b, ds_scratch=sc)
+            assert jg.jgdpa_read_device_status(ws_b) == 7
+    finally:
+        jg.jgdpa_set_wait_limit_ns(0)
+    torch.cuda.synchronize()
+    out, _ = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
+                          workspace=ws_f)
+    dq, dk, dv, _ = jg.jgdpa_bwd(d.q, d.k, d.v, out, None, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
+                                 bias_table=d.bias, workspace=ws_b, ds_scratch=scratch)
+    assert jg.jgdpa_read_device_status(ws_f) == 0 and jg.jgdpa_read_device_status(ws_b) == 0
+    # parity of one unit of the recovered call
+    b, h = 3, 1
+    sub = workloads.select_segments(x, [b])
+    ro, _ = oracle.fwd_inputs(sub, units=[h])
+    rq, rk, rv, _ = oracle.bwd_inputs(sub, units=[h])
+    q0, q1 = int(x.q_offsets[b]), int(x.q_offsets[b + 1])
+    k0, k1 = int(x.kv_offsets[b]), int(x.kv_offsets[b + 1])
+    assert_close("O after timeout", out[q0:q1, h].cpu(), ro[:, h])
+    assert_close("dQ after timeout", dq[q0:q1, h].cpu(), rq[:, h])
+    assert_close("dK after timeout", dk[k0:k1, h].cpu(), rk[:, h])
+    assert_close("dV after timeout", dv[k0:k1, h].cpu(), rv[:, h])

@@ -578,3 +578,46 @@ def test_shared_queries_need_equal_segment_lengths():
     x = workloads.make_inputs([3, 4], [5, 5], 1, 4, "gelu", seed=2)
     with pytest.raises(ValueError):
         oracle.fwd(x.q[:3], x.k, x.v, x.q_offsets, x.kv_offsets, 1, 4, "gelu", x.scale, q_shared=3)
+
+
+# ----------------------------------------------------------------------------
+# Row-restricted backward (single rows of long units)
+# ----------------------------------------------------------------------------
+
+ROW_MODES = [(a, c, w, bl) for a in ("gelu", "silu", "softmax") for c in (False, True) for w in (0, 5)
+             for bl in (0, 7)]
+
+
+@pytest.mark.parametrize("act,causal,window,bias_len", ROW_MODES)
+def test_backward_rows_equal_the_full_backward(act, causal, window, bias_len):
+    """dQ / dK / dV of selected rows equal the full backward's rows bit for bit
+    (same per-pair quantities, same summation order), and match torch
+    autograd on the dense form."""
+    x = workloads.random_case(900 + window + bias_len + int(causal), batch=3, heads=2, head_dim=8, act=act,
+                              lq_range=(1, 15), lkv_range=(1, 15), causal=causal, bias_len=bias_len,
+                              window=window)
+    dq, dk, dv, _ = oracle.bwd_inputs(x)
+    rq, rk, rv, _ = dense_torch_grads(x)
+    qo, ko = x.q_offsets.numpy(), x.kv_offsets.numpy()
+    rng = np.random.default_rng(3)
+    for b in range(x.batch):
+        for h in range(x.heads):
+            qr = np.sort(rng.choice(int(x.lq[b]), size=min(4, int(x.lq[b])), replace=False))
+            kr = np.sort(rng.choice(int(x.lkv[b]), size=min(4, int(x.lkv[b])), replace=False))
+            gq, gk, gv = oracle.bwd_rows_inputs(x, b, h, qr, kr)
+            assert np.array_equal(gq, dq[qo[b] + qr, h])
+            assert np.array_equal(gk, dk[ko[b] + kr, h])
+            assert np.array_equal(gv, dv[ko[b] + kr, h])
+            for got, ref in ((gq, rq[qo[b] + qr, h]), (gk, rk[ko[b] + kr, h]), (gv, rv[ko[b] + kr, h])):
+                if np.max(np.abs(ref), initial=0) > 0:
+                    assert _rel(got, ref) <= 1e-10
+
+
+def test_backward_rows_reject_rows_outside_the_segment():
+    x = workloads.random_case(5, batch=2, heads=1, head_dim=4, act="gelu", lq_range=(3, 5), lkv_range=(3, 5))
+    with pytest.raises(ValueError):
+        oracle.bwd_rows_inputs(x, 0, 0, [int(x.lq[0])], [])
+    with pytest.raises(ValueError):
+        oracle.bwd_rows_inputs(x, 0, 0, [], [-1])
+    with pytest.raises(ValueError):
+        oracle.bwd_rows_inputs(x, 2, 0, [0], [0])

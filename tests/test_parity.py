@@ -11,8 +11,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
-from tests._util import assert_close, oracle_bwd, oracle_fwd, sample_units, sampled_oracle
+from tests._util import assert_close, full_workload, oracle_bwd, oracle_fwd, sample_units, sampled_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -25,21 +26,21 @@ def jg():
     return m
 
 
-def run_fwd(jg, x):
+def run_fwd(jg, x, lib=None):
     d = x.to("cuda")
     out, lse = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale,
-                            bias_table=d.bias, causal=x.causal, window=x.window)
+                            bias_table=d.bias, causal=x.causal, window=x.window, lib=lib)
     torch.cuda.synchronize()
     return out.cpu(), (None if lse is None else lse.cpu())
 
 
-def run_bwd(jg, x, out=None, lse=None, stored=False):
+def run_bwd(jg, x, out=None, lse=None, stored=False, lib=None):
     """Backward through the C ABI; stored=True takes the stored-dS path
     (jgdpa_bwd_ex with a scratch of exactly jgdpa_ds_scratch_bytes)."""
     d = x.to("cuda")
     if x.act == "softmax":
         out, lse = jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale,
-                                bias_table=d.bias, causal=x.causal, window=x.window)
+                                bias_table=d.bias, causal=x.causal, window=x.window, lib=lib)
     scratch = None
     if stored:
         nbytes = jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, x.heads, x.window)
@@ -48,14 +49,14 @@ def run_bwd(jg, x, out=None, lse=None, stored=False):
                                               x.bias_len, True), dtype=torch.uint8, device="cuda")
     dq, dk, dv, db = jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act,
                                   x.scale, bias_table=d.bias, causal=x.causal, workspace=ws, ds_scratch=scratch,
-                                  window=x.window)
+                                  window=x.window, lib=lib)
     torch.cuda.synchronize()
-    assert jg.jgdpa_read_device_status(ws) == 0, "device status"
+    assert jg.jgdpa_read_device_status(ws, lib=lib) == 0, "device status"
     return dq.cpu(), dk.cpu(), dv.cpu(), (None if db is None else db.cpu())
 
 
-def check_fwd_full(jg, x, tag=""):
-    out, lse = run_fwd(jg, x)
+def check_fwd_full(jg, x, tag="", lib=None):
+    out, lse = run_fwd(jg, x, lib=lib)
     ref, rlse = oracle_fwd(x)
     assert_close(f"O {tag}", out, ref)
     if x.act == "softmax":
@@ -64,8 +65,8 @@ def check_fwd_full(jg, x, tag=""):
         assert_close(f"LSE {tag}", lse.numpy()[valid], rlse[valid])
 
 
-def check_bwd_full(jg, x, tag="", stored=False):
-    dq, dk, dv, db = run_bwd(jg, x, stored=stored)
+def check_bwd_full(jg, x, tag="", stored=False, lib=None):
+    dq, dk, dv, db = run_bwd(jg, x, stored=stored, lib=lib)
     tag = f"{tag}{' stored-dS' if stored else ''}"
     rq, rk, rv, rb = oracle_bwd(x)
     assert_close(f"dQ {tag}", dq, rq)
@@ -221,11 +222,89 @@ def check_sampled(jg, x, units_fwd, units_bwd, tag, stored=False):
     (6, 4, 4e7, 4e7),
 ])
 def test_full_size_workloads_sampled(jg, idx, n_random, max_pairs_fwd, max_pairs_bwd):
-    x = workloads.workload_inputs(idx)
+    x = full_workload(idx)
     uf = sample_units(x, n_random, seed=idx, max_pairs=max_pairs_fwd)
     ub = sample_units(x, n_random, seed=100 + idx, max_pairs=max_pairs_bwd)
     check_sampled(jg, x, uf, ub, f"w{idx}")
     check_sampled(jg, x, uf, ub, f"w{idx}", stored=True)
+
+
+@pytest.mark.parametrize("stored", [False, True])
+@pytest.mark.parametrize("idx", [5, 6])
+def test_longest_unit_backward_rows(jg, idx, stored):
+    """The backward of the workload's longest segment (14,270 tokens, about a
+    quarter of the long-tail batch's pairs), one head, at full size in the
+    launch configuration the benchmark times: dQ rows of three query tiles
+    (first, middle, and the ragged last one) and dK / dV rows of three key
+    tiles, against the oracle restricted to those rows."""
+    x = full_workload(idx)
+    dq, dk, dv, _ = run_bwd(jg, x, stored=stored)
+    pairs = x.lq.astype(np.int64) * x.lkv.astype(np.int64)
+    b = int(np.argmax(pairs))
+    h = (idx + int(stored)) % x.heads
+    sub = workloads.select_segments(x, [b])
+    rows = []
+    for n in (int(x.lq[b]), int(x.lkv[b])):
+        last = (n - 1) // 128 * 128
+        mid = (n // 2) // 128 * 128
+        rows.append(np.unique(np.concatenate([np.arange(0, min(128, n)), np.arange(mid, min(mid + 128, n)),
+                                              np.arange(last, n)])))
+    qr, kr = rows
+    rq, rk, rv = oracle.bwd_rows_inputs(sub, 0, h, qr, kr)
+    q0, k0 = int(x.q_offsets[b]), int(x.kv_offsets[b])
+    tag = f"w{idx} longest segment b={b} h={h}{' stored-dS' if stored else ''}"
+    assert_close(f"dQ {tag}", dq.float().numpy()[q0 + qr, h], rq)
+    assert_close(f"dK {tag}", dk.float().numpy()[k0 + kr, h], rk)
+    assert_close(f"dV {tag}", dv.float().numpy()[k0 + kr, h], rv)
+
+
+# ---------------------------------------------- ALU-only activation route
+# The same library built with every GELU / SiLU element of the forward and of
+# the backward on the ALU polynomial route (no special-function unit), the
+# activation design of the GDPA kernel redesign ("Meta redesigns AI training
+# infrastructure ...", section "Custom Kernels and 5D Parallelism ...").
+ALU_GRID = [(d, act, causal) for d in (32, 64, 128) for act in ("gelu", "silu") for causal in (False, True)]
+
+
+@pytest.fixture(scope="module")
+def alu_lib(jg):
+    return jg.load(jg.ALU_LIB_PATH)
+
+
+@pytest.mark.parametrize("d,act,causal", ALU_GRID)
+def test_alu_route_forward_small(jg, alu_lib, d, act, causal):
+    x = workloads.random_case(5000 + d + int(causal), batch=5, heads=2, head_dim=d, act=act,
+                              lq_range=(1, 300), lkv_range=(1, 300), causal=causal, bias_len=257)
+    check_fwd_full(jg, x, f"ALU route d={d} {act} causal={causal}", lib=alu_lib)
+
+
+@pytest.mark.parametrize("stored", [False, True])
+@pytest.mark.parametrize("d,act,causal", ALU_GRID)
+def test_alu_route_backward_small(jg, alu_lib, d, act, causal, stored):
+    x = workloads.random_case(6000 + d + int(causal), batch=4, heads=2, head_dim=d, act=act,
+                              lq_range=(1, 300), lkv_range=(1, 300), causal=causal, bias_len=257)
+    check_bwd_full(jg, x, f"ALU route d={d} {act} causal={causal}", stored=stored, lib=alu_lib)
+
+
+def test_alu_route_long_tail_sampled(jg, alu_lib):
+    """The ALU-route kernels on the full long-tail batch, sampled units."""
+    x = full_workload(5)
+    out, _ = run_fwd(jg, x, lib=alu_lib)
+    units = sample_units(x, 3, seed=77, max_pairs=3e7)
+    got, want = [], []
+    for b, h, qr, kr, (o, _) in sampled_oracle(x, units, backward=False):
+        got.append(out.float().numpy()[qr, h])
+        want.append(o)
+    assert_close("O ALU route w5", np.concatenate(got), np.concatenate(want))
+    dq, dk, dv, _ = run_bwd(jg, x, stored=True, lib=alu_lib)
+    g = {"dQ": [], "dK": [], "dV": []}
+    w = {"dQ": [], "dK": [], "dV": []}
+    for b, h, qr, kr, (rq, rk, rv) in sampled_oracle(x, units, backward=True):
+        for name, t, rows, ref in (("dQ", dq, qr, rq), ("dK", dk, kr, rk), ("dV", dv, kr, rv)):
+            g[name].append(t.float().numpy()[rows, h])
+            w[name].append(ref)
+    for name in g:
+        assert_close(f"{name} ALU route w5 stored-dS", np.concatenate(g[name]), np.concatenate(w[name]))
 
 
 def test_largest_bias_table_and_more_heads(jg):
@@ -269,14 +348,29 @@ def test_cuda_graph_capture_replays_the_step(jg):
         step()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    ref = [t.clone() for t in (out, dq, dk, dv)]
+    ref = [t.clone() for t in (out, dq, dk, dv, db)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         step()
-    for t in (out, dq, dk, dv):
+    for t in (out, dq, dk, dv, db):
         t.zero_()
     g.replay()
     torch.cuda.synchronize()
     assert jg.jgdpa_read_device_status(ws_f) == 0 and jg.jgdpa_read_device_status(ws_b) == 0
-    for a, b in zip((out, dq, dk, dv), ref):
+    for a, b in zip((out, dq, dk, dv, db), ref):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("stored", [False, True])
+def test_backward_is_bitwise_reproducible_including_dbias(jg, stored):
+    """Repeated backward calls give identical bits for dQ, dK, dV and dbias.
+    The dbias partial sums are 64-bit fixed-point integers, so their totals do
+    not depend on which CTA ran which unit or in which order the warps added
+    them (the scheduler's order among equal-cost units is not fixed)."""
+    x = workloads.random_case(66, batch=6, heads=3, head_dim=128, act="gelu", lq_range=(1, 900),
+                              lkv_range=(1, 900), bias_len=257)
+    first = run_bwd(jg, x, stored=stored)
+    for _ in range(3):
+        again = run_bwd(jg, x, stored=stored)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
