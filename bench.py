@@ -282,29 +282,60 @@ def run_native(args, world, rank, local):
     total_kv = x.k.shape[0]
     bias_len = x.bias_len
     softmax = x.act == "softmax"
+    # shared seed queries (PMA): the shared-query entry points read the S
+    # query rows once per segment and return dQ summed over the segments
+    shared = x.q_seed is not None
+    n_shared = x.q_seed.shape[0] if shared else 0
     out = torch.empty_like(d.q)
     lse = torch.empty((heads, total_q), dtype=torch.float32, device=dev) if softmax else None
-    dq, dk, dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
+    dq = torch.empty_like(d.q_seed if shared else d.q)
+    dk, dv = torch.empty_like(d.k), torch.empty_like(d.v)
     dbias = torch.empty((heads, bias_len), dtype=torch.float32, device=dev) if bias_len else None
-    ws_f = torch.empty(jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, False),
-                       dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, True),
-                       dtype=torch.uint8, device=dev)
+
+    def ws_bytes(bwd_):
+        if shared:
+            return jg.jgdpa_shared_q_workspace_bytes(x.batch, n_shared, total_kv, heads, hd, x.act, bias_len, bwd_)
+        return jg.jgdpa_workspace_bytes(x.batch, total_q, total_kv, heads, hd, x.act, bias_len, bwd_)
+
+    ws_f = torch.empty(ws_bytes(False), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(ws_bytes(True), dtype=torch.uint8, device=dev)
     # stored-dS backward: scratch sized from the (host) segment lengths
     ds_scratch = torch.empty(max(1, jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, heads, x.window)),
                              dtype=torch.uint8, device=dev)
 
+    def call_fwd(di, o, l):
+        if shared:
+            return jg.jgdpa_fwd_shared_q(di["q_seed"], di["k"], di["v"], di["kv_offsets"], x.act, x.scale,
+                                         bias_table=di.get("bias"), causal=x.causal, out=o, lse=l, workspace=ws_f,
+                                         window=x.window)
+        return jg.jgdpa_fwd(di["q"], di["k"], di["v"], di["q_offsets"], di["kv_offsets"], x.act, x.scale,
+                            bias_table=di.get("bias"), causal=x.causal, out=o, lse=l, workspace=ws_f,
+                            window=x.window)
+
+    def call_bwd(di, o, l, r, pass_events=None):
+        if shared:
+            return jg.jgdpa_bwd_shared_q(di["q_seed"], di["k"], di["v"], o, l, di["dout"], di["kv_offsets"], x.act,
+                                         x.scale, bias_table=di.get("bias"), causal=x.causal, dq=r["dq"],
+                                         dk=r["dk"], dv=r["dv"], dbias=r.get("dbias"), workspace=ws_b,
+                                         ds_scratch=ds_scratch, pass_events=pass_events, window=x.window)
+        return jg.jgdpa_bwd(di["q"], di["k"], di["v"], o, l, di["dout"], di["q_offsets"], di["kv_offsets"], x.act,
+                            x.scale, bias_table=di.get("bias"), causal=x.causal, dq=r["dq"], dk=r["dk"],
+                            dv=r["dv"], dbias=r.get("dbias"), workspace=ws_b, ds_scratch=ds_scratch,
+                            pass_events=pass_events, window=x.window)
+
+    dev_inputs = {"q": d.q, "q_seed": d.q_seed, "k": d.k, "v": d.v, "dout": d.dout, "q_offsets": d.q_offsets,
+                  "kv_offsets": d.kv_offsets, "bias": d.bias}
+    results = {"dq": dq, "dk": dk, "dv": dv, "dbias": dbias}
+
     def fwd():
-        jg.jgdpa_fwd(d.q, d.k, d.v, d.q_offsets, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
-                     causal=x.causal, out=out, lse=lse, workspace=ws_f, window=x.window)
+        call_fwd(dev_inputs, out, lse)
 
     def bwd(pass_events=None):
-        jg.jgdpa_bwd(d.q, d.k, d.v, out, lse, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
-                     bias_table=d.bias, causal=x.causal, dq=dq, dk=dk, dv=dv, dbias=dbias, workspace=ws_b,
-                     ds_scratch=ds_scratch, pass_events=pass_events, window=x.window)
+        call_bwd(dev_inputs, out, lse, results, pass_events)
 
-    # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, dQ, [dbias reduce])
-    launches_per_step = 2 + 3 + int(softmax) + int(bias_len > 0)
+    # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, dQ, [dbias reduce]);
+    # shared queries add the offset kernel of each call and the dQ reduction
+    launches_per_step = 2 + 3 + int(softmax) + int(bias_len > 0) + (3 if shared else 0)
     for _ in range(args.warmup):
         fwd()
         bwd()
@@ -348,7 +379,8 @@ def run_native(args, world, rank, local):
     # pipeline would be: a copy stream loads step i+1's inputs into the other
     # input set while step i computes, and a second copy stream reads step
     # i's results from its own output set while step i+1 computes.
-    in_names = ["q", "k", "v", "dout", "q_offsets", "kv_offsets"] + (["bias"] if bias_len else [])
+    in_names = (["q_seed"] if shared else ["q", "q_offsets"]) + ["k", "v", "dout", "kv_offsets"] + \
+        (["bias"] if bias_len else [])
     host_in = {k: getattr(x, k).pin_memory() for k in in_names}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     ms_e2e = float("nan")
@@ -388,13 +420,8 @@ def run_native(args, world, rank, local):
                 comp.wait_event(in_ready[bi])
                 comp.wait_event(out_free[bi])
                 di, r = dev_in[bi], res[bi]
-                o, l2 = jg.jgdpa_fwd(di["q"], di["k"], di["v"], di["q_offsets"], di["kv_offsets"], x.act, x.scale,
-                                     bias_table=di.get("bias"), causal=x.causal, out=r["out"], lse=lse2[bi],
-                                     workspace=ws_f, window=x.window)
-                jg.jgdpa_bwd(di["q"], di["k"], di["v"], o, l2, di["dout"], di["q_offsets"], di["kv_offsets"],
-                             x.act, x.scale, bias_table=di.get("bias"), causal=x.causal, dq=r["dq"], dk=r["dk"],
-                             dv=r["dv"], dbias=r.get("dbias"), workspace=ws_b, ds_scratch=ds_scratch,
-                             window=x.window)
+                o, l2 = call_fwd(di, r["out"], lse2[bi])
+                call_bwd(di, o, l2, r)
                 in_free[bi].record(comp)
                 out_ready[bi].record(comp)
                 s_out.wait_event(out_ready[bi])

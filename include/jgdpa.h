@@ -216,6 +216,52 @@ JGDPA_API jgdpa_status jgdpa_bwd_ex(const void* q, const void* k, const void* v,
                        void* const* pass_events);
 
 /*
+ * Shared query rows (PMA-style pooling): every segment attends with the same
+ * n_shared = S query rows, e.g. learned seed queries shared across the batch
+ * ("GEM Training: How Meta Doubled the Efficiency of Its ..."
+ * (globalainews.in), section "What to watch": PMA is one of the modules GDPA
+ * serves).  Segment b's query row i (0 <= i < S) is row i of q; its output,
+ * upstream gradient and LSE rows are b S + i.  The computation is otherwise
+ * that of jgdpa_fwd_ex / jgdpa_bwd_ex with Lq_b = S for every segment, and
+ * the gradient of the shared rows is the sum over segments of each
+ * segment's dQ.
+ *   q          bf16 [S][heads][head_dim], read by every segment (not expanded)
+ *   out, dout  bf16 [batch S][heads][head_dim]
+ *   lse        fp32 [heads][batch S] (SOFTMAX mode only, else NULL)
+ *   dq         bf16 [S][heads][head_dim], written: sum over b of dQ_b,
+ *              accumulated in fp32 in segment order (deterministic) and
+ *              rounded once
+ *   kv_offsets, k, v, dk, dv, bias_table, dbias, causal, window, ds_scratch,
+ *   pass_events
+ *              as in jgdpa_bwd_ex (there are no query offsets: they are S b,
+ *              formed in the workspace; the stored-dS scratch size is
+ *              jgdpa_ds_scratch_bytes with query offsets S b)
+ * The workspace must hold jgdpa_shared_q_workspace_bytes(...) bytes: the
+ * backward keeps each segment's dQ rows in fp32 there ([batch S][heads]
+ * [head_dim]) and a fixed-order reduction kernel sums them.  Errors as in
+ * jgdpa_fwd / jgdpa_bwd; n_shared < 1 is INVALID_ARGUMENT, batch S beyond
+ * int32 is UNSUPPORTED.
+ */
+JGDPA_API size_t jgdpa_shared_q_workspace_bytes(int32_t batch, int32_t n_shared, int64_t total_kv,
+                                                int32_t heads, int32_t head_dim, jgdpa_act act,
+                                                int32_t bias_len, int32_t for_backward);
+JGDPA_API jgdpa_status jgdpa_fwd_shared_q(const void* q, int32_t n_shared, const void* k, const void* v,
+                                          const int32_t* kv_offsets, int32_t batch, int64_t total_kv,
+                                          int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
+                                          const float* bias_table, int32_t bias_len, int32_t causal,
+                                          int32_t window, void* out, float* lse,
+                                          void* workspace, size_t workspace_bytes, jgdpa_stream_t stream);
+JGDPA_API jgdpa_status jgdpa_bwd_shared_q(const void* q, int32_t n_shared, const void* k, const void* v,
+                                          const void* out, const float* lse, const void* dout,
+                                          const int32_t* kv_offsets, int32_t batch, int64_t total_kv,
+                                          int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
+                                          const float* bias_table, int32_t bias_len, int32_t causal,
+                                          int32_t window, void* dq, void* dk, void* dv, float* dbias,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* ds_scratch, size_t ds_scratch_bytes, jgdpa_stream_t stream,
+                                          void* const* pass_events);
+
+/*
  * Forward pass without a caller-provided workspace: the same computation and
  * arguments as jgdpa_fwd minus (workspace, workspace_bytes).  There is no
  * counterpart on the pages; this entry point exists for callers that cannot

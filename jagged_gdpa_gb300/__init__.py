@@ -11,6 +11,9 @@ from ._lib import (  # noqa: F401
     EXPORTS,
     JgdpaError,
     jgdpa_bwd,
+    jgdpa_bwd_shared_q,
+    jgdpa_fwd_shared_q,
+    jgdpa_shared_q_workspace_bytes,
     jgdpa_ds_scratch_bytes,
     jgdpa_eval_activation,
     jgdpa_fwd,

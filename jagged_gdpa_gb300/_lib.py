@@ -28,7 +28,7 @@ STATUS = {
 EXPORTS = ("jgdpa_workspace_bytes", "jgdpa_fwd", "jgdpa_fwd_ex", "jgdpa_bwd", "jgdpa_bwd_ex",
            "jgdpa_ds_scratch_bytes",
            "jgdpa_read_device_status", "jgdpa_status_string", "jgdpa_eval_activation", "jgdpa_fwd_noalloc",
-           "jgdpa_set_wait_limit_ns")
+           "jgdpa_set_wait_limit_ns", "jgdpa_shared_q_workspace_bytes", "jgdpa_fwd_shared_q", "jgdpa_bwd_shared_q")
 
 
 class JgdpaError(RuntimeError):
@@ -75,6 +75,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.jgdpa_fwd_noalloc.restype = ctypes.c_int
     lib.jgdpa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.jgdpa_set_wait_limit_ns.restype = None
+    lib.jgdpa_shared_q_workspace_bytes.argtypes = [i32, i32, i64, i32, i32, ctypes.c_int, i32, i32]
+    lib.jgdpa_shared_q_workspace_bytes.restype = sz
+    lib.jgdpa_fwd_shared_q.argtypes = [P, i32, P, P, P, i32, i64, i32, i32, ctypes.c_int, f32, P, i32, i32, i32,
+                                       P, P, P, sz, P]
+    lib.jgdpa_fwd_shared_q.restype = ctypes.c_int
+    lib.jgdpa_bwd_shared_q.argtypes = [P, i32, P, P, P, P, P, P, i32, i64, i32, i32, ctypes.c_int, f32, P, i32,
+                                       i32, i32, P, P, P, P, P, sz, P, sz, P, P]
+    lib.jgdpa_bwd_shared_q.restype = ctypes.c_int
     _libs[path] = lib
     return lib
 
@@ -133,6 +141,13 @@ def _ptr(t: Optional[torch.Tensor]):
     if not t.is_contiguous():
         raise ValueError("tensors passed to libjgdpa must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _events(pass_events):
+    """Three torch.cuda.Event (or None) as a C array of cudaEvent_t, or None."""
+    if pass_events is None:
+        return None
+    return (ctypes.c_void_p * 3)(*[None if e is None else e.cuda_event for e in pass_events])
 
 
 def _stream(stream: Optional[torch.cuda.Stream]):
@@ -252,11 +267,9 @@ def jgdpa_bwd(q, k, v, out, lse, dout, q_offsets, kv_offsets, act, scale: float,
         rc = lib.jgdpa_bwd(*head, *tail, _stream(stream))
         _rc(rc, "jgdpa_bwd")
     else:
-        ev = None
-        if pass_events is not None:
-            ev = (ctypes.c_void_p * 3)(*[None if e is None else e.cuda_event for e in pass_events])
         rc = lib.jgdpa_bwd_ex(*head, int(window), *tail, _ptr(ds_scratch),
-                              0 if ds_scratch is None else ds_scratch.numel(), _stream(stream), ev)
+                              0 if ds_scratch is None else ds_scratch.numel(), _stream(stream),
+                              _events(pass_events))
         _rc(rc, "jgdpa_bwd_ex")
     return dq, dk, dv, dbias
 
@@ -304,3 +317,94 @@ def jgdpa_set_wait_limit_ns(limit_ns: int, lib=None) -> None:
     """Test hook: limit of one internal device wait for later launches (0 =
     the default of 2 s)."""
     (lib or load()).jgdpa_set_wait_limit_ns(int(limit_ns))
+
+
+# ------------------------------------------------------------ shared queries
+def jgdpa_shared_q_workspace_bytes(batch: int, n_shared: int, total_kv: int, heads: int, head_dim: int, act,
+                                   bias_len: int = 0, for_backward: bool = False, lib=None) -> int:
+    return int((lib or load()).jgdpa_shared_q_workspace_bytes(batch, n_shared, total_kv, heads, head_dim,
+                                                              _act(act), bias_len, int(bool(for_backward))))
+
+
+def _check_shared(q, k, v, kv_offsets, bias_table):
+    if not isinstance(q, torch.Tensor) or q.dim() != 3:
+        raise ValueError("q must be a bf16 tensor [n_shared, heads, head_dim]")
+    n_shared, heads, d = q.shape
+    _check(q, "q", torch.bfloat16, (None, None, None))
+    _check(k, "k", torch.bfloat16, (None, heads, d), q.device)
+    total_kv = k.shape[0]
+    _check(v, "v", torch.bfloat16, (total_kv, heads, d), q.device)
+    _check(kv_offsets, "kv_offsets", torch.int32, (None,), q.device)
+    batch = kv_offsets.numel() - 1
+    if batch < 0:
+        raise ValueError("kv_offsets must hold batch + 1 >= 1 entries")
+    _check(bias_table, "bias_table", torch.float32, (heads, None), q.device, optional=True)
+    bias_len = 0 if bias_table is None else int(bias_table.shape[1])
+    return n_shared, heads, d, total_kv, batch, bias_len
+
+
+def jgdpa_fwd_shared_q(q, k, v, kv_offsets, act, scale: float, bias_table=None, causal: bool = False,
+                       out=None, lse=None, workspace=None, stream=None, window: int = 0, lib=None):
+    """Forward with query rows shared by every segment: q is [S, H, d]; out is
+    [batch S, H, d] (segment b's rows b S .. b S + S - 1); returns (out, lse)."""
+    lib = lib or load()
+    n_shared, heads, d, total_kv, batch, bias_len = _check_shared(q, k, v, kv_offsets, bias_table)
+    a = _act(act)
+    total_q = batch * n_shared
+    if out is None:
+        out = torch.empty((total_q, heads, d), dtype=q.dtype, device=q.device)
+    if lse is None and a == ACT["softmax"]:
+        lse = torch.empty((heads, total_q), dtype=torch.float32, device=q.device)
+    _check(out, "out", torch.bfloat16, (total_q, heads, d), q.device)
+    if a == ACT["softmax"]:
+        _check(lse, "lse", torch.float32, (heads, total_q), q.device)
+    elif lse is not None:
+        raise ValueError("lse is written in softmax mode only; pass None")
+    _check_bytes(workspace, "workspace", q.device)
+    nbytes = jgdpa_shared_q_workspace_bytes(batch, n_shared, total_kv, heads, d, a, bias_len, False, lib=lib)
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.jgdpa_fwd_shared_q(_ptr(q), n_shared, _ptr(k), _ptr(v), _ptr(kv_offsets), batch, total_kv, heads, d,
+                                a, float(scale), _ptr(bias_table), bias_len, int(bool(causal)), int(window),
+                                _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _rc(rc, "jgdpa_fwd_shared_q")
+    return out, lse
+
+
+def jgdpa_bwd_shared_q(q, k, v, out, lse, dout, kv_offsets, act, scale: float, bias_table=None,
+                       causal: bool = False, dq=None, dk=None, dv=None, dbias=None, want_dbias: bool = True,
+                       workspace=None, stream=None, ds_scratch=None, window: int = 0, pass_events=None,
+                       lib=None):
+    """Backward with shared query rows; dq [S, H, d] is the sum over segments.
+    pass_events as in jgdpa_bwd.  Returns (dq, dk, dv, dbias)."""
+    lib = lib or load()
+    n_shared, heads, d, total_kv, batch, bias_len = _check_shared(q, k, v, kv_offsets, bias_table)
+    a = _act(act)
+    total_q = batch * n_shared
+    _check(dout, "dout", torch.bfloat16, (total_q, heads, d), q.device)
+    opt = a != ACT["softmax"]
+    _check(out, "out", torch.bfloat16, (total_q, heads, d), q.device, optional=opt)
+    _check(lse, "lse", torch.float32, (heads, total_q), q.device, optional=opt)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dbias is None and bias_len and want_dbias:
+        dbias = torch.empty((heads, bias_len), dtype=torch.float32, device=q.device)
+    _check(dq, "dq", torch.bfloat16, (n_shared, heads, d), q.device)
+    _check(dk, "dk", torch.bfloat16, (total_kv, heads, d), q.device)
+    _check(dv, "dv", torch.bfloat16, (total_kv, heads, d), q.device)
+    if dbias is not None:
+        if not bias_len:
+            raise ValueError("dbias needs a bias table")
+        _check(dbias, "dbias", torch.float32, (heads, bias_len), q.device)
+    _check_bytes(workspace, "workspace", q.device)
+    _check_bytes(ds_scratch, "ds_scratch", q.device)
+    nbytes = jgdpa_shared_q_workspace_bytes(batch, n_shared, total_kv, heads, d, a, bias_len, True, lib=lib)
+    ws = _workspace(nbytes, q.device, workspace)
+    rc = lib.jgdpa_bwd_shared_q(_ptr(q), n_shared, _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                _ptr(kv_offsets), batch, total_kv, heads, d, a, float(scale), _ptr(bias_table),
+                                bias_len, int(bool(causal)), int(window), _ptr(dq), _ptr(dk), _ptr(dv),
+                                _ptr(dbias), _ptr(ws), ws.numel(), _ptr(ds_scratch),
+                                0 if ds_scratch is None else ds_scratch.numel(), _stream(stream),
+                                _events(pass_events))
+    _rc(rc, "jgdpa_bwd_shared_q")
+    return dq, dk, dv, dbias

@@ -28,6 +28,8 @@ cudaError_t launch_softmax_delta_d(const void* out, const void* dout, float* del
                                    const int* status, cudaStream_t stream);
 cudaError_t launch_dbias_reduce(const unsigned long long* part, float* dbias, int n_parts, int n,
                                 cudaStream_t stream);
+cudaError_t launch_dq_shared_reduce(const float* part, void* dq, int batch, int64_t n, const int* status,
+                                    cudaStream_t stream);
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t stream);
 
 cudaError_t launch_fwd(const FwdParams& p, int head_dim, int act, int grid, cudaStream_t stream) {
@@ -147,6 +149,8 @@ struct Layout {
   size_t delta = 0;       // softmax bwd: [H][total_q]
   size_t dbias = 0;       // bwd with dbias: [grid][H][T] 64-bit fixed-point partial sums
   size_t ds_base = 0;     // bwd: first stored-dS tile per segment, int64 [batch + 1]
+  size_t q_off = 0;       // shared queries: the synthesized query offsets S b, int32 [batch + 1]
+  size_t dq_part = 0;     // shared queries, bwd: fp32 dQ of every segment's rows [batch S][H][d]
   size_t total = 0;
   int max0 = 0, max1 = 0;
   int grid = 0;
@@ -157,7 +161,7 @@ int64_t max_units(int64_t total, int64_t batch, int rows_per_unit, int heads) {
 }
 
 bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads, int32_t act, int32_t bias_len,
-                bool bwd, Layout* L) {
+                bool bwd, Layout* L, int32_t q_shared = 0, int32_t head_dim = 0) {
   const int sms = sm_count();
   if (sms <= 0) return false;
   int64_t m0, m1 = 0;
@@ -186,6 +190,10 @@ bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
   if (bwd && bias_len > 0) off += up(static_cast<size_t>(sms) * heads * bias_len * sizeof(unsigned long long));
   L->ds_base = off;
   if (bwd) off += up((static_cast<size_t>(batch) + 1) * sizeof(int64_t));
+  L->q_off = off;
+  if (q_shared > 0) off += up((static_cast<size_t>(batch) + 1) * sizeof(int32_t));
+  L->dq_part = off;
+  if (q_shared > 0 && bwd) off += up(static_cast<size_t>(total_q) * heads * head_dim * sizeof(float));
   L->total = off;
   return true;
 }
@@ -219,6 +227,11 @@ jgdpa_status check_common(int32_t batch, int64_t total_q, int64_t total_kv, int3
 __global__ void fill_f32_kernel(float* p, int64_t n, float v) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i < n) p[i] = v;
+}
+
+__global__ void shared_q_offsets_kernel(int32_t* q_off, int32_t batch, int32_t n_shared) {
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (b <= batch) q_off[b] = static_cast<int32_t>(b * n_shared);
 }
 
 cudaError_t fill_f32(float* p, int64_t n, float v, cudaStream_t s) {
@@ -310,14 +323,18 @@ size_t jgdpa_workspace_bytes(int32_t batch, int64_t total_q, int64_t total_kv, i
 
 namespace {
 
+// q_shared > 0: every segment reads the same q_shared query rows (q is
+// [q_shared][H][d]); q_offsets is then ignored and synthesized in the
+// workspace as q_shared b, so that O and LSE keep one block of rows per
+// segment (total_q = batch q_shared).
 jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t* q_offsets,
                       const int32_t* kv_offsets, int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
                       int32_t head_dim, jgdpa_act act, float scale, const float* bias_table, int32_t bias_len,
                       int32_t causal, int32_t window, void* out, float* lse, void* workspace,
-                      size_t workspace_bytes, jgdpa_stream_t stream_) {
+                      size_t workspace_bytes, jgdpa_stream_t stream_, int32_t q_shared = 0) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   jgdpa_status st = check_common(batch, total_q, total_kv, heads, head_dim, act, scale, bias_table, bias_len,
-                                 causal, q_offsets, kv_offsets);
+                                 causal, q_shared > 0 ? kv_offsets : q_offsets, kv_offsets);
   if (st != JGDPA_OK) return st;
   if (window < 0) return JGDPA_ERR_INVALID_ARGUMENT;
   if ((act == JGDPA_ACT_SOFTMAX) != (lse != nullptr)) return JGDPA_ERR_INVALID_ARGUMENT;
@@ -326,12 +343,19 @@ jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
     return JGDPA_ERR_MISALIGNED;
   Layout L;
-  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, false, &L)) return JGDPA_ERR_CUDA;
+  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, false, &L, q_shared, head_dim))
+    return JGDPA_ERR_CUDA;
   if (workspace == nullptr || workspace_bytes < L.total) return JGDPA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, kAlign)) return JGDPA_ERR_MISALIGNED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   JG_CUDA(cudaMemsetAsync(ws + L.header, 0, 64 * sizeof(int), stream));
   if (batch == 0 || total_q == 0) return JGDPA_OK;
+  if (q_shared > 0) {
+    int32_t* qo = reinterpret_cast<int32_t*>(ws + L.q_off);
+    shared_q_offsets_kernel<<<static_cast<unsigned>((batch + 1 + 255) / 256), 256, 0, stream>>>(qo, batch, q_shared);
+    JG_CUDA(cudaGetLastError());
+    q_offsets = qo;
+  }
   if (total_kv == 0) {  // no keys anywhere: O = 0, LSE = -inf
     JG_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(total_q) * heads * head_dim * 2, stream));
     if (lse) JG_CUDA(fill_f32(lse, total_q * heads, -INFINITY, stream));
@@ -341,9 +365,10 @@ jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t
   if (st != JGDPA_OK) return st;
 
   jg::FwdParams p{};
-  if (!make_map(&p.tm_q, q, total_q, heads, head_dim) || !make_map(&p.tm_k, k, total_kv, heads, head_dim) ||
-      !make_map(&p.tm_v, v, total_kv, heads, head_dim))
+  if (!make_map(&p.tm_q, q, q_shared > 0 ? q_shared : total_q, heads, head_dim) ||
+      !make_map(&p.tm_k, k, total_kv, heads, head_dim) || !make_map(&p.tm_v, v, total_kv, heads, head_dim))
     return JGDPA_ERR_CUDA;
+  p.q_shared = q_shared > 0 ? 1 : 0;
   int* hdr = reinterpret_cast<int*>(ws + L.header);
   p.q_off = q_offsets;
   p.kv_off = kv_offsets;
@@ -398,14 +423,15 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
                       int64_t total_q, int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act,
                       float scale, const float* bias_table, int32_t bias_len, int32_t causal, int32_t window,
                       void* dq, void* dk, void* dv, float* dbias, void* workspace, size_t workspace_bytes,
-                      jgdpa_stream_t stream_, void* ds_scratch, size_t ds_scratch_bytes, void* const* ev) {
+                      jgdpa_stream_t stream_, void* ds_scratch, size_t ds_scratch_bytes, void* const* ev,
+                      int32_t q_shared = 0) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   auto record = [&](int i) -> cudaError_t {
     return (ev != nullptr && ev[i] != nullptr) ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), stream)
                                                : cudaSuccess;
   };
   jgdpa_status st = check_common(batch, total_q, total_kv, heads, head_dim, act, scale, bias_table, bias_len,
-                                 causal, q_offsets, kv_offsets);
+                                 causal, q_shared > 0 ? kv_offsets : q_offsets, kv_offsets);
   if (st != JGDPA_OK) return st;
   if (window < 0) return JGDPA_ERR_INVALID_ARGUMENT;
   if (dbias != nullptr && bias_len == 0) return JGDPA_ERR_INVALID_ARGUMENT;
@@ -418,7 +444,8 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(dbias, 4))
     return JGDPA_ERR_MISALIGNED;
   Layout L;
-  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, true, &L)) return JGDPA_ERR_CUDA;
+  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, true, &L, q_shared, head_dim))
+    return JGDPA_ERR_CUDA;
   if (workspace == nullptr || workspace_bytes < L.total) return JGDPA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, kAlign)) return JGDPA_ERR_MISALIGNED;
   // stored dS: capacity in tiles (the device checks the lengths against it)
@@ -430,8 +457,9 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   if (dbias) JG_CUDA(cudaMemsetAsync(dbias, 0, static_cast<size_t>(heads) * bias_len * sizeof(float), stream));
   if (batch == 0) return JGDPA_OK;
   const size_t row_bytes = static_cast<size_t>(heads) * head_dim * 2;
+  const int64_t dq_rows = q_shared > 0 ? q_shared : total_q;  // rows of dq
   if (total_q == 0 || total_kv == 0) {  // no valid pair anywhere: all gradients are zero
-    if (total_q) JG_CUDA(cudaMemsetAsync(dq, 0, total_q * row_bytes, stream));
+    if (total_q) JG_CUDA(cudaMemsetAsync(dq, 0, dq_rows * row_bytes, stream));
     if (total_kv) {
       JG_CUDA(cudaMemsetAsync(dk, 0, total_kv * row_bytes, stream));
       JG_CUDA(cudaMemsetAsync(dv, 0, total_kv * row_bytes, stream));
@@ -439,14 +467,22 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     return JGDPA_OK;
   }
   const bool stored_ds = ds_scratch != nullptr && ds_tiles > 0;
+  if (q_shared > 0) {
+    int32_t* qo = reinterpret_cast<int32_t*>(ws + L.q_off);
+    shared_q_offsets_kernel<<<static_cast<unsigned>((batch + 1 + 255) / 256), 256, 0, stream>>>(qo, batch, q_shared);
+    JG_CUDA(cudaGetLastError());
+    q_offsets = qo;
+  }
   st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, true, stream,
                  ds_scratch ? std::max<int64_t>(ds_tiles, 0) : -1);
   if (st != JGDPA_OK) return st;
 
   jg::BwdParams p{};
-  if (!make_map(&p.tm_q, q, total_q, heads, head_dim) || !make_map(&p.tm_k, k, total_kv, heads, head_dim) ||
+  if (!make_map(&p.tm_q, q, dq_rows, heads, head_dim) || !make_map(&p.tm_k, k, total_kv, heads, head_dim) ||
       !make_map(&p.tm_v, v, total_kv, heads, head_dim) || !make_map(&p.tm_do, dout, total_q, heads, head_dim))
     return JGDPA_ERR_CUDA;
+  p.q_shared = q_shared > 0 ? 1 : 0;
+  p.dq_part = q_shared > 0 ? reinterpret_cast<float*>(ws + L.dq_part) : nullptr;
   if (stored_ds) {
     if (!make_ds_map(&p.tm_ds, ds_scratch, ds_tiles)) return JGDPA_ERR_CUDA;
     p.ds_base = reinterpret_cast<const int64_t*>(ws + L.ds_base);
@@ -489,6 +525,9 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   else JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
   JG_CUDA(record(2));
   if (part) JG_CUDA(jg::launch_dbias_reduce(part, dbias, grid_kv, heads * bias_len, stream));
+  if (q_shared > 0)
+    JG_CUDA(jg::launch_dq_shared_reduce(p.dq_part, dq, batch, static_cast<int64_t>(q_shared) * heads * head_dim, hdr,
+                                        stream));
   return JGDPA_OK;
 }
 
@@ -516,6 +555,45 @@ jgdpa_status jgdpa_bwd_ex(const void* q, const void* k, const void* v, const voi
   return bwd_impl(q, k, v, out, lse, dout, q_offsets, kv_offsets, batch, total_q, total_kv, heads, head_dim, act,
                   scale, bias_table, bias_len, causal, window, dq, dk, dv, dbias, workspace, workspace_bytes,
                   stream, ds_scratch, ds_scratch_bytes, pass_events);
+}
+
+size_t jgdpa_shared_q_workspace_bytes(int32_t batch, int32_t n_shared, int64_t total_kv, int32_t heads,
+                                      int32_t head_dim, jgdpa_act act, int32_t bias_len, int32_t for_backward) {
+  if (batch < 0 || n_shared < 1 || total_kv < 0 || heads < 1 || bias_len < 0) return 0;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return 0;
+  const int64_t total_q = static_cast<int64_t>(batch) * n_shared;
+  if (total_q > INT32_MAX) return 0;
+  Layout L;
+  if (!layout_for(batch, total_q, total_kv, heads, act, bias_len, for_backward != 0, &L, n_shared, head_dim))
+    return 0;
+  return L.total;
+}
+
+jgdpa_status jgdpa_fwd_shared_q(const void* q, int32_t n_shared, const void* k, const void* v,
+                                const int32_t* kv_offsets, int32_t batch, int64_t total_kv, int32_t heads,
+                                int32_t head_dim, jgdpa_act act, float scale, const float* bias_table,
+                                int32_t bias_len, int32_t causal, int32_t window, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, jgdpa_stream_t stream) {
+  if (n_shared < 1 || batch < 0) return JGDPA_ERR_INVALID_ARGUMENT;
+  const int64_t total_q = static_cast<int64_t>(batch) * n_shared;
+  if (total_q > INT32_MAX) return JGDPA_ERR_UNSUPPORTED;
+  return fwd_impl(q, k, v, nullptr, kv_offsets, batch, total_q, total_kv, heads, head_dim, act, scale, bias_table,
+                  bias_len, causal, window, out, lse, workspace, workspace_bytes, stream, n_shared);
+}
+
+jgdpa_status jgdpa_bwd_shared_q(const void* q, int32_t n_shared, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, const int32_t* kv_offsets, int32_t batch,
+                                int64_t total_kv, int32_t heads, int32_t head_dim, jgdpa_act act, float scale,
+                                const float* bias_table, int32_t bias_len, int32_t causal, int32_t window,
+                                void* dq, void* dk, void* dv, float* dbias, void* workspace,
+                                size_t workspace_bytes, void* ds_scratch, size_t ds_scratch_bytes,
+                                jgdpa_stream_t stream, void* const* pass_events) {
+  if (n_shared < 1 || batch < 0) return JGDPA_ERR_INVALID_ARGUMENT;
+  const int64_t total_q = static_cast<int64_t>(batch) * n_shared;
+  if (total_q > INT32_MAX) return JGDPA_ERR_UNSUPPORTED;
+  return bwd_impl(q, k, v, out, lse, dout, nullptr, kv_offsets, batch, total_q, total_kv, heads, head_dim, act,
+                  scale, bias_table, bias_len, causal, window, dq, dk, dv, dbias, workspace, workspace_bytes,
+                  stream, ds_scratch, ds_scratch_bytes, pass_events, n_shared);
 }
 
 size_t jgdpa_ds_scratch_bytes(const int32_t* q_offsets_host, const int32_t* kv_offsets_host, int32_t batch,

@@ -236,19 +236,23 @@ __device__ void bwd_producer(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
       if (!(ok = mbar_wait_warp(&bars->res_empty[rs], ((res_it / C::kNumRes) & 1) ^ 1, fail))) break;
       ++res_it;
       const int row = (KV_MAJOR ? u.seg.k0 : u.seg.q0) + u.tile * kTile;
+      // shared queries (Q-major pass): the Q map holds the shared rows once
+      const int row0 = (!KV_MAJOR && p.q_shared) ? u.tile * kTile : row;
       if (leader) {
         uint64_t* bar = &bars->res_full[rs];
         mbar_arrive_tx(bar, 2 * C::kTileBytes);
         uint8_t* d0 = smem + C::kResOff + rs * C::kResBytes;
 #pragma unroll
         for (int cb = 0; cb < C::kNumBlocks; ++cb) {
-          tma_load_3d(d0 + cb * C::kBlockBytes, res0, bar, cb * C::kBlockCols, u.h, row);
+          tma_load_3d(d0 + cb * C::kBlockBytes, res0, bar, cb * C::kBlockCols, u.h, row0);
           tma_load_3d(d0 + C::kTileBytes + cb * C::kBlockBytes, res1, bar, cb * C::kBlockCols, u.h, row);
         }
       }
     }
+    // shared queries (key-major pass, stream A = Q): the Q map holds the shared rows once
+    const int sbase = KV_MAJOR ? ((STREAM == 0 && p.q_shared) ? 0 : u.seg.q0) : u.seg.k0;
     for (int i = 0; i < u.count; ++i) {
-      const int row = (KV_MAJOR ? u.seg.q0 : u.seg.k0) + (u.first + i) * kTile;
+      const int row = sbase + (u.first + i) * kTile;
       const int st = st_it % kStages;
       if (!(ok = mbar_wait_warp(&empty[st], ((st_it / kStages) & 1) ^ 1, fail))) break;
       if (leader) {
@@ -688,6 +692,10 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
           __nv_bfloat16* dst = (half == 0 ? p.dv : p.dk) + (grow * H + u.h) * D;
 #pragma unroll
           for (int c = 0; c < D; c += 8) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
+        } else if (p.dq_part) {
+          float* dst = p.dq_part + (grow * H + u.h) * D + half * (D / 2);
+#pragma unroll
+          for (int c = 0; c < D / 2; c += 4) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
         } else {
           __nv_bfloat16* dst = p.dq + (grow * H + u.h) * D + half * (D / 2);
 #pragma unroll
@@ -929,23 +937,34 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         }
       }
     } else {
-      // warpgroup h stores dQ columns [h D/2, (h+1) D/2), scaled by s
+      // warpgroup h stores dQ columns [h D/2, (h+1) D/2), scaled by s (shared
+      // queries: fp32 into the per-segment partial rows, summed afterwards)
       const uint32_t t_acc = tmem + lane_off + 256 + (D / 2) * half;
       __nv_bfloat16* dst = p.dq + (grow * H + u.h) * D + (D / 2) * half;
+      float* dst32 = p.dq_part + (grow * H + u.h) * D + (D / 2) * half;
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 16) {
         uint32_t o[16];
         tmem_ld16(t_acc + c0, o);
         tmem_ld_wait16(o);
         if (row_ok) {
+          if (p.dq_part) {
 #pragma unroll
-          for (int c = 0; c < 16; c += 8) {
-            uint32_t w[4];
+            for (int c = 0; c < 16; c += 4)
+              st_global_v4(dst32 + c0 + c, __float_as_uint(__uint_as_float(o[c]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[c + 1]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[c + 2]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[c + 3]) * p.scale));
+          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * p.scale,
-                               __uint_as_float(o[c + 2 * e + 1]) * p.scale);
-            st_global_v4(dst + c0 + c, w[0], w[1], w[2], w[3]);
+            for (int c = 0; c < 16; c += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * p.scale,
+                                 __uint_as_float(o[c + 2 * e + 1]) * p.scale);
+              st_global_v4(dst + c0 + c, w[0], w[1], w[2], w[3]);
+            }
           }
         }
       }
@@ -1175,10 +1194,16 @@ __global__ void __launch_bounds__(256, 1) gdpa_dq_ds_kernel(const __grid_constan
       const bool row_ok = r < u.rows;
       const int64_t grow = static_cast<int64_t>(u.seg.q0) + u.tile * kTile + r;
       __nv_bfloat16* dst = p.dq + (grow * H + u.h) * D;
+      float* dst32 = p.dq_part + (grow * H + u.h) * D;  // shared queries: fp32 partial rows
       if (u.count == 0) {  // no keys: zero rows
         if (row_ok) {
+          if (p.dq_part) {
 #pragma unroll
-          for (int c = 0; c < D; c += 8) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
+            for (int c = 0; c < D; c += 4) st_global_v4(dst32 + c, 0u, 0u, 0u, 0u);
+          } else {
+#pragma unroll
+            for (int c = 0; c < D; c += 8) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
+          }
         }
         continue;
       }
@@ -1192,7 +1217,14 @@ __global__ void __launch_bounds__(256, 1) gdpa_dq_ds_kernel(const __grid_constan
         uint32_t o[32];
         tmem_ld32(t_acc + c0, o);
         tmem_ld_wait(o);
-        if (row_ok) {
+        if (row_ok && p.dq_part) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            st_global_v4(dst32 + c0 + c, __float_as_uint(__uint_as_float(o[c]) * p.scale),
+                         __float_as_uint(__uint_as_float(o[c + 1]) * p.scale),
+                         __float_as_uint(__uint_as_float(o[c + 2]) * p.scale),
+                         __float_as_uint(__uint_as_float(o[c + 3]) * p.scale));
+        } else if (row_ok) {
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint32_t w[4];
@@ -1308,6 +1340,25 @@ template cudaError_t launch_softmax_delta_d<JGDPA_HEAD_DIM>(const void*, const v
                                                             const int*, cudaStream_t);
 
 #if JGDPA_HEAD_DIM == 128
+// Shared queries: dq[s][h][c] = sum over segments b (in order) of the fp32
+// partial dQ rows part[b S + s][h][c], rounded to bf16 once.
+__global__ void dq_shared_reduce_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ dq,
+                                        int batch, int64_t n, const int* status) {
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (s, h, c) of [S][H][D]
+  if (e >= n || *status != kOk) return;
+  float acc = 0.f;
+  for (int b = 0; b < batch; ++b) acc += part[static_cast<int64_t>(b) * n + e];
+  dq[e] = __float2bfloat16_rn(acc);
+}
+
+cudaError_t launch_dq_shared_reduce(const float* part, void* dq, int batch, int64_t n, const int* status,
+                                    cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  dq_shared_reduce_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+      part, static_cast<__nv_bfloat16*>(dq), batch, n, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dbias_reduce(const unsigned long long* part, float* dbias, int n_parts, int n,
                                 cudaStream_t stream) {
   if (n == 0) return cudaSuccess;

@@ -116,6 +116,7 @@ struct FwdParams {
   int32_t window;         // > 0: sliding window |i - j| < window
   float scale;            // s (GELU/SiLU) or s * log2(e) (softmax)
   unsigned long long wait_limit_ns;  // limit of one internal wait
+  int32_t q_shared;       // 1: every segment reads the same query rows (Q map row 0 = its row 0)
 };
 
 struct BwdParams {
@@ -148,6 +149,8 @@ struct BwdParams {
   CUtensorMap tm_ds;       // 2-D over the scratch: 128 columns x (tiles * 128) rows
   const int64_t* ds_base;  // nullptr: no stored dS
   unsigned long long wait_limit_ns;  // limit of one internal wait
+  int32_t q_shared;        // 1: every segment reads the same query rows (Q map row 0 = its row 0)
+  float* dq_part;          // q_shared: fp32 dQ of every segment's rows [total_q][H][D], summed afterwards
 };
 
 constexpr int kDsTileBytes = kTile * kTile * 2;

@@ -154,7 +154,8 @@ __device__ void fwd_producer(const FwdParams& p, uint8_t* smem, FwdBars* bars, i
       if (leader) {
         mbar_arrive_tx(&bars->q_full[s], C::kTileBytes);
         uint8_t* dst = smem + C::kQOff + s * C::kTileBytes;
-        const int row = u.seg.q0 + (2 * u.pair + s) * kTile;
+        // shared queries: the Q map holds the shared rows once
+        const int row = (p.q_shared ? 0 : u.seg.q0) + (2 * u.pair + s) * kTile;
 #pragma unroll
         for (int cb = 0; cb < C::kNumBlocks; ++cb)
           tma_load_3d(dst + cb * C::kBlockBytes, &p.tm_q, &bars->q_full[s], cb * C::kBlockCols, u.h, row);

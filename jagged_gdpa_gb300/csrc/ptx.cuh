@@ -55,6 +55,38 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test for completion of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The same test with a suspend-time hint: a thread that finds the phase
+// incomplete sleeps at most about hint_ns before the call returns false.  (A
+// test without a hint may sleep until the phase completes, which is what the
+// kernels want in normal operation but hides a short limit.)
+__device__ __forceinline__ bool mbar_try_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are test settings: their waits test with a short hint.
+constexpr unsigned long long kShortLimitNs = 1000000ull;
+
 // Per-CTA failure state: `abort` lives in shared memory, `status` in global.
 struct Fail {
   volatile int* abort;          // shared: nonzero once any role of this CTA gave up
@@ -66,14 +98,18 @@ struct Fail {
 // Inline on purpose: these waits sit inside loops that keep most registers
 // live, where a call would cost saves and restores around it.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Fail f) {
-  if (mbar_try(bar, parity)) return true;
+  if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  // a short limit (the test hook) is checked after every try
-  const int tries = f.limit_ns < 1000000ull ? 1 : 64;
+  // Normal limits: each test may sleep until the phase completes (~1 ms at
+  // most), and the clock is read every 64 tests.  A short (test) limit: each
+  // test sleeps ~100 ns at most and the clock is read after every one.
+  const bool short_limit = f.limit_ns < kShortLimitNs;
+  const uint32_t hint = short_limit ? 100u : 1000000u;
+  const int tries = short_limit ? 1 : 64;
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < tries; ++i)
-      if (mbar_try(bar, parity)) return true;
+      if (mbar_try_hint(bar, parity, hint)) return true;
     if (*f.abort) return false;
     if (globaltimer() - t0 > f.limit_ns) {
       *f.abort = 1;
