@@ -239,21 +239,29 @@ __device__ __forceinline__ float2 act2_route(float2 hx) {
 }
 
 // act(x) and act'(x) for two lanes from hx = x / 2 (SFU route).
-//   GELU: act' = s + x s (1 - s) k'(x), s = (1 + t) / 2, s (1 - s) = (1 - t^2) / 4,
-//         k'(x) / 2 = a / 2 + 6 b hx^2  ->  act' = s + hx (1 - t^2) k'/2
+//   GELU: act' = Phi(x) + x phi(x) with Phi(x) ~ s = (1 + t) / 2 (the same
+//         tanh as the value) and x phi(x) = x e^(-x^2/2) / sqrt(2 pi)
+//         = hx 2^w, w = -2 log2(e) hx^2 + log2(2 / sqrt(2 pi)), from one ex2
+//         (the special-function unit has room in the backward, the FMA pipe
+//         does not: this takes two fewer packed FMAs than differentiating
+//         x s(k(x)), and its error against exact GELU' is smaller, 4.1e-4
+//         against 8.7e-4)
 //   SiLU: act' = s + x s (1 - s) = s + hx (1 - t^2) / 2
+constexpr float kLog2TwoOverSqrt2Pi = -0.3257480647361593f;
 template <int ACT>
 __device__ __forceinline__ float2 act2_d_sfu(float2 hx, float2& dy) {
   const float2 h2 = __fmul2_rn(hx, hx);
   float2 u = hx;
   if constexpr (ACT == 0) u = __fmul2_rn(hx, __ffma2_rn(h2, f2(4.0f * kGeluB), f2(kGeluA)));
   const float2 t = tanh2_sfu(u);
-  const float2 q = __ffma2_rn(make_float2(-t.x, -t.y), t, f2(1.0f));
   const float2 s = __ffma2_rn(t, f2(0.5f), f2(0.5f));
-  float2 kp;
-  if constexpr (ACT == 0) kp = __ffma2_rn(h2, f2(6.0f * kGeluB), f2(0.5f * kGeluA));
-  else kp = f2(0.5f);
-  dy = __ffma2_rn(__fmul2_rn(hx, q), kp, s);
+  if constexpr (ACT == 0) {
+    const float2 w = __ffma2_rn(h2, f2(-2.0f * kLog2e), f2(kLog2TwoOverSqrt2Pi));
+    dy = __ffma2_rn(hx, make_float2(ex2_sfu(w.x), ex2_sfu(w.y)), s);
+  } else {
+    const float2 q = __ffma2_rn(make_float2(-t.x, -t.y), t, f2(1.0f));
+    dy = __ffma2_rn(__fmul2_rn(hx, q), f2(0.5f), s);
+  }
   return __ffma2_rn(hx, t, hx);
 }
 // ALU route: with s = sigmoid(k), s (1 - s) = e s^2 (e = 2^(-k log2 e)):
