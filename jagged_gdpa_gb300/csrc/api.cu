@@ -30,6 +30,9 @@ cudaError_t launch_dbias_reduce(const unsigned long long* part, float* dbias, in
                                 cudaStream_t stream);
 cudaError_t launch_dq_shared_reduce(const float* part, void* dq, int batch, int64_t n, const int* status,
                                     cudaStream_t stream);
+cudaError_t launch_dq_fused_reduce(const float* part, float* tmp, void* dq, const int32_t* item_base, int batch,
+                                   int heads, int rows, int d, const int* status, cudaStream_t stream);
+size_t dq_fused_tmp_floats(int heads, int rows, int d);
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t stream);
 
 cudaError_t launch_fwd(const FwdParams& p, int head_dim, int act, int grid, cudaStream_t stream) {
@@ -151,6 +154,9 @@ struct Layout {
   size_t ds_base = 0;     // bwd: first stored-dS tile per segment, int64 [batch + 1]
   size_t q_off = 0;       // shared queries: the synthesized query offsets S b, int32 [batch + 1]
   size_t dq_part = 0;     // shared queries, bwd: fp32 dQ of every segment's rows [batch S][H][d]
+  size_t dq_fused = 0;    // fused dQ (shared, S <= 128, d <= 64): [key items][H][S][d] fp32 blocks
+  size_t dq_fused_tmp = 0;  // its first-stage sums
+  bool fused_dq = false;
   size_t total = 0;
   int max0 = 0, max1 = 0;
   int grid = 0;
@@ -158,6 +164,13 @@ struct Layout {
 
 int64_t max_units(int64_t total, int64_t batch, int rows_per_unit, int heads) {
   return (total / rows_per_unit + batch) * heads;
+}
+
+// Shared queries with at most one query tile and d <= 64: the key-major pass
+// has TMEM room to form each unit's dQ contribution itself, so the backward
+// stores no dS and runs no dQ pass (the fused split-dQ).
+bool fused_dq_applies(int32_t q_shared, int32_t head_dim) {
+  return q_shared > 0 && q_shared <= kTile && head_dim <= 64;
 }
 
 bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads, int32_t act, int32_t bias_len,
@@ -192,8 +205,18 @@ bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
   if (bwd) off += up((static_cast<size_t>(batch) + 1) * sizeof(int64_t));
   L->q_off = off;
   if (q_shared > 0) off += up((static_cast<size_t>(batch) + 1) * sizeof(int32_t));
+  L->fused_dq = bwd && fused_dq_applies(q_shared, head_dim);
   L->dq_part = off;
-  if (q_shared > 0 && bwd) off += up(static_cast<size_t>(total_q) * heads * head_dim * sizeof(float));
+  if (q_shared > 0 && bwd && !L->fused_dq)
+    off += up(static_cast<size_t>(total_q) * heads * head_dim * sizeof(float));
+  L->dq_fused = off;
+  L->dq_fused_tmp = off;
+  if (L->fused_dq) {
+    const size_t items = static_cast<size_t>(m0 / heads);  // key tiles, all segments
+    off += up(items * heads * q_shared * head_dim * sizeof(float));
+    L->dq_fused_tmp = off;
+    off += up(jg::dq_fused_tmp_floats(heads, q_shared, head_dim) * sizeof(float));
+  }
   L->total = off;
   return true;
 }
@@ -448,6 +471,11 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     return JGDPA_ERR_CUDA;
   if (workspace == nullptr || workspace_bytes < L.total) return JGDPA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, kAlign)) return JGDPA_ERR_MISALIGNED;
+  // the fused dQ needs no stored dS: a scratch the caller passes is not used
+  if (L.fused_dq) {
+    ds_scratch = nullptr;
+    ds_scratch_bytes = 0;
+  }
   // stored dS: capacity in tiles (the device checks the lengths against it)
   const int64_t ds_tiles = ds_scratch ? static_cast<int64_t>(ds_scratch_bytes / jg::kDsTileBytes) : -1;
   if (ds_scratch && !aligned(ds_scratch, kAlign)) return JGDPA_ERR_MISALIGNED;
@@ -482,7 +510,12 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
       !make_map(&p.tm_v, v, total_kv, heads, head_dim) || !make_map(&p.tm_do, dout, total_q, heads, head_dim))
     return JGDPA_ERR_CUDA;
   p.q_shared = q_shared > 0 ? 1 : 0;
-  p.dq_part = q_shared > 0 ? reinterpret_cast<float*>(ws + L.dq_part) : nullptr;
+  p.dq_part = (q_shared > 0 && !L.fused_dq) ? reinterpret_cast<float*>(ws + L.dq_part) : nullptr;
+  if (L.fused_dq) {
+    p.dq_fused = reinterpret_cast<float*>(ws + L.dq_fused);
+    p.kv_item_base = reinterpret_cast<const int32_t*>(ws + L.item_base);  // list 0: the key tiles
+    p.q_rows = q_shared;
+  }
   if (stored_ds) {
     if (!make_ds_map(&p.tm_ds, ds_scratch, ds_tiles)) return JGDPA_ERR_CUDA;
     p.ds_base = reinterpret_cast<const int64_t*>(ws + L.ds_base);
@@ -521,11 +554,17 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   p.dbias_part = nullptr;
   p.units = reinterpret_cast<const jg::Unit*>(ws + L.units1);
   p.n_units = hdr + 2;
-  if (stored_ds) JG_CUDA(jg::launch_dq_ds(p, head_dim, grid_q, stream));
-  else JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
+  if (L.fused_dq) {  // dQ = the ordered sum of the key-major pass's contributions
+    JG_CUDA(jg::launch_dq_fused_reduce(p.dq_fused, reinterpret_cast<float*>(ws + L.dq_fused_tmp), dq,
+                                       p.kv_item_base, batch, heads, q_shared, head_dim, hdr, stream));
+  } else if (stored_ds) {
+    JG_CUDA(jg::launch_dq_ds(p, head_dim, grid_q, stream));
+  } else {
+    JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
+  }
   JG_CUDA(record(2));
   if (part) JG_CUDA(jg::launch_dbias_reduce(part, dbias, grid_kv, heads * bias_len, stream));
-  if (q_shared > 0)
+  if (q_shared > 0 && !L.fused_dq)
     JG_CUDA(jg::launch_dq_shared_reduce(p.dq_part, dq, batch, static_cast<int64_t>(q_shared) * heads * head_dim, hdr,
                                         stream));
   return JGDPA_OK;

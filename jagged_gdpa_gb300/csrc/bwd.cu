@@ -166,6 +166,22 @@ __device__ __forceinline__ void mma_tile_ts(uint32_t d_tmem, uint32_t a_lo, uint
   }
 }
 
+// C(tmem, 128 x D) = dS(128 x 128) * K(128 x D): the X tile (dS^T, K-major
+// [keys][queries]) read as the MN-major A operand is dS, and the key tile
+// ([keys][D], MN-major B) is K.
+template <int D>
+__device__ __forceinline__ void mma_ds_k(uint32_t d_tmem, uint32_t x_tile, uint32_t k_tile, bool leader) {
+  using C = TileCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(kTile, D, 1, 1);
+  const uint64_t a0 = mnmajor_desc0<kTile>(x_tile), b0 = mnmajor_desc0<D>(k_tile);
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk) {
+    const uint64_t aoff = static_cast<uint64_t>(kk * 16 * TileCfg<kTile>::kRowBytes) >> 4;
+    const uint64_t boff = static_cast<uint64_t>(kk * 16 * C::kRowBytes) >> 4;
+    if (leader) mma_ss(d_tmem, a0 + aoff, b0 + boff, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
 // Unit geometry.  KV-major units: x = b, y = h, z = kv tile.  Q-major: z = q tile.
 struct BwdUnit {
   int b, h, tile;
@@ -358,6 +374,12 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
         if (!(ok = mbar_wait_warp(&bars->x_full[xs], x.full_parity<C::kNumX>(), fail))) break;
         tc_fence_after();
         mma_tile_xs<D>(tmem + 256 + D, x_base + xs * C::kXBytes, q_t, i > 0, leader);
+        if constexpr (D <= 64) {
+          // fused dQ: this unit's whole contribution dS K (its only query
+          // tile), dS read from X as the MN-major A operand and K from the
+          // resident tile, into TMEM columns [256 + 2D, 256 + 3D)
+          if (p.dq_fused != nullptr) mma_ds_k<D>(tmem + 256 + 2 * D, x_base + xs * C::kXBytes, k_t, leader);
+        }
         if (leader) mma_commit(&bars->x_empty[xs]);
         if (leader) mma_commit(&bars->a_empty[sa]);  // Q(i): S^T(i) and dK(i) issued
         ++x.n;
@@ -505,6 +527,14 @@ __device__ void bwd_ds_store(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
   }
   if (leader) bulk_wait_all();
   __syncwarp();
+}
+
+// Fused dQ: row r (a shared query row) of the dQ contribution block of unit
+// (segment b, head h, key tile kt), [q_rows][D] fp32 per block.
+template <int D>
+__device__ __forceinline__ float* dq_fused_row(const BwdParams& p, const BwdUnit& u, int r) {
+  const int64_t block = (static_cast<int64_t>(__ldg(p.kv_item_base + u.b)) + u.tile) * p.heads + u.h;
+  return p.dq_fused + (block * p.q_rows + r) * D;
 }
 
 // --------------------------------------------------------- activation warps
@@ -687,6 +717,13 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     const float bc_lo = brow ? __ldg(brow) : 0.f, bc_hi = brow ? __ldg(brow + 2 * R) : 0.f;
 
     if (u.count == 0) {  // no partner rows: the gradient rows are zero
+      if constexpr (KV_MAJOR && D <= 64) {
+        if (p.dq_fused != nullptr && r < p.q_rows) {  // (so is this unit's dQ contribution)
+          float* dst = dq_fused_row<D>(p, u, r) + half * (D / 2);
+#pragma unroll
+          for (int c = 0; c < D / 2; c += 4) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
+        }
+      }
       if (row_ok) {
         if constexpr (KV_MAJOR) {
           __nv_bfloat16* dst = (half == 0 ? p.dv : p.dk) + (grow * H + u.h) * D;
@@ -965,6 +1002,28 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
                                  __uint_as_float(o[c + 2 * e + 1]) * p.scale);
               st_global_v4(dst + c0 + c, w[0], w[1], w[2], w[3]);
             }
+          }
+        }
+      }
+    }
+    if constexpr (KV_MAJOR && D <= 64) {
+      // fused dQ: this unit's contribution dS K (TMEM lanes are query rows),
+      // scaled by s, fp32; warpgroup h writes columns [h D/2, (h+1) D/2)
+      if (p.dq_fused != nullptr) {
+        const uint32_t t_dq = tmem + lane_off + 256 + 2 * D + (D / 2) * half;
+        float* dst = dq_fused_row<D>(p, u, r) + half * (D / 2);
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 16) {
+          uint32_t o[16];
+          tmem_ld16(t_dq + c0, o);
+          tmem_ld_wait16(o);
+          if (r < p.q_rows) {
+#pragma unroll
+            for (int c = 0; c < 16; c += 4)
+              st_global_v4(dst + c0 + c, __float_as_uint(__uint_as_float(o[c]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[c + 1]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[c + 2]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[c + 3]) * p.scale));
           }
         }
       }
@@ -1357,6 +1416,54 @@ cudaError_t launch_dq_shared_reduce(const float* part, void* dq, int batch, int6
   dq_shared_reduce_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
       part, static_cast<__nv_bfloat16*>(dq), batch, n, status);
   return cudaGetLastError();
+}
+
+// Fused dQ of shared queries: dq[s][h][c] = sum over key items i (in item
+// order) of the blocks part[i H + h][s][c].  Stage 1: kFusedChunks threads
+// per element each sum a contiguous, fixed range of items into tmp; stage 2
+// sums those in chunk order and rounds once.  The item count is read from the
+// scheduler's prefix (item_base[batch]); the split depends only on it, so
+// the result is the same bit for bit on every run.
+constexpr int kFusedChunks = 64;
+__global__ void dq_fused_stage1_kernel(const float* __restrict__ part, float* __restrict__ tmp,
+                                       const int32_t* __restrict__ item_base, int batch, int heads, int rows,
+                                       int d, const int* status) {
+  const int64_t per = static_cast<int64_t>(rows) * heads * d;  // elements of dq
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= per * kFusedChunks || *status != kOk) return;
+  const int chunk = static_cast<int>(t / per);
+  const int64_t e = t % per;  // (s, h, c) of [S][H][D]
+  const int s_row = static_cast<int>(e / (static_cast<int64_t>(heads) * d));
+  const int h = static_cast<int>((e / d) % heads), c = static_cast<int>(e % d);
+  const int n_items = item_base[batch];
+  const int len = (n_items + kFusedChunks - 1) / kFusedChunks;
+  const int i0 = chunk * len, i1 = min(n_items, i0 + len);
+  float acc = 0.f;
+  for (int i = i0; i < i1; ++i)
+    acc += part[((static_cast<int64_t>(i) * heads + h) * rows + s_row) * d + c];
+  tmp[t] = acc;
+}
+__global__ void dq_fused_stage2_kernel(const float* __restrict__ tmp, __nv_bfloat16* __restrict__ dq, int64_t per,
+                                       const int* status) {
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= per || *status != kOk) return;
+  float acc = 0.f;
+  for (int k = 0; k < kFusedChunks; ++k) acc += tmp[static_cast<int64_t>(k) * per + e];
+  dq[e] = __float2bfloat16_rn(acc);
+}
+
+cudaError_t launch_dq_fused_reduce(const float* part, float* tmp, void* dq, const int32_t* item_base, int batch,
+                                   int heads, int rows, int d, const int* status, cudaStream_t stream) {
+  const int64_t per = static_cast<int64_t>(rows) * heads * d;
+  if (per == 0) return cudaSuccess;
+  dq_fused_stage1_kernel<<<static_cast<unsigned>((per * kFusedChunks + 255) / 256), 256, 0, stream>>>(
+      part, tmp, item_base, batch, heads, rows, d, status);
+  dq_fused_stage2_kernel<<<static_cast<unsigned>((per + 255) / 256), 256, 0, stream>>>(
+      tmp, static_cast<__nv_bfloat16*>(dq), per, status);
+  return cudaGetLastError();
+}
+size_t dq_fused_tmp_floats(int heads, int rows, int d) {
+  return static_cast<size_t>(kFusedChunks) * rows * heads * d;
 }
 
 cudaError_t launch_dbias_reduce(const unsigned long long* part, float* dbias, int n_parts, int n,

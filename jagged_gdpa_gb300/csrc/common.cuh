@@ -151,6 +151,13 @@ struct BwdParams {
   unsigned long long wait_limit_ns;  // limit of one internal wait
   int32_t q_shared;        // 1: every segment reads the same query rows (Q map row 0 = its row 0)
   float* dq_part;          // q_shared: fp32 dQ of every segment's rows [total_q][H][D], summed afterwards
+  // Fused dQ (shared queries with at most 128 rows, d <= 64): the key-major
+  // pass also forms each unit's dQ contribution dS K and writes it in fp32 to
+  // dq_fused[(kv_item_base[b] + kt) H + h][q_rows][D]; no dS is stored and no
+  // dQ pass runs.  nullptr otherwise.
+  float* dq_fused;
+  const int32_t* kv_item_base;  // the scheduler's key-tile prefix per segment
+  int32_t q_rows;               // rows of each dq_fused block (the shared query count)
 };
 
 constexpr int kDsTileBytes = kTile * kTile * 2;
