@@ -333,9 +333,15 @@ def run_native(args, world, rank, local):
     def bwd(pass_events=None):
         call_bwd(dev_inputs, out, lse, results, pass_events)
 
-    # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, dQ, [dbias reduce]);
-    # shared queries add the offset kernel of each call and the dQ reduction
-    launches_per_step = 2 + 3 + int(softmax) + int(bias_len > 0) + (3 if shared else 0)
+    # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, [dbias reduce]) + the dQ
+    # kernels: with a dS scratch the stored-dS pass and the recompute pass (the
+    # segments whose tiles did not fit; an empty list here); shared queries add
+    # the offset kernel of each call and the dQ sum over segments, and with at
+    # most 128 of them at d <= 64 the key-major pass forms dQ itself (two
+    # reduction kernels, no dQ pass)
+    fused_dq = shared and n_shared <= 128 and hd <= 64
+    launches_per_step = 2 + 2 + int(softmax) + int(bias_len > 0) + (2 if shared else 0) + \
+        (2 if fused_dq else 2 + int(shared))
     for _ in range(args.warmup):
         fwd()
         bwd()

@@ -82,7 +82,7 @@ typedef enum {
     JGDPA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, bad enum, even bias_len */
     JGDPA_ERR_UNSUPPORTED = 2,        /* head_dim not in {32, 64, 128}, sizes beyond int32 rows */
     JGDPA_ERR_MISALIGNED = 3,         /* a tensor or the workspace is not suitably aligned */
-    JGDPA_ERR_WORKSPACE_TOO_SMALL = 4,  /* also device-detected: stored-dS scratch too small */
+    JGDPA_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace (or the no-alloc array) too small for the sizes */
     JGDPA_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
     JGDPA_ERR_BAD_OFFSETS = 6,        /* device-detected: offsets not monotone / wrong ends */
     JGDPA_ERR_DEVICE_TIMEOUT = 7      /* device-detected: an internal wait gave up */
@@ -192,11 +192,14 @@ JGDPA_API size_t jgdpa_ds_scratch_bytes(const int32_t* q_offsets_host, const int
  *       jgdpa_bwd.  With scratch the dK/dV pass writes every bf16 dS tile it
  *       forms to the scratch and the dQ pass is one streaming matmul
  *       dQ = s * dS K over the stored tiles, instead of recomputing S, dP and
- *       the activation derivative.  It needs jgdpa_ds_scratch_bytes(...)
- *       bytes; if the device finds the scratch too small for the actual
- *       lengths it records JGDPA_ERR_WORKSPACE_TOO_SMALL in the status word
- *       and computes nothing (read it with jgdpa_read_device_status).  The
- *       scratch contents need no initialisation and are clobbered.
+ *       the activation derivative.  jgdpa_ds_scratch_bytes(...) bytes hold
+ *       every segment's tiles; a smaller scratch is used as far as it goes:
+ *       the tiles are laid out segment by segment, the segments whose tiles
+ *       end within the scratch get the stored-dS dQ and the others (a suffix
+ *       of the batch) get their dQ by recomputation, so the results are the
+ *       same up to rounding whatever the scratch size.  A scratch smaller
+ *       than one tile (32 KB) is not used.  The scratch contents need no
+ *       initialisation and are clobbered.
  *   pass_events
  *       optional three CUDA events (cudaEvent_t, created by the caller on the
  *       current device; any entry, or pass_events itself, may be NULL),

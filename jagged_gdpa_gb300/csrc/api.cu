@@ -148,7 +148,8 @@ struct Layout {
   size_t header = 0;      // status word + unit counters
   size_t item_base = 0;   // scheduler scratch, 2 lists x (batch + 1)
   size_t units0 = 0;      // fwd units, or dkdv units
-  size_t units1 = 0;      // dq units (bwd)
+  size_t units1 = 0;      // dq units (bwd): all, or those of the segments with stored dS
+  size_t units2 = 0;      // bwd with a dS scratch: dq units of the segments recomputed
   size_t delta = 0;       // softmax bwd: [H][total_q]
   size_t dbias = 0;       // bwd with dbias: [grid][H][T] 64-bit fixed-point partial sums
   size_t ds_base = 0;     // bwd: first stored-dS tile per segment, int64 [batch + 1]
@@ -192,11 +193,13 @@ bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
   L->header = off;
   off += up(64 * sizeof(int));
   L->item_base = off;
-  off += up(2 * (static_cast<size_t>(batch) + 1) * sizeof(int32_t));
+  off += up(3 * (static_cast<size_t>(batch) + 1) * sizeof(int32_t));
   L->units0 = off;
   off += up(static_cast<size_t>(m0) * sizeof(jg::Unit));
   L->units1 = off;
   off += up(static_cast<size_t>(m1) * sizeof(jg::Unit));
+  L->units2 = off;
+  if (bwd) off += up(static_cast<size_t>(m1) * sizeof(jg::Unit));
   L->delta = off;
   if (bwd && act == JGDPA_ACT_SOFTMAX) off += up(static_cast<size_t>(heads) * total_q * sizeof(float));
   L->dbias = off;
@@ -317,12 +320,18 @@ jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batc
   sp.list[0].max_units = L.max0;
   sp.list[0].n_units = hdr + 1;
   sp.list[0].units = reinterpret_cast<jg::Unit*>(ws + L.units0);
-  sp.n_lists = bwd ? 2 : 1;
+  sp.n_lists = bwd ? (ds_capacity >= 0 ? 3 : 2) : 1;
   if (bwd) {
-    sp.list[1].kind = jg::kUnitsQ;
+    sp.list[1].kind = ds_capacity >= 0 ? jg::kUnitsQStored : jg::kUnitsQ;
     sp.list[1].max_units = L.max1;
     sp.list[1].n_units = hdr + 2;
     sp.list[1].units = reinterpret_cast<jg::Unit*>(ws + L.units1);
+  }
+  if (bwd && ds_capacity >= 0) {
+    sp.list[2].kind = jg::kUnitsQRecompute;
+    sp.list[2].max_units = L.max1;
+    sp.list[2].n_units = hdr + 3;
+    sp.list[2].units = reinterpret_cast<jg::Unit*>(ws + L.units2);
   }
   JG_CUDA(jg::launch_sched(sp, stream));
   JG_CUDA(cudaGetLastError());
@@ -501,8 +510,9 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     JG_CUDA(cudaGetLastError());
     q_offsets = qo;
   }
+  // (a scratch smaller than one tile is no scratch: every dQ is recomputed)
   st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, true, stream,
-                 ds_scratch ? std::max<int64_t>(ds_tiles, 0) : -1);
+                 stored_ds ? ds_tiles : -1);
   if (st != JGDPA_OK) return st;
 
   jg::BwdParams p{};
@@ -558,7 +568,12 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     JG_CUDA(jg::launch_dq_fused_reduce(p.dq_fused, reinterpret_cast<float*>(ws + L.dq_fused_tmp), dq,
                                        p.kv_item_base, batch, heads, q_shared, head_dim, hdr, stream));
   } else if (stored_ds) {
+    // dQ from the stored tiles for the segments that fit the scratch, then by
+    // recomputation for the rest (a pass with an empty list ends at once)
     JG_CUDA(jg::launch_dq_ds(p, head_dim, grid_q, stream));
+    p.units = reinterpret_cast<const jg::Unit*>(ws + L.units2);
+    p.n_units = hdr + 3;
+    JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
   } else {
     JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, false, grid_q, stream));
   }

@@ -505,10 +505,14 @@ __device__ void bwd_ds_store(const BwdParams& p, uint8_t* smem, BwdBars* bars, i
     if (idx >= n_units) break;
     const BwdUnit u = bwd_unit<true, WIN>(p, idx);
     if (u.count == 0) continue;
+    // a segment whose dS tiles do not fit the scratch gets its dQ by
+    // recomputation: nothing is stored, the X tiles are only released
+    const bool store = __ldg(p.ds_base + u.b) >= 0;
     for (int i = 0; i < u.count; ++i) {
       const int xs = x.slot<C::kNumX>();
       if (!(ok = mbar_wait_warp(&bars->x_full[xs], x.full_parity<C::kNumX>(), fail))) break;
-      if (leader) {
+      if (leader && !store) mbar_arrive(&bars->x_empty[xs]);
+      if (leader && store) {
         const int row = ds_row(p.ds_base, u.seg, u.b, u.h, u.tile, u.first + i, WIN ? p.window : 0);
         const uint8_t* src = x_base + xs * C::kXBytes;
         tma_store_2d_hint(&p.tm_ds, src, 0, row, policy);

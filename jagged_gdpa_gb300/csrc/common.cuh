@@ -16,6 +16,12 @@ enum UnitKind : int {
   kUnitsFwd = 0,   // (segment, head, pair of 128-row query tiles)
   kUnitsKv = 1,    // (segment, head, 128-row key/value tile): dK, dV
   kUnitsQ = 2,     // (segment, head, 128-row query tile): dQ
+  // With a stored-dS scratch: the query-tile units of the segments whose dS
+  // tiles fit the scratch (dQ from the stored tiles) and of the others (dQ by
+  // recomputation).  A segment's tiles fit when the prefix of the tile counts
+  // up to and including it is within the scratch's capacity.
+  kUnitsQStored = 3,
+  kUnitsQRecompute = 4,
 };
 
 // One work unit: x = segment, y = head, z = tile (or tile pair) index, w = cost.
@@ -39,9 +45,12 @@ struct SchedParams {
   int32_t window;       // > 0: sliding window |i - j| < window
   int* status;
   int32_t* item_base;   // scratch [batch + 1] per list
-  SchedList list[2];
+  SchedList list[3];
   int n_lists;
-  int64_t* ds_base;     // backward with stored dS: first dS tile of each segment [batch + 1], or nullptr
+  // backward with stored dS: first dS tile of each segment, or -1 for a
+  // segment whose tiles do not fit ([batch + 1]; entry batch = tiles used);
+  // nullptr without a scratch
+  int64_t* ds_base;
   int64_t ds_capacity;  // dS tiles the caller's scratch holds
 };
 
@@ -147,7 +156,7 @@ struct BwdParams {
   // h, key tile kt, query tile qt) = ds_base[b] + (h nk_b + kt) span_b +
   // slot (see ds_span / ds_slot).
   CUtensorMap tm_ds;       // 2-D over the scratch: 128 columns x (tiles * 128) rows
-  const int64_t* ds_base;  // nullptr: no stored dS
+  const int64_t* ds_base;  // nullptr: no stored dS; entry < 0: that segment's dS is not stored
   unsigned long long wait_limit_ns;  // limit of one internal wait
   int32_t q_shared;        // 1: every segment reads the same query rows (Q map row 0 = its row 0)
   float* dq_part;          // q_shared: fp32 dQ of every segment's rows [total_q][H][D], summed afterwards

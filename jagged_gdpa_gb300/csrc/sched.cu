@@ -18,11 +18,21 @@ namespace jg {
 namespace {
 
 constexpr int kSchedThreads = 1024;
+constexpr int kSmemBase = 6144;  // segments whose item prefix is searched in shared memory
 
-__device__ int items_of_segment(int kind, const Seg& s) {
+// Items of segment s in a list of this kind; `stored` tells whether the
+// segment's dS tiles fit the scratch (used by the two split query lists).
+__device__ int items_of_segment(int kind, const Seg& s, bool stored) {
   if (kind == kUnitsFwd) return ceil_div(s.lq, 2 * kTile);
   if (kind == kUnitsKv) return ceil_div(s.lkv, kTile);
+  if (kind == kUnitsQStored && !stored) return 0;
+  if (kind == kUnitsQRecompute && stored) return 0;
   return ceil_div(s.lq, kTile);
+}
+
+// dS tiles of segment s in the scratch: H nk span (see ds_span).
+__device__ long long ds_tiles_of_segment(const SchedParams& p, const Seg& s) {
+  return static_cast<long long>(p.heads) * ceil_div(s.lkv, kTile) * ds_span(ceil_div(s.lq, kTile), p.window);
 }
 
 __device__ int cost_of_item(int kind, const Seg& s, int tile, int causal, int window) {
@@ -33,7 +43,7 @@ __device__ int cost_of_item(int kind, const Seg& s, int tile, int causal, int wi
     return c;
   }
   if (kind == kUnitsKv) return q_span_for_kv_tile(tile, s.lq, causal, window).count + 1;
-  return kv_span_for_q_tile(tile, s.lkv, causal, window).count + 1;
+  return kv_span_for_q_tile(tile, s.lkv, causal, window).count + 1;  // the query lists
 }
 
 // Inclusive scan of one value per thread over the whole block.
@@ -90,6 +100,7 @@ __device__ long long block_inclusive_scan64(long long v, long long* warp_tot) {
 
 __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_constant__ SchedParams p) {
   __shared__ int hist[kCostBuckets];
+  __shared__ int32_t base_sm[kSmemBase];
   __shared__ int warp_tot[32];
   __shared__ int bad;
   __shared__ int carry;
@@ -123,47 +134,39 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
     return;
   }
 
-  // ---- stored dS (backward): first scratch tile of each segment, H nk span
-  // tiles per segment (span: ds_span), checked against the caller's capacity
-  if (p.ds_base != nullptr && blockIdx.x == 0) {
-    __shared__ long long warp_tot64[32];
-    __shared__ long long carry64;
-    if (tid == 0) carry64 = 0;
-    __syncthreads();
-    for (int c0 = 0; c0 < p.batch; c0 += kSchedThreads) {
-      const int b = c0 + tid;
-      long long v = 0;
-      if (b < p.batch) {
-        const Seg sg = load_seg(p.q_off, p.kv_off, b);
-        v = static_cast<long long>(p.heads) * ceil_div(sg.lkv, kTile) * ds_span(ceil_div(sg.lq, kTile), p.window);
-      }
-      const long long incl = block_inclusive_scan64(v, warp_tot64);
-      if (b < p.batch) p.ds_base[b] = carry64 + incl - v;
-      __syncthreads();
-      if (tid == kSchedThreads - 1) carry64 += incl;
-      __syncthreads();
-    }
-    if (tid == 0) {
-      p.ds_base[p.batch] = carry64;
-      if (carry64 > p.ds_capacity) {  // the scratch is too small for these lengths
-        atomicCAS(p.status, kOk, kErrScratchTooSmall);
-        *L.n_units = 0;
-      }
-    }
-    __syncthreads();
-    if (carry64 > p.ds_capacity) return;
-  }
-
-  // ---- items per segment, exclusive prefix sum into base[]
+  // ---- items per segment, exclusive prefix sum into base[].  With a stored
+  // dS scratch the dS tiles are laid out in segment order (H nk span tiles per
+  // segment, span: ds_span); a segment is stored when its tiles end within
+  // the caller's capacity, so the stored segments are a prefix of the batch.
+  // The key list's CTA writes each segment's first tile (-1: not stored);
+  // every CTA recomputes the same prefix for its own decisions.
+  const bool split_q = L.kind == kUnitsQStored || L.kind == kUnitsQRecompute;
+  const bool ds_prefix = p.ds_base != nullptr && (blockIdx.x == 0 || split_q);
+  __shared__ long long warp_tot64[32];
+  __shared__ long long carry64;
+  if (tid == 0) carry64 = 0;
+  __syncthreads();
   for (int c0 = 0; c0 < p.batch; c0 += kSchedThreads) {
     const int b = c0 + tid;
-    const int v = b < p.batch ? items_of_segment(L.kind, load_seg(p.q_off, p.kv_off, b)) : 0;
+    const Seg sg = b < p.batch ? load_seg(p.q_off, p.kv_off, b) : Seg{0, 0, 0, 0};
+    bool stored = false;
+    if (ds_prefix) {
+      const long long need = b < p.batch ? ds_tiles_of_segment(p, sg) : 0;
+      const long long incl64 = carry64 + block_inclusive_scan64(need, warp_tot64);
+      stored = incl64 <= p.ds_capacity;
+      if (blockIdx.x == 0 && b < p.batch) p.ds_base[b] = stored ? incl64 - need : -1;
+      __syncthreads();
+      if (tid == kSchedThreads - 1) carry64 = incl64;
+      __syncthreads();
+    }
+    const int v = b < p.batch ? items_of_segment(L.kind, sg, stored) : 0;
     const int incl = block_inclusive_scan(v, warp_tot);
     if (b < p.batch) base[b] = carry + incl - v;
     __syncthreads();
     if (tid == kSchedThreads - 1) carry += incl;
     __syncthreads();
   }
+  if (ds_prefix && blockIdx.x == 0 && tid == 0) p.ds_base[p.batch] = carry64;
   const int n_items = carry;
   if (tid == 0) base[p.batch] = n_items;
   __syncthreads();
@@ -176,16 +179,25 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
     return;
   }
 
-  // ---- counting sort of items by decreasing cost
+  // ---- counting sort of items by decreasing cost.  Each item finds its
+  // segment by a binary search over the prefix; the prefix is copied to
+  // shared memory first when it fits (each search step is then a shared
+  // load instead of a dependent global one).
+  const int32_t* sbase = base;
+  if (p.batch + 1 <= kSmemBase) {
+    for (int b = tid; b <= p.batch; b += kSchedThreads) base_sm[b] = base[b];
+    __syncthreads();
+    sbase = base_sm;
+  }
   auto locate = [&](int it, int& b, int& tile) {
     int lo = 0, hi = p.batch - 1;  // largest b with base[b] <= it
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (base[mid] <= it) lo = mid;
+      if (sbase[mid] <= it) lo = mid;
       else hi = mid - 1;
     }
     b = lo;
-    tile = it - base[lo];
+    tile = it - sbase[lo];
   };
   for (int it = tid; it < n_items; it += kSchedThreads) {
     int b, tile;
