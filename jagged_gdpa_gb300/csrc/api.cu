@@ -20,6 +20,8 @@ namespace jg {
 template <int D>
 cudaError_t launch_fwd_d(const FwdParams& p, int act, int grid, cudaStream_t stream);
 template <int D>
+cudaError_t launch_fwd_shortq_d(const FwdParams& p, int act, int nq, int grid, cudaStream_t stream);
+template <int D>
 cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream);
 template <int D>
 cudaError_t launch_dq_ds_d(const BwdParams& p, int grid, cudaStream_t stream);
@@ -39,6 +41,12 @@ cudaError_t launch_fwd(const FwdParams& p, int head_dim, int act, int grid, cuda
   if (head_dim == 128) return launch_fwd_d<128>(p, act, grid, stream);
   if (head_dim == 64) return launch_fwd_d<64>(p, act, grid, stream);
   if (head_dim == 32) return launch_fwd_d<32>(p, act, grid, stream);
+  return cudaErrorInvalidValue;
+}
+cudaError_t launch_fwd_shortq(const FwdParams& p, int head_dim, int act, int nq, int grid, cudaStream_t stream) {
+  if (head_dim == 128) return launch_fwd_shortq_d<128>(p, act, nq, grid, stream);
+  if (head_dim == 64) return launch_fwd_shortq_d<64>(p, act, nq, grid, stream);
+  if (head_dim == 32) return launch_fwd_shortq_d<32>(p, act, nq, grid, stream);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_bwd_pass(const BwdParams& p, int head_dim, int act, bool kv_major, int grid,
@@ -67,6 +75,7 @@ namespace {
 using jg::kTile;
 
 constexpr size_t kAlign = 256;
+constexpr int kShortQMax = 64;  // largest shared query block the short-query forward takes
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Limit of one internal device wait for the kernels launched from now on
@@ -418,7 +427,12 @@ jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t
   p.scale = act == JGDPA_ACT_SOFTMAX ? scale * jg::kLog2e : scale;
   p.wait_limit_ns = wait_limit_ns();
   const int grid = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max0)));
-  JG_CUDA(jg::launch_fwd(p, head_dim, act, grid, stream));
+  // shared queries of at most 64 rows (GELU / SiLU): keys on the MMA's 128
+  // rows and the queries as N, so the activation touches only live elements
+  if (q_shared > 0 && q_shared <= kShortQMax && act != JGDPA_ACT_SOFTMAX)
+    JG_CUDA(jg::launch_fwd_shortq(p, head_dim, act, q_shared, grid, stream));
+  else
+    JG_CUDA(jg::launch_fwd(p, head_dim, act, grid, stream));
   return JGDPA_OK;
 }
 

@@ -29,18 +29,18 @@ def jg():
     return m
 
 
-def shared_case(seed, s, batch, heads, d, act, bias_len=0, causal=False, lkv_range=(1, 300)):
+def shared_case(seed, s, batch, heads, d, act, bias_len=0, causal=False, lkv_range=(1, 300), window=0):
     rng = np.random.default_rng(seed)
     lkv = rng.integers(lkv_range[0], lkv_range[1] + 1, size=batch)
     lkv[rng.integers(0, batch)] = 0  # one segment without keys
     return workloads.make_inputs(np.full(batch, s), lkv, heads, d, act, causal=causal, bias_len=bias_len,
-                                 rng=rng, shared_q=s)
+                                 rng=rng, shared_q=s, window=window)
 
 
 def run(jg, x, stored):
     d = x.to("cuda")
     out, lse = jg.jgdpa_fwd_shared_q(d.q_seed, d.k, d.v, d.kv_offsets, x.act, x.scale, bias_table=d.bias,
-                                     causal=x.causal)
+                                     causal=x.causal, window=x.window)
     scratch = None
     if stored:
         n = jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, x.heads)
@@ -49,7 +49,8 @@ def run(jg, x, stored):
     ws = torch.empty(jg.jgdpa_shared_q_workspace_bytes(x.batch, s, x.k.shape[0], x.heads, x.head_dim, x.act,
                                                        x.bias_len, True), dtype=torch.uint8, device="cuda")
     dq, dk, dv, db = jg.jgdpa_bwd_shared_q(d.q_seed, d.k, d.v, out, lse, d.dout, d.kv_offsets, x.act, x.scale,
-                                           bias_table=d.bias, causal=x.causal, workspace=ws, ds_scratch=scratch)
+                                           bias_table=d.bias, causal=x.causal, workspace=ws, ds_scratch=scratch,
+                                           window=x.window)
     torch.cuda.synchronize()
     assert jg.jgdpa_read_device_status(ws) == 0
     return out.cpu(), (None if lse is None else lse.cpu()), dq.cpu(), dk.cpu(), dv.cpu(), \
@@ -59,9 +60,10 @@ def run(jg, x, stored):
 def reference(x, units=None):
     s = x.q_seed.shape[0]
     o, lse = oracle.fwd(x.q_seed, x.k, x.v, x.q_offsets, x.kv_offsets, x.heads, x.head_dim, x.act, x.scale,
-                        bias=x.bias, causal=x.causal, q_shared=s, units=units)
+                        bias=x.bias, causal=x.causal, q_shared=s, units=units, window=x.window)
     dq, dk, dv, db = oracle.bwd(x.q_seed, x.k, x.v, x.dout, x.q_offsets, x.kv_offsets, x.heads, x.head_dim,
-                                x.act, x.scale, bias=x.bias, causal=x.causal, q_shared=s, units=units)
+                                x.act, x.scale, bias=x.bias, causal=x.causal, q_shared=s, units=units,
+                                window=x.window)
     return o, lse, dq, dk, dv, db
 
 
@@ -89,10 +91,31 @@ def test_shared_queries_match_the_oracle(jg, d, act, s, bias_len, causal, stored
         assert_close(f"dbias {tag}", db, rb)
 
 
+# the short-query forward (keys on the MMA's rows; GELU / SiLU, S <= 64) at
+# each of its widths NQ = 16, 32, 64, with bias, causal masking and a window
+SHORT = [(d, act, s, causal, w) for d in (64, 128) for act in ("gelu", "silu") for (s, causal, w) in
+         ((5, False, 0), (20, True, 0), (40, False, 0), (64, False, 37), (33, True, 130))]
+
+
+@pytest.mark.parametrize("d,act,s,causal,w", SHORT)
+def test_short_query_forward_widths(jg, d, act, s, causal, w):
+    x = shared_case(7100 + d + s + w, s, batch=7, heads=2, d=d, act=act, bias_len=7, causal=causal,
+                    lkv_range=(1, 400), window=w)
+    out, _, dq, dk, dv, db = run(jg, x, stored=True)
+    ro, _, rq, rk, rv, rb = reference(x)
+    tag = f"short-query d={d} {act} S={s} causal={causal} window={w}"
+    assert_close(f"O {tag}", out, ro)
+    assert_close(f"dQ {tag}", dq, rq)
+    assert_close(f"dK {tag}", dk, rk)
+    assert_close(f"dV {tag}", dv, rv)
+    assert_close(f"dbias {tag}", db, rb)
+
+
 def test_shared_queries_equal_the_expanded_batch(jg):
-    """The shared-query call gives the same O, dK, dV bits as the regular
-    call on the expanded batch, and its dQ matches the expanded dQ summed
-    over segments."""
+    """The shared-query call matches the regular call on the expanded batch:
+    the same dK, dV bits (the same key-major pass), O within the parity bar
+    (the short-query forward sums in another order), and dQ equal to the
+    expanded dQ summed over segments."""
     x = shared_case(77, 16, batch=9, heads=3, d=64, act="silu")
     out, _, dq, dk, dv, _ = run(jg, x, stored=True)
     d = x.to("cuda")
@@ -100,7 +123,7 @@ def test_shared_queries_equal_the_expanded_batch(jg):
     n = jg.jgdpa_ds_scratch_bytes(x.q_offsets, x.kv_offsets, x.heads)
     dq2, dk2, dv2, _ = jg.jgdpa_bwd(d.q, d.k, d.v, None, None, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
                                    ds_scratch=torch.empty(n, dtype=torch.uint8, device="cuda"))
-    assert torch.equal(out, o2.cpu())
+    assert_close("O vs expanded O", out, o2.double().cpu().numpy())
     assert torch.equal(dk, dk2.cpu()) and torch.equal(dv, dv2.cpu())
     summed = dq2.float().cpu().view(x.batch, 16, x.heads, 64).sum(0)
     assert_close("dQ vs expanded dQ summed", dq, summed.double().numpy())
