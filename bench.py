@@ -103,9 +103,9 @@ WORKLOAD_TEXT = {
 # long-tail workload, from a one-pass ncu capture of the current kernels at
 # that size; emptied whenever a kernel changes after the capture.
 TRAFFIC = {
-    "gdpa_fwd_kernel": 1.484378e9 + 0.331805e9,
-    "gdpa_bwd_kernel (dK/dV pass)": 2.265223e9 + 13.140428e9,
-    "gdpa_bwd_kernel (dQ pass)": 12.911190e9 + 0.263775e9,
+    "gdpa_fwd_kernel": 1.468381e9 + 0.328024e9,
+    "gdpa_bwd_kernel (dK/dV pass)": 2.360132e9 + 13.150991e9,
+    "gdpa_bwd_kernel (dQ pass)": 12.909607e9 + 0.262244e9,
 }
 
 
