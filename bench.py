@@ -99,13 +99,17 @@ WORKLOAD_TEXT = {
 }
 
 
+# Workloads whose roofline is HBM (they stream more than L2 per step at a low
+# arithmetic intensity): their roofline object reports algorithmic GB/s.
+HBM_BOUND = (2, 3, 4)
+
 # dram__bytes_read.sum + dram__bytes_write.sum per launch on the full
 # long-tail workload, from a one-pass ncu capture of the current kernels at
 # that size; emptied whenever a kernel changes after the capture.
 TRAFFIC = {
     "gdpa_fwd_kernel": 1.468381e9 + 0.328024e9,
     "gdpa_bwd_kernel (dK/dV pass)": 2.360132e9 + 13.150991e9,
-    "gdpa_bwd_kernel (dQ pass)": 12.909607e9 + 0.262244e9,
+    "gdpa_dq_ds_kernel (dQ pass)": 12.909607e9 + 0.262244e9,
 }
 
 
@@ -339,7 +343,13 @@ def run_native(args, world, rank, local):
     # the offset kernel of each call and the dQ sum over segments, and with at
     # most 128 of them at d <= 64 the key-major pass forms dQ itself (two
     # reduction kernels, no dQ pass)
-    fused_dq = shared and n_shared <= 128 and hd <= 64
+    # which kernels the library runs for this workload (the same rules as its
+    # launcher): shared queries of at most 64 rows with GELU / SiLU take the
+    # short-query kernels (keys on the MMA's rows); the backward then writes
+    # one dQ contribution per key-tile chunk, as the key-major pass does for
+    # at most 128 shared rows at d <= 64, and dQ is their ordered sum
+    shortq = shared and n_shared <= 64 and not softmax
+    fused_dq = shortq or (shared and n_shared <= 128 and hd <= 64)
     launches_per_step = 2 + 2 + int(softmax) + int(bias_len > 0) + (2 if shared else 0) + \
         (2 if fused_dq else 2 + int(shared))
     for _ in range(args.warmup):
@@ -459,33 +469,63 @@ def run_native(args, world, rank, local):
     # forward's time includes the ~10 us
     # scheduling kernel of its call; the passes are timed by events recorded
     # between their launches inside the backward call.
+    # Algorithmic bytes per launch: the forward's b_fwd; the backward's b_bwd
+    # split into dQ (written by the second pass) and the rest (the first).
+    k_fwd = "gdpa_fwd_shortq_kernel" if shortq else "gdpa_fwd_kernel"
+    if shortq:
+        k_kv, k_q = "gdpa_bwd_shortq_kernel (dK, dV, dQ contributions)", "dq_fused_stage1/2 (dQ sum)"
+    elif fused_dq:
+        k_kv, k_q = "gdpa_bwd_kernel (dK/dV pass, dQ contributions)", "dq_fused_stage1/2 (dQ sum)"
+    else:
+        k_kv, k_q = "gdpa_bwd_kernel (dK/dV pass)", "gdpa_dq_ds_kernel (dQ pass)"
+    dq_bytes = float(dq.numel() * dq.element_size())
     kernels = {
-        "gdpa_fwd_kernel": (fwd_ms, f_fwd),
-        "gdpa_bwd_kernel (dK/dV pass)": (statistics.mean(ms_kv), 2.0 * f_fwd),
-        "gdpa_bwd_kernel (dQ pass)": (statistics.mean(ms_q), 0.5 * f_fwd),
+        k_fwd: (fwd_ms, f_fwd, b_fwd),
+        k_kv: (statistics.mean(ms_kv), 2.0 * f_fwd, b_bwd - dq_bytes),
+        k_q: (statistics.mean(ms_q), 0.5 * f_fwd, dq_bytes),
     }
+    hbm_bound = args.workload in HBM_BOUND
     # The kernels are timed in a region of well under a second at full clock,
     # so the denominator is the measured burst GEMM rate; the fraction of the
     # measured sustained rate (a seconds-long GEMM loop under the power cap)
     # is reported beside it.
     per_kernel = {k: {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                       "frac": round(fl / (ms * 1e-3) / 1e12 / bf16_burst, 4),
-                      "frac_of_sustained": round(fl / (ms * 1e-3) / 1e12 / bf16_sust, 4)}
-                  for k, (ms, fl) in kernels.items()}
+                      "frac_of_sustained": round(fl / (ms * 1e-3) / 1e12 / bf16_sust, 4),
+                      "algorithmic_gbs": round(by / (ms * 1e-3) / 1e9, 1),
+                      "hbm_frac": round(by / (ms * 1e-3) / 1e9 / hbm, 4)}
+                  for k, (ms, fl, by) in kernels.items()}
     # dram bytes per launch from the ncu capture above, valid for the full
     # long-tail workload only; with them each kernel also reports its DRAM
     # throughput against the measured copy bandwidth (the dQ pass streams the
     # stored dS tiles and is bound there, not on the tensor pipe)
     full_size = args.workload == 5 and not args.segments
     if full_size:
-        for k, (ms, _) in kernels.items():
+        for k, (ms, _, _) in kernels.items():
             if k in TRAFFIC:
                 gbs = TRAFFIC[k] / (ms * 1e-3) / 1e9
                 per_kernel[k].update({"dram_gb": round(TRAFFIC[k] / 1e9, 3), "dram_gbs": round(gbs, 1),
                                       "dram_frac": round(gbs / hbm, 4)})
     dom = max(kernels, key=lambda k: kernels[k][0])
-    dom_ms, dom_fl = kernels[dom]
+    dom_ms, dom_fl, dom_by = kernels[dom]
     traffic = TRAFFIC.get(dom) if full_size else None
+    if hbm_bound:  # bound by HBM (the survey's roofline for this workload): algorithmic GB/s
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(dom_by / (dom_ms * 1e-3) / 1e9, 1),
+                    "peak": hbm, "unit": "GB/s", "frac": round(dom_by / (dom_ms * 1e-3) / 1e9 / hbm, 4),
+                    "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic}
+    else:
+        roofline = {
+            "kernel": dom,
+            "bound": "tensor",
+            "achieved": round(dom_fl / (dom_ms * 1e-3) / 1e12, 2),
+            "peak": bf16_burst,
+            "unit": "TFLOP/s",
+            "frac": round(dom_fl / (dom_ms * 1e-3) / 1e12 / bf16_burst, 4),
+            "peak_kind": f"{peak_kind} bf16 burst (kernels timed in a {ms_total / 1e3:.2f} s region)",
+            "frac_of_sustained": round(dom_fl / (dom_ms * 1e-3) / 1e12 / bf16_sust, 4),
+            "peak_sustained": bf16_sust,
+            "traffic": traffic,
+        }
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -521,18 +561,7 @@ def run_native(args, world, rank, local):
         "step_ms_median": round(statistics.median(a + b for a, b in zip(ms_fwd, ms_bwd)), 4),
         "fwd_tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
         "bwd_tflops": round(f_bwd / (bwd_ms * 1e-3) / 1e12, 2),
-        "roofline": {
-            "kernel": dom,
-            "bound": "tensor",
-            "achieved": round(dom_fl / (dom_ms * 1e-3) / 1e12, 2),
-            "peak": bf16_burst,
-            "unit": "TFLOP/s",
-            "frac": round(dom_fl / (dom_ms * 1e-3) / 1e12 / bf16_burst, 4),
-            "peak_kind": f"{peak_kind} bf16 burst (kernels timed in a {ms_total / 1e3:.2f} s region)",
-            "frac_of_sustained": round(dom_fl / (dom_ms * 1e-3) / 1e12 / bf16_sust, 4),
-            "peak_sustained": bf16_sust,
-            "traffic": traffic,
-        },
+        "roofline": roofline,
         "kernels": per_kernel,
         "e2e": {
             "value": round(world * (f_fwd + f_bwd) / (ms_e2e * 1e-3) / 1e12, 2),

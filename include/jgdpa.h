@@ -232,16 +232,24 @@ JGDPA_API jgdpa_status jgdpa_bwd_ex(const void* q, const void* k, const void* v,
  *   out, dout  bf16 [batch S][heads][head_dim]
  *   lse        fp32 [heads][batch S] (SOFTMAX mode only, else NULL)
  *   dq         bf16 [S][heads][head_dim], written: sum over b of dQ_b,
- *              accumulated in fp32 in segment order (deterministic) and
- *              rounded once
+ *              accumulated in fp32 in a fixed order (the same bits on every
+ *              run) and rounded once
  *   kv_offsets, k, v, dk, dv, bias_table, dbias, causal, window, ds_scratch,
  *   pass_events
  *              as in jgdpa_bwd_ex (there are no query offsets: they are S b,
  *              formed in the workspace; the stored-dS scratch size is
  *              jgdpa_ds_scratch_bytes with query offsets S b)
- * The workspace must hold jgdpa_shared_q_workspace_bytes(...) bytes: the
- * backward keeps each segment's dQ rows in fp32 there ([batch S][heads]
- * [head_dim]) and a fixed-order reduction kernel sums them.  Errors as in
+ * The workspace must hold jgdpa_shared_q_workspace_bytes(...) bytes; what
+ * the backward keeps there depends on S:
+ *   S <= 64 with GELU / SiLU: the short-query kernels (the keys take the
+ *     MMA's 128 rows, the S queries are its N).  The backward writes one
+ *     fp32 [S][head_dim] dQ contribution per (segment, head, chunk of up to
+ *     16 key tiles) and sums them in a fixed order; ds_scratch is not used.
+ *   S <= 128 and head_dim <= 64 otherwise: the key-major pass writes one such
+ *     contribution per (segment, head, key tile); ds_scratch is not used.
+ *   otherwise: each segment's dQ rows in fp32 ([batch S][heads][head_dim]),
+ *     summed in segment order; ds_scratch as in jgdpa_bwd_ex.
+ * Errors as in
  * jgdpa_fwd / jgdpa_bwd; n_shared < 1 is INVALID_ARGUMENT, batch S beyond
  * int32 is UNSUPPORTED.
  */

@@ -29,7 +29,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libjgdpa.so")
 HEAD_DIMS = (32, 64, 128)
 SOURCES = ["api.cu", "sched.cu"]                 # compiled once
-PER_DIM_SOURCES = ["fwd.cu", "fwd_shortq.cu", "bwd.cu"]  # compiled once per head dimension
+PER_DIM_SOURCES = ["fwd.cu", "fwd_shortq.cu", "bwd.cu", "bwd_shortq.cu"]  # compiled once per head dimension
 HEADERS = ["act.cuh", "common.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -24,6 +24,8 @@ cudaError_t launch_fwd_shortq_d(const FwdParams& p, int act, int nq, int grid, c
 template <int D>
 cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream);
 template <int D>
+cudaError_t launch_bwd_shortq_d(const BwdParams& p, int act, int nq, int grid, cudaStream_t stream);
+template <int D>
 cudaError_t launch_dq_ds_d(const BwdParams& p, int grid, cudaStream_t stream);
 template <int D>
 cudaError_t launch_softmax_delta_d(const void* out, const void* dout, float* delta, int64_t total_q, int heads,
@@ -56,6 +58,12 @@ cudaError_t launch_bwd_pass(const BwdParams& p, int head_dim, int act, bool kv_m
   if (head_dim == 32) return launch_bwd_pass_d<32>(p, act, kv_major, grid, stream);
   return cudaErrorInvalidValue;
 }
+cudaError_t launch_bwd_shortq(const BwdParams& p, int head_dim, int act, int nq, int grid, cudaStream_t stream) {
+  if (head_dim == 128) return launch_bwd_shortq_d<128>(p, act, nq, grid, stream);
+  if (head_dim == 64) return launch_bwd_shortq_d<64>(p, act, nq, grid, stream);
+  if (head_dim == 32) return launch_bwd_shortq_d<32>(p, act, nq, grid, stream);
+  return cudaErrorInvalidValue;
+}
 cudaError_t launch_dq_ds(const BwdParams& p, int head_dim, int grid, cudaStream_t stream) {
   if (head_dim == 128) return launch_dq_ds_d<128>(p, grid, stream);
   if (head_dim == 64) return launch_dq_ds_d<64>(p, grid, stream);
@@ -75,7 +83,7 @@ namespace {
 using jg::kTile;
 
 constexpr size_t kAlign = 256;
-constexpr int kShortQMax = 64;  // largest shared query block the short-query forward takes
+constexpr int kShortQMax = 64;  // largest shared query block the short-query kernels take
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Limit of one internal device wait for the kernels launched from now on
@@ -119,16 +127,17 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a packed [rows][heads][d] bf16 tensor; box = 128 rows x 1 head
-// x min(d, 64) columns, swizzled to match the MMA operand layout.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int heads, int d) {
+// 3-D map over a packed [rows][heads][d] bf16 tensor; box = box_rows (128 by
+// default) rows x 1 head x min(d, 64) columns, swizzled to match the MMA
+// operand layout.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int heads, int d, int box_rows = kTile) {
   std::memset(m, 0, sizeof(*m));
   EncodeFn enc = encode_fn();
   if (!enc || rows <= 0) return false;
   const int box_cols = d < 64 ? d : 64;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), 1, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw = box_cols * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
@@ -182,6 +191,12 @@ int64_t max_units(int64_t total, int64_t batch, int rows_per_unit, int heads) {
 bool fused_dq_applies(int32_t q_shared, int32_t head_dim) {
   return q_shared > 0 && q_shared <= kTile && head_dim <= 64;
 }
+// Shared queries of at most kShortQMax rows with GELU / SiLU: the short-query
+// backward (keys on the MMA's rows, the queries as N), which also writes one
+// fp32 dQ contribution per unit for the same ordered reduction.
+bool shortq_bwd_applies(int32_t q_shared, int32_t act) {
+  return q_shared > 0 && q_shared <= kShortQMax && act != JGDPA_ACT_SOFTMAX;
+}
 
 bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads, int32_t act, int32_t bias_len,
                 bool bwd, Layout* L, int32_t q_shared = 0, int32_t head_dim = 0) {
@@ -217,14 +232,14 @@ bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
   if (bwd) off += up((static_cast<size_t>(batch) + 1) * sizeof(int64_t));
   L->q_off = off;
   if (q_shared > 0) off += up((static_cast<size_t>(batch) + 1) * sizeof(int32_t));
-  L->fused_dq = bwd && fused_dq_applies(q_shared, head_dim);
+  L->fused_dq = bwd && (fused_dq_applies(q_shared, head_dim) || shortq_bwd_applies(q_shared, act));
   L->dq_part = off;
   if (q_shared > 0 && bwd && !L->fused_dq)
     off += up(static_cast<size_t>(total_q) * heads * head_dim * sizeof(float));
   L->dq_fused = off;
   L->dq_fused_tmp = off;
   if (L->fused_dq) {
-    const size_t items = static_cast<size_t>(m0 / heads);  // key tiles, all segments
+    const size_t items = static_cast<size_t>(m0 / heads);  // key tiles (at least the chunks), all segments
     off += up(items * heads * q_shared * head_dim * sizeof(float));
     L->dq_fused_tmp = off;
     off += up(jg::dq_fused_tmp_floats(heads, q_shared, head_dim) * sizeof(float));
@@ -308,7 +323,8 @@ __global__ void eval_act_kernel(int act, int path, const float* x, int64_t n, fl
 
 jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batch, int32_t heads,
                           int64_t total_q, int64_t total_kv, int32_t causal, int32_t window, uint8_t* ws,
-                          const Layout& L, bool bwd, cudaStream_t stream, int64_t ds_capacity = -1) {
+                          const Layout& L, bool bwd, cudaStream_t stream, int64_t ds_capacity = -1,
+                          bool kv_chunks = false) {
   jg::SchedParams sp{};
   if (ds_capacity >= 0) {
     sp.ds_base = reinterpret_cast<int64_t*>(ws + L.ds_base);
@@ -325,18 +341,19 @@ jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batc
   int* hdr = reinterpret_cast<int*>(ws + L.header);
   sp.status = hdr;
   sp.item_base = reinterpret_cast<int32_t*>(ws + L.item_base);
-  sp.list[0].kind = bwd ? jg::kUnitsKv : jg::kUnitsFwd;
+  // (short-query backward: the key-tile chunks only, no query lists)
+  sp.list[0].kind = kv_chunks ? jg::kUnitsKvChunk : (bwd ? jg::kUnitsKv : jg::kUnitsFwd);
   sp.list[0].max_units = L.max0;
   sp.list[0].n_units = hdr + 1;
   sp.list[0].units = reinterpret_cast<jg::Unit*>(ws + L.units0);
-  sp.n_lists = bwd ? (ds_capacity >= 0 ? 3 : 2) : 1;
-  if (bwd) {
+  sp.n_lists = kv_chunks ? 1 : (bwd ? (ds_capacity >= 0 ? 3 : 2) : 1);
+  if (bwd && !kv_chunks) {
     sp.list[1].kind = ds_capacity >= 0 ? jg::kUnitsQStored : jg::kUnitsQ;
     sp.list[1].max_units = L.max1;
     sp.list[1].n_units = hdr + 2;
     sp.list[1].units = reinterpret_cast<jg::Unit*>(ws + L.units1);
   }
-  if (bwd && ds_capacity >= 0) {
+  if (bwd && !kv_chunks && ds_capacity >= 0) {
     sp.list[2].kind = jg::kUnitsQRecompute;
     sp.list[2].max_units = L.max1;
     sp.list[2].n_units = hdr + 3;
@@ -524,14 +541,19 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     JG_CUDA(cudaGetLastError());
     q_offsets = qo;
   }
+  const bool shortq = shortq_bwd_applies(q_shared, act);
   // (a scratch smaller than one tile is no scratch: every dQ is recomputed)
   st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, true, stream,
-                 stored_ds ? ds_tiles : -1);
+                 stored_ds ? ds_tiles : -1, shortq);
   if (st != JGDPA_OK) return st;
 
   jg::BwdParams p{};
-  if (!make_map(&p.tm_q, q, dq_rows, heads, head_dim) || !make_map(&p.tm_k, k, total_kv, heads, head_dim) ||
-      !make_map(&p.tm_v, v, total_kv, heads, head_dim) || !make_map(&p.tm_do, dout, total_q, heads, head_dim))
+  // the short-query backward loads its query and dO blocks as boxes of its
+  // block width (16, 32 or 64 rows)
+  const int q_box = shortq ? (q_shared <= 16 ? 16 : (q_shared <= 32 ? 32 : 64)) : kTile;
+  if (!make_map(&p.tm_q, q, dq_rows, heads, head_dim, q_box) || !make_map(&p.tm_k, k, total_kv, heads, head_dim) ||
+      !make_map(&p.tm_v, v, total_kv, heads, head_dim) ||
+      !make_map(&p.tm_do, dout, total_q, heads, head_dim, q_box))
     return JGDPA_ERR_CUDA;
   p.q_shared = q_shared > 0 ? 1 : 0;
   p.dq_part = (q_shared > 0 && !L.fused_dq) ? reinterpret_cast<float*>(ws + L.dq_part) : nullptr;
@@ -573,7 +595,8 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   p.units = reinterpret_cast<const jg::Unit*>(ws + L.units0);
   p.n_units = hdr + 1;
   JG_CUDA(record(0));
-  JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, true, grid_kv, stream));
+  if (shortq) JG_CUDA(jg::launch_bwd_shortq(p, head_dim, act, q_shared, grid_kv, stream));
+  else JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, true, grid_kv, stream));
   JG_CUDA(record(1));
   p.dbias_part = nullptr;
   p.units = reinterpret_cast<const jg::Unit*>(ws + L.units1);

@@ -22,7 +22,11 @@ enum UnitKind : int {
   // up to and including it is within the scratch's capacity.
   kUnitsQStored = 3,
   kUnitsQRecompute = 4,
+  // Short-query backward: (segment, head, chunk of up to kChunkTiles key
+  // tiles); z = the chunk index.
+  kUnitsKvChunk = 5,
 };
+constexpr int kChunkTiles = 16;
 
 // One work unit: x = segment, y = head, z = tile (or tile pair) index, w = cost.
 using Unit = int4;

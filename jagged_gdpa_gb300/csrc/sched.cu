@@ -25,6 +25,7 @@ constexpr int kSmemBase = 6144;  // segments whose item prefix is searched in sh
 __device__ int items_of_segment(int kind, const Seg& s, bool stored) {
   if (kind == kUnitsFwd) return ceil_div(s.lq, 2 * kTile);
   if (kind == kUnitsKv) return ceil_div(s.lkv, kTile);
+  if (kind == kUnitsKvChunk) return ceil_div(ceil_div(s.lkv, kTile), kChunkTiles);
   if (kind == kUnitsQStored && !stored) return 0;
   if (kind == kUnitsQRecompute && stored) return 0;
   return ceil_div(s.lq, kTile);
@@ -43,6 +44,7 @@ __device__ int cost_of_item(int kind, const Seg& s, int tile, int causal, int wi
     return c;
   }
   if (kind == kUnitsKv) return q_span_for_kv_tile(tile, s.lq, causal, window).count + 1;
+  if (kind == kUnitsKvChunk) return min(kChunkTiles, ceil_div(s.lkv, kTile) - tile * kChunkTiles) + 1;
   return kv_span_for_q_tile(tile, s.lkv, causal, window).count + 1;  // the query lists
 }
 
@@ -199,11 +201,22 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
     b = lo;
     tile = it - sbase[lo];
   };
-  for (int it = tid; it < n_items; it += kSchedThreads) {
-    int b, tile;
+  // Items of equal cost are counted and placed with one shared-memory atomic
+  // per group of equal buckets in a warp (many units often share one cost,
+  // and one atomic per item would serialise on that bucket).  Every lane of a
+  // warp walks the same rounds so that the warp-wide matches are complete.
+  const int lane = tid & 31;
+  auto bucket_of = [&](int it, int& b, int& tile, int& cost) -> int {
+    if (it >= n_items) return -1;
     locate(it, b, tile);
-    const int cost = cost_of_item(L.kind, load_seg(p.q_off, p.kv_off, b), tile, p.causal, p.window);
-    atomicAdd(&hist[kCostBuckets - 1 - min(cost, kCostBuckets - 1)], 1);
+    cost = cost_of_item(L.kind, load_seg(p.q_off, p.kv_off, b), tile, p.causal, p.window);
+    return kCostBuckets - 1 - min(cost, kCostBuckets - 1);
+  };
+  for (int c = 0; c < n_items; c += kSchedThreads) {
+    int b = 0, tile = 0, cost = 0;
+    const int bk = bucket_of(c + tid, b, tile, cost);
+    const unsigned grp = __match_any_sync(0xffffffffu, bk);
+    if (bk >= 0 && lane == __ffs(grp) - 1) atomicAdd(&hist[bk], __popc(grp));
   }
   __syncthreads();
   {
@@ -224,11 +237,16 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
     }
   }
   __syncthreads();
-  for (int it = tid; it < n_items; it += kSchedThreads) {
-    int b, tile;
-    locate(it, b, tile);
-    const int cost = cost_of_item(L.kind, load_seg(p.q_off, p.kv_off, b), tile, p.causal, p.window);
-    const int pos = atomicAdd(&hist[kCostBuckets - 1 - min(cost, kCostBuckets - 1)], 1);
+  for (int c = 0; c < n_items; c += kSchedThreads) {
+    int b = 0, tile = 0, cost = 0;
+    const int bk = bucket_of(c + tid, b, tile, cost);
+    const unsigned grp = __match_any_sync(0xffffffffu, bk);
+    const int leader = __ffs(grp) - 1;
+    int first = 0;
+    if (bk >= 0 && lane == leader) first = atomicAdd(&hist[bk], __popc(grp));
+    first = __shfl_sync(0xffffffffu, first, leader);
+    if (bk < 0) continue;
+    const int pos = first + __popc(grp & ((1u << lane) - 1u));
     for (int h = 0; h < p.heads; ++h)
       L.units[static_cast<int64_t>(pos) * p.heads + h] = make_int4(b, h, tile, cost);
   }

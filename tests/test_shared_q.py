@@ -91,14 +91,15 @@ def test_shared_queries_match_the_oracle(jg, d, act, s, bias_len, causal, stored
         assert_close(f"dbias {tag}", db, rb)
 
 
-# the short-query forward (keys on the MMA's rows; GELU / SiLU, S <= 64) at
-# each of its widths NQ = 16, 32, 64, with bias, causal masking and a window
-SHORT = [(d, act, s, causal, w) for d in (64, 128) for act in ("gelu", "silu") for (s, causal, w) in
+# the short-query forward and backward (keys on the MMA's rows; GELU / SiLU,
+# S <= 64) at each of their widths NQ = 16, 32, 64, with bias, causal masking
+# and a window
+SHORT = [(d, act, s, causal, w) for d in (32, 64, 128) for act in ("gelu", "silu") for (s, causal, w) in
          ((5, False, 0), (20, True, 0), (40, False, 0), (64, False, 37), (33, True, 130))]
 
 
 @pytest.mark.parametrize("d,act,s,causal,w", SHORT)
-def test_short_query_forward_widths(jg, d, act, s, causal, w):
+def test_short_query_widths(jg, d, act, s, causal, w):
     x = shared_case(7100 + d + s + w, s, batch=7, heads=2, d=d, act=act, bias_len=7, causal=causal,
                     lkv_range=(1, 400), window=w)
     out, _, dq, dk, dv, db = run(jg, x, stored=True)
@@ -111,11 +112,30 @@ def test_short_query_forward_widths(jg, d, act, s, causal, w):
     assert_close(f"dbias {tag}", db, rb)
 
 
+# segments of more than one chunk of key tiles (16 tiles = 2048 keys): each
+# chunk writes its own dQ contribution; the first two key tiles of every
+# segment meet the bias table's band (R = 128), the rest its first entry
+CHUNKS = [(d, act, s) for d in (32, 64, 128) for (act, s) in (("gelu", 16), ("silu", 48))]
+
+
+@pytest.mark.parametrize("d,act,s", CHUNKS)
+def test_short_query_backward_chunks(jg, d, act, s):
+    x = shared_case(7200 + d + s, s, batch=3, heads=2, d=d, act=act, bias_len=257, lkv_range=(1500, 5000))
+    out, _, dq, dk, dv, db = run(jg, x, stored=False)
+    ro, _, rq, rk, rv, rb = reference(x)
+    tag = f"short-query chunks d={d} {act} S={s}"
+    assert_close(f"O {tag}", out, ro)
+    assert_close(f"dQ {tag}", dq, rq)
+    assert_close(f"dK {tag}", dk, rk)
+    assert_close(f"dV {tag}", dv, rv)
+    assert_close(f"dbias {tag}", db, rb)
+
+
 def test_shared_queries_equal_the_expanded_batch(jg):
     """The shared-query call matches the regular call on the expanded batch:
-    the same dK, dV bits (the same key-major pass), O within the parity bar
-    (the short-query forward sums in another order), and dQ equal to the
-    expanded dQ summed over segments."""
+    O, dK and dV within the parity bar (the short-query kernels sum over the
+    16 query rows in another order than the 128-row tiles) and dQ equal to
+    the expanded dQ summed over segments."""
     x = shared_case(77, 16, batch=9, heads=3, d=64, act="silu")
     out, _, dq, dk, dv, _ = run(jg, x, stored=True)
     d = x.to("cuda")
@@ -124,7 +144,8 @@ def test_shared_queries_equal_the_expanded_batch(jg):
     dq2, dk2, dv2, _ = jg.jgdpa_bwd(d.q, d.k, d.v, None, None, d.dout, d.q_offsets, d.kv_offsets, x.act, x.scale,
                                    ds_scratch=torch.empty(n, dtype=torch.uint8, device="cuda"))
     assert_close("O vs expanded O", out, o2.double().cpu().numpy())
-    assert torch.equal(dk, dk2.cpu()) and torch.equal(dv, dv2.cpu())
+    assert_close("dK vs expanded dK", dk, dk2.double().cpu().numpy())
+    assert_close("dV vs expanded dV", dv, dv2.double().cpu().numpy())
     summed = dq2.float().cpu().view(x.batch, 16, x.heads, 64).sum(0)
     assert_close("dQ vs expanded dQ summed", dq, summed.double().numpy())
 
