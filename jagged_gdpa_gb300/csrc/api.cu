@@ -22,7 +22,8 @@ cudaError_t launch_fwd_d(const FwdParams& p, int act, int grid, cudaStream_t str
 template <int D>
 cudaError_t launch_fwd_shortq_d(const FwdParams& p, int act, int nq, int grid, cudaStream_t stream);
 template <int D>
-cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream,
+                              bool direct);
 template <int D>
 cudaError_t launch_bwd_shortq_d(const BwdParams& p, int act, int nq, int grid, cudaStream_t stream);
 template <int D>
@@ -51,11 +52,12 @@ cudaError_t launch_fwd_shortq(const FwdParams& p, int head_dim, int act, int nq,
   if (head_dim == 32) return launch_fwd_shortq_d<32>(p, act, nq, grid, stream);
   return cudaErrorInvalidValue;
 }
+// direct: the key-major pass over the units of the direct-dQ segments
 cudaError_t launch_bwd_pass(const BwdParams& p, int head_dim, int act, bool kv_major, int grid,
-                            cudaStream_t stream) {
-  if (head_dim == 128) return launch_bwd_pass_d<128>(p, act, kv_major, grid, stream);
-  if (head_dim == 64) return launch_bwd_pass_d<64>(p, act, kv_major, grid, stream);
-  if (head_dim == 32) return launch_bwd_pass_d<32>(p, act, kv_major, grid, stream);
+                            cudaStream_t stream, bool direct = false) {
+  if (head_dim == 128) return launch_bwd_pass_d<128>(p, act, kv_major, grid, stream, direct);
+  if (head_dim == 64) return launch_bwd_pass_d<64>(p, act, kv_major, grid, stream, direct);
+  if (head_dim == 32) return launch_bwd_pass_d<32>(p, act, kv_major, grid, stream, direct);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_bwd_shortq(const BwdParams& p, int head_dim, int act, int nq, int grid, cudaStream_t stream) {
@@ -168,6 +170,7 @@ struct Layout {
   size_t units0 = 0;      // fwd units, or dkdv units
   size_t units1 = 0;      // dq units (bwd): all, or those of the segments with stored dS
   size_t units2 = 0;      // bwd with a dS scratch: dq units of the segments recomputed
+  size_t units3 = 0;      // bwd: dkdv units of the segments whose dQ that pass forms directly
   size_t delta = 0;       // softmax bwd: [H][total_q]
   size_t dbias = 0;       // bwd with dbias: [grid][H][T] 64-bit fixed-point partial sums
   size_t ds_base = 0;     // bwd: first stored-dS tile per segment, int64 [batch + 1]
@@ -217,13 +220,15 @@ bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
   L->header = off;
   off += up(64 * sizeof(int));
   L->item_base = off;
-  off += up(3 * (static_cast<size_t>(batch) + 1) * sizeof(int32_t));
+  off += up(4 * (static_cast<size_t>(batch) + 1) * sizeof(int32_t));
   L->units0 = off;
   off += up(static_cast<size_t>(m0) * sizeof(jg::Unit));
   L->units1 = off;
   off += up(static_cast<size_t>(m1) * sizeof(jg::Unit));
   L->units2 = off;
   if (bwd) off += up(static_cast<size_t>(m1) * sizeof(jg::Unit));
+  L->units3 = off;
+  if (bwd) off += up(static_cast<size_t>(m0) * sizeof(jg::Unit));
   L->delta = off;
   if (bwd && act == JGDPA_ACT_SOFTMAX) off += up(static_cast<size_t>(heads) * total_q * sizeof(float));
   L->dbias = off;
@@ -324,8 +329,9 @@ __global__ void eval_act_kernel(int act, int path, const float* x, int64_t n, fl
 jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batch, int32_t heads,
                           int64_t total_q, int64_t total_kv, int32_t causal, int32_t window, uint8_t* ws,
                           const Layout& L, bool bwd, cudaStream_t stream, int64_t ds_capacity = -1,
-                          bool kv_chunks = false) {
+                          bool kv_chunks = false, bool dq_direct = false) {
   jg::SchedParams sp{};
+  sp.dq_direct = dq_direct ? 1 : 0;
   if (ds_capacity >= 0) {
     sp.ds_base = reinterpret_cast<int64_t*>(ws + L.ds_base);
     sp.ds_capacity = ds_capacity;
@@ -358,6 +364,13 @@ jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batc
     sp.list[2].max_units = L.max1;
     sp.list[2].n_units = hdr + 3;
     sp.list[2].units = reinterpret_cast<jg::Unit*>(ws + L.units2);
+  }
+  if (dq_direct) {  // the key-major units of the direct-dQ segments, last list
+    jg::SchedList& dl = sp.list[sp.n_lists++];
+    dl.kind = jg::kUnitsKvDirect;
+    dl.max_units = L.max0;
+    dl.n_units = hdr + 4;
+    dl.units = reinterpret_cast<jg::Unit*>(ws + L.units3);
   }
   JG_CUDA(jg::launch_sched(sp, stream));
   JG_CUDA(cudaGetLastError());
@@ -543,8 +556,11 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   }
   const bool shortq = shortq_bwd_applies(q_shared, act);
   // (a scratch smaller than one tile is no scratch: every dQ is recomputed)
+  // every backward but the fused-dQ ones forms the dQ of single-key-tile
+  // segments in its key-major pass
+  const bool dq_direct = !L.fused_dq;
   st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, true, stream,
-                 stored_ds ? ds_tiles : -1, shortq);
+                 stored_ds ? ds_tiles : -1, shortq, dq_direct);
   if (st != JGDPA_OK) return st;
 
   jg::BwdParams p{};
@@ -597,6 +613,11 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   JG_CUDA(record(0));
   if (shortq) JG_CUDA(jg::launch_bwd_shortq(p, head_dim, act, q_shared, grid_kv, stream));
   else JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, true, grid_kv, stream));
+  if (dq_direct) {  // the segments with one key tile: dK, dV and dQ in one pass
+    p.units = reinterpret_cast<const jg::Unit*>(ws + L.units3);
+    p.n_units = hdr + 4;
+    JG_CUDA(jg::launch_bwd_pass(p, head_dim, act, true, grid_kv, stream, true));
+  }
   JG_CUDA(record(1));
   p.dbias_part = nullptr;
   p.units = reinterpret_cast<const jg::Unit*>(ws + L.units1);
@@ -697,6 +718,8 @@ size_t jgdpa_ds_scratch_bytes(const int32_t* q_offsets_host, const int32_t* kv_o
     const int64_t lq = static_cast<int64_t>(q_offsets_host[b + 1]) - q_offsets_host[b];
     const int64_t lkv = static_cast<int64_t>(kv_offsets_host[b + 1]) - kv_offsets_host[b];
     if (lq < 0 || lkv < 0) return 0;
+    // (a segment whose dQ the key-major pass forms directly stores nothing)
+    if (jg::dq_direct_segment(static_cast<int>(lq), static_cast<int>(lkv), window)) continue;
     const int64_t nq = (lq + jg::kTile - 1) / jg::kTile, nk = (lkv + jg::kTile - 1) / jg::kTile;
     tiles += static_cast<uint64_t>(nk) * static_cast<uint64_t>(jg::ds_span(nq, window));
   }

@@ -101,6 +101,7 @@ struct BwdBars {
   uint64_t a_full[4], a_empty[4], b_full[4], b_empty[4];
   uint32_t tmem_base;
   int abort;
+  uint64_t dq_full, dq_empty;  // direct dQ of one query tile (dK/dV pass, DIRECT kernels)
 };
 
 // K-major operand at column offset kk*16 inside a [128][D] tile: byte
@@ -313,7 +314,16 @@ struct XRing {
 // shared X tile, so the two products of a tile never wait on each other for
 // X; the pass is bound by the activation warps, which hides the pipeline
 // switch between the TMEM-operand dV and the shared-operand MMAs.
-template <int D, bool WIN>
+// DIRECT (units of segments with dq_direct_segment only): after dK(i),
+// dQ(i) = dS(i) K of the unit's only key tile, complete, into kDqCol -- the
+// free columns past dK at d <= 64, dP^T's columns at d = 128 (once the
+// activation warps have read dP^T(i); dP^T(i+1) then waits until they have
+// read dQ(i)).  A separate instantiation, so that the general kernel's code
+// is not touched by it.
+template <int D>
+constexpr uint32_t kDqCol = D <= 64 ? 256 + 2 * D : 128;
+
+template <int D, bool WIN, bool DIRECT>
 __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units,
                            Fail fail) {
   using C = BwdCfg<D, true>;
@@ -321,9 +331,16 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
   const uint32_t a_base = smem_u32(smem + C::kAOff), b_base = smem_u32(smem + C::kBOff);
   const uint32_t x_base = smem_u32(smem + C::kXOff);
   uint32_t res_it = 0, st_it = 0, acc_it = 0, p_n = 0, dp_n = 0;
+  [[maybe_unused]] uint32_t dq_n = 0, dq_w = 0;
   XRing x;
   const bool leader = elect_one();
   bool ok = true;
+  // DIRECT: waits until the activation warps have read every dQ issued so far
+  [[maybe_unused]] auto dq_read = [&]() -> bool {
+    for (; dq_w < dq_n; ++dq_w)
+      if (!mbar_wait_warp(&bars->dq_empty, dq_w & 1, fail)) return false;
+    return true;
+  };
   for (int r = 0; ok; ++r) {
     const int idx = unit_index(r, blockIdx.x, gridDim.x);
     if (idx >= n_units) break;
@@ -341,6 +358,9 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
       mma_tile_nt<D>(tmem, k_t, a_base + sa * C::kTileBytes, leader);  // S^T = K Q^T
       if (leader) mma_commit(&bars->s_full);
       if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
+      if constexpr (DIRECT && D == 128) {  // (the previous unit's last dQ in dP^T's columns)
+        if (!(ok = dq_read())) break;
+      }
       if (!(ok = mbar_wait_warp(&bars->b_full[sb], (st_it / C::kStagesB) & 1, fail))) break;
       tc_fence_after();
       mma_tile_nt<D>(tmem + 128, v_t, b_base + sb * C::kTileBytes, leader);  // dP^T = V dO^T
@@ -380,12 +400,26 @@ __device__ void bwd_mma_kv(const BwdParams& p, uint8_t* smem, BwdBars* bars, uin
           // resident tile, into TMEM columns [256 + 2D, 256 + 3D)
           if (p.dq_fused != nullptr) mma_ds_k<D>(tmem + 256 + 2 * D, x_base + xs * C::kXBytes, k_t, leader);
         }
+        if constexpr (DIRECT) {  // dQ(i) = dS(i) K, complete: the segment has one key tile
+          if constexpr (D == 128) {  // into dP^T's columns, read by now
+            if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
+          } else {
+            if (!(ok = dq_read())) break;
+          }
+          tc_fence_after();
+          mma_ds_k<D>(tmem + kDqCol<D>, x_base + xs * C::kXBytes, k_t, leader);
+          if (leader) mma_commit(&bars->dq_full);
+          ++dq_n;
+        }
         if (leader) mma_commit(&bars->x_empty[xs]);
         if (leader) mma_commit(&bars->a_empty[sa]);  // Q(i): S^T(i) and dK(i) issued
         ++x.n;
       }
-      if (more) {  // dP^T of the next query tile, once dP^T(i) is in registers
+      if (more) {  // dP^T of the next query tile, once dP^T(i) (DIRECT, d = 128: and dQ(i)) is read
         if (!(ok = mbar_wait_warp(&bars->dp_free, (dp_n & 1) ^ 1, fail))) break;
+        if constexpr (DIRECT && D == 128) {
+          if (!(ok = dq_read())) break;
+        }
         if (!(ok = mbar_wait_warp(&bars->b_full[sb1], ((it + 1) / C::kStagesB) & 1, fail))) break;
         tc_fence_after();
         mma_tile_nt<D>(tmem + 128, v_t, b_base + sb1 * C::kTileBytes, leader);
@@ -687,7 +721,57 @@ __device__ __forceinline__ void phase_b_chunk(const uint32_t (&dv)[32], const fl
   }
 }
 
-template <int D, int ACT, bool KV_MAJOR, bool WIN>
+// DIRECT: dQ of query tile qt (key-major pass): TMEM lane r is query row r
+// of the tile; warpgroup `half` owns columns [half D/2, (half+1) D/2).
+// Scaled by s into dq (bf16), or into dq_part (fp32) with shared queries.
+template <int D>
+__device__ __forceinline__ bool read_dq(const BwdParams& p, BwdBars* bars, uint32_t t_dq, int half, int r, int q0,
+                                        int lq, int h, int qt, uint32_t parity, Fail fail) {
+  if (!mbar_wait(&bars->dq_full, parity, fail)) return false;
+  tc_fence_after();
+  const bool q_ok = qt * kTile + r < lq;
+  const int64_t qrow = (static_cast<int64_t>(q0) + qt * kTile + r) * p.heads + h;
+  constexpr int kChunk = D / 2 < 32 ? D / 2 : 32;
+#pragma unroll
+  for (int c0 = 0; c0 < D / 2; c0 += kChunk) {
+    uint32_t o[32];
+    if constexpr (kChunk == 32) {
+      tmem_ld32(t_dq + c0, o);
+      tmem_ld_wait(o);
+    } else {
+      uint32_t(&o16)[16] = *reinterpret_cast<uint32_t(*)[16]>(o);
+      tmem_ld16(t_dq + c0, o16);
+      tmem_ld_wait16(o16);
+    }
+    if (c0 + kChunk == D / 2) {  // every column of this tile's dQ is in registers
+      tc_fence_before();
+      mbar_arrive_warp(&bars->dq_empty);
+    }
+    if (q_ok) {
+      const int col = (D / 2) * half + c0;
+      if (p.dq_part) {
+#pragma unroll
+        for (int c = 0; c < kChunk; c += 4)
+          st_global_v4(p.dq_part + qrow * D + col + c, __float_as_uint(__uint_as_float(o[c]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[c + 1]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[c + 2]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[c + 3]) * p.scale));
+      } else {
+#pragma unroll
+        for (int c = 0; c < kChunk; c += 8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * p.scale, __uint_as_float(o[c + 2 * e + 1]) * p.scale);
+          st_global_v4(p.dq + qrow * D + col + c, w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  }
+  return true;
+}
+
+template <int D, int ACT, bool KV_MAJOR, bool WIN, bool DIRECT>
 __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32_t tmem, int n_units, Fail fail) {
   using C = BwdCfg<D, KV_MAJOR>;
   constexpr bool kSoftmax = ACT == 2;
@@ -703,6 +787,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
   const bool want_dbias = KV_MAJOR && p.dbias_part != nullptr;
   const int R = (p.bias_len - 1) / 2;
   uint32_t s_it = 0, dp_it = 0, acc_it = 0;
+  [[maybe_unused]] uint32_t dq_it = 0;
   XRing x;
   const float hs = 0.5f * p.scale;                 // x / 2 = hs S + bias / 2
   const float s2 = p.scale * kLog2e;               // softmax: x log2 e
@@ -840,6 +925,14 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         tc_fence_before();
         mbar_arrive_warp(&bars->p_full);
       }
+      if constexpr (DIRECT) {  // the previous query tile's dQ, before this tile's dP^T (d = 128: its columns)
+        if (i > 0) {
+          if (!(ok = read_dq<D>(p, bars, tmem + lane_off + kDqCol<D> + (D / 2) * half, half, r, u.seg.q0,
+                                u.seg.lq, u.h, pt - 1, dq_it & 1, fail)))
+            break;
+          ++dq_it;
+        }
+      }
 
       // ---- phase B: dP -> dS (bf16 into X), dbias partial sums
       if (!(ok = mbar_wait(&bars->dp_full, dp_it & 1, fail))) break;
@@ -908,6 +1001,12 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       }
     }
     if (!ok) break;
+    if constexpr (DIRECT) {
+      if (!read_dq<D>(p, bars, tmem + lane_off + kDqCol<D> + (D / 2) * half, half, r, u.seg.q0, u.seg.lq, u.h,
+                      u.first + u.count - 1, dq_it & 1, fail))
+        break;
+      ++dq_it;
+    }
 
     // epilogue
     if (!mbar_wait(&bars->acc_full, acc_it & 1, fail)) break;
@@ -1052,7 +1151,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
 }
 
 // ------------------------------------------------------------------- kernel
-template <int D, int ACT, bool KV_MAJOR, bool WIN>
+template <int D, int ACT, bool KV_MAJOR, bool WIN, bool DIRECT = false>
 __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D, KV_MAJOR>;
   extern __shared__ uint8_t smem_raw[];
@@ -1072,6 +1171,10 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
+    if constexpr (DIRECT) {
+      mbar_init(&bars->dq_full, 1);
+      mbar_init(&bars->dq_empty, 8);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->x_full[s], 8);
       // released by the consuming MMA's commit, plus the dS copy when stored
@@ -1106,10 +1209,10 @@ __global__ void __launch_bounds__(384, 1) gdpa_bwd_kernel(const __grid_constant_
       if (p.ds_base != nullptr) bwd_ds_store<D, WIN>(p, smem, bars, n_units, fail);
     }
   } else if (warp == 1) {
-    if constexpr (KV_MAJOR) bwd_mma_kv<D, WIN>(p, smem, bars, tmem, n_units, fail);
+    if constexpr (KV_MAJOR) bwd_mma_kv<D, WIN, DIRECT>(p, smem, bars, tmem, n_units, fail);
     else bwd_mma_q<D, WIN>(p, smem, bars, tmem, n_units, fail);
   } else if (warp >= 4) {
-    bwd_act<D, ACT, KV_MAJOR, WIN>(p, smem, bars, tmem, n_units, fail);
+    bwd_act<D, ACT, KV_MAJOR, WIN, DIRECT>(p, smem, bars, tmem, n_units, fail);
   }
   tc_fence_before();
   __syncthreads();
@@ -1353,18 +1456,27 @@ __global__ void dbias_reduce_kernel(const unsigned long long* __restrict__ part,
 #error "compile bwd.cu with -DJGDPA_HEAD_DIM=32, 64 or 128"
 #endif
 
-template <int D, int ACT, bool KV_MAJOR>
+template <int D, int ACT, bool KV_MAJOR, bool DIRECT = false>
 static cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t stream) {
   using C = BwdCfg<D, KV_MAJOR>;
-  auto kern = p.window > 0 ? gdpa_bwd_kernel<D, ACT, KV_MAJOR, true> : gdpa_bwd_kernel<D, ACT, KV_MAJOR, false>;
+  decltype(&gdpa_bwd_kernel<D, ACT, KV_MAJOR, false>) kern;
+  if constexpr (DIRECT) kern = gdpa_bwd_kernel<D, ACT, true, false, true>;  // (direct-dQ segments: no window)
+  else kern = p.window > 0 ? gdpa_bwd_kernel<D, ACT, KV_MAJOR, true> : gdpa_bwd_kernel<D, ACT, KV_MAJOR, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
+// direct: the key-major pass over the direct-dQ segments' units (DIRECT).
 template <int D>
-cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream) {
+cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream,
+                              bool direct) {
+  if (direct) {
+    if (act == 0) return launch_bwd_t<D, 0, true, true>(p, grid, stream);
+    if (act == 1) return launch_bwd_t<D, 1, true, true>(p, grid, stream);
+    return launch_bwd_t<D, 2, true, true>(p, grid, stream);
+  }
   if (kv_major) {
     if (act == 0) return launch_bwd_t<D, 0, true>(p, grid, stream);
     if (act == 1) return launch_bwd_t<D, 1, true>(p, grid, stream);
@@ -1374,7 +1486,7 @@ cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int gr
   if (act == 1) return launch_bwd_t<D, 1, false>(p, grid, stream);
   return launch_bwd_t<D, 2, false>(p, grid, stream);
 }
-template cudaError_t launch_bwd_pass_d<JGDPA_HEAD_DIM>(const BwdParams&, int, bool, int, cudaStream_t);
+template cudaError_t launch_bwd_pass_d<JGDPA_HEAD_DIM>(const BwdParams&, int, bool, int, cudaStream_t, bool);
 
 template <int D>
 cudaError_t launch_dq_ds_d(const BwdParams& p, int grid, cudaStream_t stream) {

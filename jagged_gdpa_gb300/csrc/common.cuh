@@ -25,6 +25,9 @@ enum UnitKind : int {
   // Short-query backward: (segment, head, chunk of up to kChunkTiles key
   // tiles); z = the chunk index.
   kUnitsKvChunk = 5,
+  // Key-major units of the segments whose dQ the key-major pass forms
+  // directly (dq_direct_segment); kUnitsKv then holds the others.
+  kUnitsKvDirect = 6,
 };
 constexpr int kChunkTiles = 16;
 
@@ -49,13 +52,14 @@ struct SchedParams {
   int32_t window;       // > 0: sliding window |i - j| < window
   int* status;
   int32_t* item_base;   // scratch [batch + 1] per list
-  SchedList list[3];
+  SchedList list[4];
   int n_lists;
   // backward with stored dS: first dS tile of each segment, or -1 for a
   // segment whose tiles do not fit ([batch + 1]; entry batch = tiles used);
   // nullptr without a scratch
   int64_t* ds_base;
   int64_t ds_capacity;  // dS tiles the caller's scratch holds
+  int32_t dq_direct;    // backward: segments with dq_direct_segment get no query-major units and no dS
 };
 
 // Lengths and tile counts of one segment.
@@ -102,6 +106,15 @@ __device__ __forceinline__ TileSpan q_span_for_kv_tile(int kt, int lq, int causa
   int lo = causal ? kt : 0, hi = ceil_div(lq, kTile);
   window_tiles(kt, window, lo, hi);
   return {lo, max(0, hi - lo)};
+}
+
+// A segment whose keys fit one tile: the key-major backward forms each query
+// tile's dQ itself (dS K with that key tile, complete after one product), so
+// the segment needs no stored dS and no query-major dQ units.
+// (Without a window only: under a window the single key tile may not reach
+// every query tile.)
+__host__ __device__ __forceinline__ bool dq_direct_segment(int lq, int lkv, int window) {
+  return window <= 0 && lq > 0 && lkv > 0 && lkv <= kTile;
 }
 
 // Index of the i-th unit processed by CTA c of G (serpentine over rounds, so

@@ -20,19 +20,28 @@ namespace {
 constexpr int kSchedThreads = 1024;
 constexpr int kSmemBase = 6144;  // segments whose item prefix is searched in shared memory
 
+__device__ __forceinline__ bool direct_dq(const SchedParams& p, const Seg& s) {
+  return p.dq_direct && dq_direct_segment(s.lq, s.lkv, p.window);
+}
+
 // Items of segment s in a list of this kind; `stored` tells whether the
 // segment's dS tiles fit the scratch (used by the two split query lists).
-__device__ int items_of_segment(int kind, const Seg& s, bool stored) {
+// Segments whose dQ the key-major pass forms directly have no query items.
+__device__ int items_of_segment(const SchedParams& p, int kind, const Seg& s, bool stored) {
   if (kind == kUnitsFwd) return ceil_div(s.lq, 2 * kTile);
-  if (kind == kUnitsKv) return ceil_div(s.lkv, kTile);
   if (kind == kUnitsKvChunk) return ceil_div(ceil_div(s.lkv, kTile), kChunkTiles);
+  if (kind == kUnitsKvDirect) return direct_dq(p, s) ? 1 : 0;
+  if (kind == kUnitsKv) return direct_dq(p, s) ? 0 : ceil_div(s.lkv, kTile);
+  if (direct_dq(p, s)) return 0;
   if (kind == kUnitsQStored && !stored) return 0;
   if (kind == kUnitsQRecompute && stored) return 0;
   return ceil_div(s.lq, kTile);
 }
 
-// dS tiles of segment s in the scratch: H nk span (see ds_span).
+// dS tiles of segment s in the scratch: H nk span (see ds_span); none for a
+// segment whose dQ the key-major pass forms directly.
 __device__ long long ds_tiles_of_segment(const SchedParams& p, const Seg& s) {
+  if (direct_dq(p, s)) return 0;
   return static_cast<long long>(p.heads) * ceil_div(s.lkv, kTile) * ds_span(ceil_div(s.lq, kTile), p.window);
 }
 
@@ -43,7 +52,7 @@ __device__ int cost_of_item(int kind, const Seg& s, int tile, int causal, int wi
     if (s.lq > t1 * kTile) c += kv_span_for_q_tile(t1, s.lkv, causal, window).count + 1;
     return c;
   }
-  if (kind == kUnitsKv) return q_span_for_kv_tile(tile, s.lq, causal, window).count + 1;
+  if (kind == kUnitsKv || kind == kUnitsKvDirect) return q_span_for_kv_tile(tile, s.lq, causal, window).count + 1;
   if (kind == kUnitsKvChunk) return min(kChunkTiles, ceil_div(s.lkv, kTile) - tile * kChunkTiles) + 1;
   return kv_span_for_q_tile(tile, s.lkv, causal, window).count + 1;  // the query lists
 }
@@ -156,12 +165,12 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const __grid_const
       const long long need = b < p.batch ? ds_tiles_of_segment(p, sg) : 0;
       const long long incl64 = carry64 + block_inclusive_scan64(need, warp_tot64);
       stored = incl64 <= p.ds_capacity;
-      if (blockIdx.x == 0 && b < p.batch) p.ds_base[b] = stored ? incl64 - need : -1;
+      if (blockIdx.x == 0 && b < p.batch) p.ds_base[b] = (stored && !direct_dq(p, sg)) ? incl64 - need : -1;
       __syncthreads();
       if (tid == kSchedThreads - 1) carry64 = incl64;
       __syncthreads();
     }
-    const int v = b < p.batch ? items_of_segment(L.kind, sg, stored) : 0;
+    const int v = b < p.batch ? items_of_segment(p, L.kind, sg, stored) : 0;
     const int incl = block_inclusive_scan(v, warp_tot);
     if (b < p.batch) base[b] = carry + incl - v;
     __syncthreads();
