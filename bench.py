@@ -337,12 +337,9 @@ def run_native(args, world, rank, local):
     def bwd(pass_events=None):
         call_bwd(dev_inputs, out, lse, results, pass_events)
 
-    # (scheduler, forward) + (scheduler, [softmax row dots], dK/dV, [dbias reduce]) + the dQ
-    # kernels: with a dS scratch the stored-dS pass and the recompute pass (the
-    # segments whose tiles did not fit; an empty list here); shared queries add
-    # the offset kernel of each call and the dQ sum over segments, and with at
-    # most 128 of them at d <= 64 the key-major pass forms dQ itself (two
-    # reduction kernels, no dQ pass)
+    # Kernels per step: ([shared-query offsets], scheduler, forward) +
+    # ([shared-query offsets], scheduler, [softmax row dots], dK/dV, [direct
+    # dQ], the dQ kernels, [dbias reduce], [shared dQ sum]).
     # which kernels the library runs for this workload (the same rules as its
     # launcher): shared queries of at most 64 rows with GELU / SiLU take the
     # short-query kernels (keys on the MMA's rows); the backward then writes
@@ -350,8 +347,16 @@ def run_native(args, world, rank, local):
     # at most 128 shared rows at d <= 64, and dQ is their ordered sum
     shortq = shared and n_shared <= 64 and not softmax
     fused_dq = shortq or (shared and n_shared <= 128 and hd <= 64)
-    launches_per_step = 2 + 2 + int(softmax) + int(bias_len > 0) + (2 if shared else 0) + \
-        (2 if fused_dq else 2 + int(shared))
+    # otherwise (no window) the segments whose keys fit one tile get their
+    # dQ from a second key-major launch over their own units (direct dQ)
+    dq_direct = not fused_dq and x.window == 0
+    # dQ kernels: the two reduction stages (fused), or the stored-dS pass and
+    # the recompute pass (a scratch of at least one tile), or the recompute
+    # pass alone
+    stored = ds_scratch.numel() >= 128 * 128 * 2
+    n_dq = 2 if fused_dq else (2 if stored else 1)
+    launches_per_step = (2 + int(shared)) + \
+        (2 + int(shared) + int(softmax) + int(dq_direct) + n_dq + int(bias_len > 0) + int(shared and not fused_dq))
     for _ in range(args.warmup):
         fwd()
         bwd()
@@ -479,10 +484,20 @@ def run_native(args, world, rank, local):
     else:
         k_kv, k_q = "gdpa_bwd_kernel (dK/dV pass)", "gdpa_dq_ds_kernel (dQ pass)"
     dq_bytes = float(dq.numel() * dq.element_size())
+    # the dQ product (f_fwd / 2) and the dQ rows of the direct-dQ segments
+    # (keys within one tile) belong to the first pass, the rest to the second
+    f_dq_direct, dq_bytes_direct = 0.0, 0.0
+    if dq_direct:
+        one = (np.asarray(x.lkv) >= 1) & (np.asarray(x.lkv) <= 128) & (np.asarray(x.lq) >= 1)
+        f_dq_direct = 2.0 * float(segment_pairs(x.lq, x.lkv, x.causal)[one].sum()) * heads * hd
+        # (shared queries: dQ is the S shared rows, summed after both passes)
+        dq_bytes_direct = 0.0 if shared else float(np.asarray(x.lq)[one].sum()) * heads * hd * 2
+        if one.any():
+            k_kv = "gdpa_bwd_kernel (dK/dV pass; dQ of the one-key-tile segments)"
     kernels = {
         k_fwd: (fwd_ms, f_fwd, b_fwd),
-        k_kv: (statistics.mean(ms_kv), 2.0 * f_fwd, b_bwd - dq_bytes),
-        k_q: (statistics.mean(ms_q), 0.5 * f_fwd, dq_bytes),
+        k_kv: (statistics.mean(ms_kv), 2.0 * f_fwd + f_dq_direct, b_bwd - dq_bytes + dq_bytes_direct),
+        k_q: (statistics.mean(ms_q), 0.5 * f_fwd - f_dq_direct, dq_bytes - dq_bytes_direct),
     }
     hbm_bound = args.workload in HBM_BOUND
     # The kernels are timed in a region of well under a second at full clock,
