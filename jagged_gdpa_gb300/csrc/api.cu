@@ -131,8 +131,42 @@ EncodeFn encode_fn() {
 
 // 3-D map over a packed [rows][heads][d] bf16 tensor; box = box_rows (128 by
 // default) rows x 1 head x min(d, 64) columns, swizzled to match the MMA
-// operand layout.
+// operand layout.  The last kMapCache encodings are kept (a map holds only
+// the address, extents, strides and box, so an entry stays valid for any
+// tensor of that address and shape), so that repeated calls with the same
+// tensors skip the driver's encode.
+constexpr int kMapCache = 64;
+struct MapEntry {
+  const void* ptr;
+  int64_t rows;
+  int heads, d, box_rows;
+  bool valid;
+  CUtensorMap map;
+};
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int heads, int d, int box_rows);
+
 bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int heads, int d, int box_rows = kTile) {
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (const MapEntry& e : g_maps)
+      if (e.valid && e.ptr == ptr && e.rows == rows && e.heads == heads && e.d == d && e.box_rows == box_rows) {
+        *m = e.map;
+        return true;
+      }
+  }
+  if (!encode_map(m, ptr, rows, heads, d, box_rows)) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry& e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCache;
+  e = MapEntry{ptr, rows, heads, d, box_rows, true, *m};
+  return true;
+}
+
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int heads, int d, int box_rows) {
   std::memset(m, 0, sizeof(*m));
   EncodeFn enc = encode_fn();
   if (!enc || rows <= 0) return false;

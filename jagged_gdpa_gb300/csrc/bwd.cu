@@ -1462,7 +1462,8 @@ static cudaError_t launch_bwd_t(const BwdParams& p, int grid, cudaStream_t strea
   decltype(&gdpa_bwd_kernel<D, ACT, KV_MAJOR, false>) kern;
   if constexpr (DIRECT) kern = gdpa_bwd_kernel<D, ACT, true, false, true>;  // (direct-dQ segments: no window)
   else kern = p.window > 0 ? gdpa_bwd_kernel<D, ACT, KV_MAJOR, true> : gdpa_bwd_kernel<D, ACT, KV_MAJOR, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  static DeviceFlags attr_set[2] = {};
+  cudaError_t e = smem_attr_once(kern, C::kSmemBytes, attr_set[!DIRECT && p.window > 0]);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
@@ -1492,7 +1493,8 @@ template <int D>
 cudaError_t launch_dq_ds_d(const BwdParams& p, int grid, cudaStream_t stream) {
   using C = DqCfg<D>;
   auto kern = gdpa_dq_ds_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  static DeviceFlags attr_set = {};
+  cudaError_t e = smem_attr_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
   kern<<<grid, 256, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();

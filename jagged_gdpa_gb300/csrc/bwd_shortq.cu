@@ -552,7 +552,8 @@ static cudaError_t launch_bsq_t(const BwdParams& p, int grid, cudaStream_t strea
   // at least half the SM's shared memory: one CTA per SM, so that a second
   // CTA never waits in its TMEM allocation for the first to finish
   constexpr int kSmem = BsqCfg<D, NQ>::kSmemBytes > 120 * 1024 ? BsqCfg<D, NQ>::kSmemBytes : 120 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  static DeviceFlags attr_set[2] = {};
+  cudaError_t e = smem_attr_once(kern, kSmem, attr_set[p.window > 0]);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, kSmem, stream>>>(p);
   return cudaGetLastError();

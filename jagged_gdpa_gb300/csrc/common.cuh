@@ -3,6 +3,9 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 namespace jg {
@@ -187,6 +190,23 @@ struct BwdParams {
 };
 
 constexpr int kDsTileBytes = kTile * kTile * 2;
+
+// Host side: a kernel's dynamic shared-memory limit is a per-device
+// attribute; each launcher keeps, per kernel, one flag per device and sets
+// the attribute only the first time it launches that kernel on a device.
+constexpr int kMaxDevices = 128;
+using DeviceFlags = std::atomic<unsigned char>[kMaxDevices];
+template <typename Kernel>
+inline cudaError_t smem_attr_once(Kernel kern, int bytes, DeviceFlags& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) done[dev].store(1, std::memory_order_release);
+  return e;
+}
 
 // dbias partial sums are 64-bit two's-complement fixed point with this many
 // fraction bits (resolution 2^-24, range +-2^39).  Integer additions are exact

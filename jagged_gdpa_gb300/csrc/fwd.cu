@@ -706,7 +706,8 @@ template <int D, int ACT>
 static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
   auto kern = p.window > 0 ? gdpa_fwd_kernel<D, ACT, kFwdAluChunks, true> : gdpa_fwd_kernel<D, ACT, kFwdAluChunks, false>;
   constexpr int kSmemBytes = FwdSmem<D, ACT>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static DeviceFlags attr_set[2] = {};
+  cudaError_t e = smem_attr_once(kern, kSmemBytes, attr_set[p.window > 0]);
   if (e != cudaSuccess) return e;
   kern<<<grid, 384, kSmemBytes, stream>>>(p);
   return cudaGetLastError();

@@ -399,7 +399,8 @@ template <int D, int ACT, int NQ>
 static cudaError_t launch_sq_t(const FwdParams& p, int grid, cudaStream_t stream) {
   auto kern = p.window > 0 ? gdpa_fwd_shortq_kernel<D, ACT, NQ, true> : gdpa_fwd_shortq_kernel<D, ACT, NQ, false>;
   constexpr int kSmem = SqCfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  static DeviceFlags attr_set[2] = {};
+  cudaError_t e = smem_attr_once(kern, kSmem, attr_set[p.window > 0]);
   if (e != cudaSuccess) return e;
   kern<<<grid, 256, kSmem, stream>>>(p);
   return cudaGetLastError();
