@@ -1412,26 +1412,39 @@ __global__ void __launch_bounds__(256, 1) gdpa_dq_ds_kernel(const __grid_constan
 }
 
 // delta_i = <dO_i, O_i> per (row, head), fp32 from bf16 (softmax backward).
+// D / 16 consecutive lanes share a row: each loads two 16-byte pieces of O
+// and of dO (lanes of a group read whole 128-byte lines, a warp 32 / (D / 16)
+// rows per load), and the group's partial sums are added by shuffles in a
+// fixed order.
 template <int D>
 __global__ void softmax_delta_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                                      float* __restrict__ delta, int64_t total_q, int heads, const int* status) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // row * heads + h
-  if (row >= total_q * heads || *status != kOk) return;
-  const uint4* o4 = reinterpret_cast<const uint4*>(out + row * D);
-  const uint4* d4 = reinterpret_cast<const uint4*>(dout + row * D);
+  constexpr int kLanes = D / 16;  // lanes per (row, head)
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = t / kLanes;  // row * heads + h
+  const int part = static_cast<int>(t % kLanes);
+  if (*status != kOk) return;
   float acc = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < D / 8; ++c) {
-    const uint4 a = __ldg(o4 + c), b = __ldg(d4 + c);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  if (row < total_q * heads) {
+    const uint4* o4 = reinterpret_cast<const uint4*>(out + row * D);
+    const uint4* d4 = reinterpret_cast<const uint4*>(dout + row * D);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      acc = __fmaf_rn(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
-      acc = __fmaf_rn(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(bw[e] & 0xFFFF0000u), acc);
+    for (int k = 0; k < 2; ++k) {
+      const uint4 a = __ldg(o4 + part + k * kLanes), b = __ldg(d4 + part + k * kLanes);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = __fmaf_rn(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
+        acc = __fmaf_rn(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(bw[e] & 0xFFFF0000u), acc);
+      }
     }
   }
-  const int64_t t = row / heads, h = row % heads;
-  delta[h * total_q + t] = acc;
+#pragma unroll
+  for (int o = kLanes / 2; o > 0; o >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, o, kLanes);
+  if (part == 0 && row < total_q * heads) {
+    const int64_t tq = row / heads, h = row % heads;
+    delta[h * total_q + tq] = acc;
+  }
 }
 
 #if JGDPA_HEAD_DIM == 128
@@ -1507,7 +1520,8 @@ cudaError_t launch_softmax_delta_d(const void* out, const void* dout, float* del
   const int64_t rows = total_q * heads;
   if (rows == 0) return cudaSuccess;
   const int threads = 256;
-  const unsigned blocks = static_cast<unsigned>((rows + threads - 1) / threads);
+  const int64_t lanes = rows * (D / 16);
+  const unsigned blocks = static_cast<unsigned>((lanes + threads - 1) / threads);
   softmax_delta_kernel<D><<<blocks, threads, 0, stream>>>(static_cast<const __nv_bfloat16*>(out),
                                                           static_cast<const __nv_bfloat16*>(dout), delta, total_q,
                                                           heads, status);
