@@ -174,3 +174,71 @@ def test_device_wait_timeout_is_reported_and_the_next_call_recovers(jg):
     assert_close("dQ after timeout", dq[q0:q1, h].cpu(), rq[:, h])
     assert_close("dK after timeout", dk[k0:k1, h].cpu(), rk[:, h])
     assert_close("dV after timeout", dv[k0:k1, h].cpu(), rv[:, h])
+
+
+def test_device_wait_timeout_in_the_short_query_and_direct_kernels(jg):
+    """The same bounded-wait contract for the short-query forward and
+    backward (shared query blocks of at most 64 rows; several chunks of key
+    tiles per segment) and for the direct-dQ key-major pass (segments whose
+    keys fit one tile, many query tiles each): with a 1 ns limit each call
+    reports JGDPA_ERR_DEVICE_TIMEOUT (7); with the default limit back the
+    next calls return status 0 and match the oracle."""
+    import oracle
+    from tests._util import assert_close
+    rng = np.random.default_rng(77)
+    batch, s_rows = 24, 16
+    lkv = rng.integers(2500, 4500, size=batch)
+    xs = workloads.make_inputs(np.full(batch, s_rows), lkv, 2, 64, "silu", rng=rng, shared_q=s_rows)
+    xd = workloads.random_case(33, batch=24, heads=2, head_dim=128, act="gelu", lq_range=(1500, 3000),
+                               lkv_range=(32, 128), bias_len=7)
+
+    def short_query_calls():
+        d = xs.to("cuda")
+        ws_f = torch.empty(jg.jgdpa_shared_q_workspace_bytes(xs.batch, s_rows, xs.k.shape[0], xs.heads,
+                                                             xs.head_dim, xs.act, 0, False),
+                           dtype=torch.uint8, device="cuda")
+        ws_b = torch.empty(jg.jgdpa_shared_q_workspace_bytes(xs.batch, s_rows, xs.k.shape[0], xs.heads,
+                                                             xs.head_dim, xs.act, 0, True),
+                           dtype=torch.uint8, device="cuda")
+        out, _ = jg.jgdpa_fwd_shared_q(d.q_seed, d.k, d.v, d.kv_offsets, xs.act, xs.scale, workspace=ws_f)
+        st_f = jg.jgdpa_read_device_status(ws_f)
+        dq, dk, dv, _ = jg.jgdpa_bwd_shared_q(d.q_seed, d.k, d.v, out, None, d.dout, d.kv_offsets, xs.act,
+                                              xs.scale, workspace=ws_b)
+        return st_f, jg.jgdpa_read_device_status(ws_b), out, dq, dk, dv
+
+    def direct_calls():
+        d = xd.to("cuda")
+        ws_b = torch.empty(jg.jgdpa_workspace_bytes(xd.batch, xd.q.shape[0], xd.k.shape[0], xd.heads, xd.head_dim,
+                                                    xd.act, xd.bias_len, True), dtype=torch.uint8, device="cuda")
+        dq, dk, dv, db = jg.jgdpa_bwd(d.q, d.k, d.v, None, None, d.dout, d.q_offsets, d.kv_offsets, xd.act,
+                                      xd.scale, bias_table=d.bias, workspace=ws_b)
+        return jg.jgdpa_read_device_status(ws_b), dq, dk, dv
+
+    try:
+        jg.jgdpa_set_wait_limit_ns(1)
+        st_f, st_b, *_ = short_query_calls()
+        assert st_f == 7 and st_b == 7
+        assert direct_calls()[0] == 7
+    finally:
+        jg.jgdpa_set_wait_limit_ns(0)
+    torch.cuda.synchronize()
+    st_f, st_b, out, dq, dk, dv = short_query_calls()
+    assert st_f == 0 and st_b == 0
+    ro, _ = oracle.fwd(xs.q_seed, xs.k, xs.v, xs.q_offsets, xs.kv_offsets, xs.heads, xs.head_dim, xs.act, xs.scale,
+                       q_shared=s_rows)
+    rq, rk, rv, _ = oracle.bwd(xs.q_seed, xs.k, xs.v, xs.dout, xs.q_offsets, xs.kv_offsets, xs.heads, xs.head_dim,
+                               xs.act, xs.scale, q_shared=s_rows)
+    assert_close("short-query O after timeout", out.cpu(), ro)
+    assert_close("short-query dQ after timeout", dq.cpu(), rq)
+    assert_close("short-query dK after timeout", dk.cpu(), rk)
+    assert_close("short-query dV after timeout", dv.cpu(), rv)
+    st, dq, dk, dv = direct_calls()
+    assert st == 0
+    b, h = 5, 1
+    sub = workloads.select_segments(xd, [b])
+    rq, rk, rv, _ = oracle.bwd_inputs(sub, units=[h])
+    q0, q1 = int(xd.q_offsets[b]), int(xd.q_offsets[b + 1])
+    k0, k1 = int(xd.kv_offsets[b]), int(xd.kv_offsets[b + 1])
+    assert_close("direct dQ after timeout", dq[q0:q1, h].cpu(), rq[:, h])
+    assert_close("direct dK after timeout", dk[k0:k1, h].cpu(), rk[:, h])
+    assert_close("direct dV after timeout", dv[k0:k1, h].cpu(), rv[:, h])

@@ -131,6 +131,24 @@ def test_short_query_backward_chunks(jg, d, act, s):
     assert_close(f"dbias {tag}", db, rb)
 
 
+@pytest.mark.parametrize("act", ["gelu", "silu"])
+def test_short_query_backward_chunk_edges(jg, act):
+    """Key counts at the short-query backward's edges: one and two tiles
+    around 128, exactly one chunk of 16 tiles (2048 keys), one key past it
+    (a second chunk of one tile), two full chunks, and no keys."""
+    rng = np.random.default_rng(7300)
+    lkv = np.array([2048, 2049, 1, 128, 129, 4096, 0])
+    x = workloads.make_inputs(np.full(len(lkv), 16), lkv, 2, 64, act, bias_len=257, rng=rng, shared_q=16)
+    out, _, dq, dk, dv, db = run(jg, x, stored=False)
+    ro, _, rq, rk, rv, rb = reference(x)
+    tag = f"short-query chunk edges {act}"
+    assert_close(f"O {tag}", out, ro)
+    assert_close(f"dQ {tag}", dq, rq)
+    assert_close(f"dK {tag}", dk, rk)
+    assert_close(f"dV {tag}", dv, rv)
+    assert_close(f"dbias {tag}", db, rb)
+
+
 def test_shared_queries_equal_the_expanded_batch(jg):
     """The shared-query call matches the regular call on the expanded batch:
     O, dK and dV within the parity bar (the short-query kernels sum over the
