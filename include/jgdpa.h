@@ -285,8 +285,9 @@ JGDPA_API jgdpa_status jgdpa_bwd_shared_q(const void* q, int32_t n_shared, const
  * Scratch comes from a fixed array of JGDPA_NOALLOC_SCRATCH_BYTES (4 MiB)
  * compiled into the library; every GPU that loads the library holds that
  * array until the process exits.  Sizes whose scratch would not fit (about
- * 260,000 units of (segment, head, pair of 128-row query tiles)) are rejected
- * with JGDPA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ * 87,000 to 130,000 units of (segment, head, pair of 128-row query tiles),
+ * depending on the segment lengths) are rejected with
+ * JGDPA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call

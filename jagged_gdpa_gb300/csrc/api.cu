@@ -22,6 +22,8 @@ cudaError_t launch_fwd_d(const FwdParams& p, int act, int grid, cudaStream_t str
 template <int D>
 cudaError_t launch_fwd_shortq_d(const FwdParams& p, int act, int nq, int grid, cudaStream_t stream);
 template <int D>
+cudaError_t launch_fwd_kvres_d(const FwdParams& p, int act, int grid, cudaStream_t stream);
+template <int D>
 cudaError_t launch_bwd_pass_d(const BwdParams& p, int act, bool kv_major, int grid, cudaStream_t stream,
                               bool direct);
 template <int D>
@@ -64,6 +66,12 @@ cudaError_t launch_bwd_shortq(const BwdParams& p, int head_dim, int act, int nq,
   if (head_dim == 128) return launch_bwd_shortq_d<128>(p, act, nq, grid, stream);
   if (head_dim == 64) return launch_bwd_shortq_d<64>(p, act, nq, grid, stream);
   if (head_dim == 32) return launch_bwd_shortq_d<32>(p, act, nq, grid, stream);
+  return cudaErrorInvalidValue;
+}
+cudaError_t launch_fwd_kvres(const FwdParams& p, int head_dim, int act, int grid, cudaStream_t stream) {
+  if (head_dim == 128) return launch_fwd_kvres_d<128>(p, act, grid, stream);
+  if (head_dim == 64) return launch_fwd_kvres_d<64>(p, act, grid, stream);
+  if (head_dim == 32) return launch_fwd_kvres_d<32>(p, act, grid, stream);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_dq_ds(const BwdParams& p, int head_dim, int grid, cudaStream_t stream) {
@@ -202,7 +210,7 @@ struct Layout {
   size_t header = 0;      // status word + unit counters
   size_t item_base = 0;   // scheduler scratch, 2 lists x (batch + 1)
   size_t units0 = 0;      // fwd units, or dkdv units
-  size_t units1 = 0;      // dq units (bwd): all, or those of the segments with stored dS
+  size_t units1 = 0;      // dq units (bwd): all, or those of the segments with stored dS; fwd: key/value-resident units
   size_t units2 = 0;      // bwd with a dS scratch: dq units of the segments recomputed
   size_t units3 = 0;      // bwd: dkdv units of the segments whose dQ that pass forms directly
   size_t delta = 0;       // softmax bwd: [H][total_q]
@@ -242,6 +250,7 @@ bool layout_for(int32_t batch, int64_t total_q, int64_t total_kv, int32_t heads,
   int64_t m0, m1 = 0;
   if (!bwd) {
     m0 = max_units(total_q, batch, 2 * kTile, heads);
+    m1 = max_units(total_q, batch, kTile, heads);  // key/value-resident units (one per query tile at most)
   } else {
     m0 = max_units(total_kv, batch, kTile, heads);
     m1 = max_units(total_q, batch, kTile, heads);
@@ -363,9 +372,9 @@ __global__ void eval_act_kernel(int act, int path, const float* x, int64_t n, fl
 jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batch, int32_t heads,
                           int64_t total_q, int64_t total_kv, int32_t causal, int32_t window, uint8_t* ws,
                           const Layout& L, bool bwd, cudaStream_t stream, int64_t ds_capacity = -1,
-                          bool kv_chunks = false, bool dq_direct = false) {
+                          bool kv_chunks = false, bool one_tile = false) {
   jg::SchedParams sp{};
-  sp.dq_direct = dq_direct ? 1 : 0;
+  sp.one_tile = one_tile ? 1 : 0;
   if (ds_capacity >= 0) {
     sp.ds_base = reinterpret_cast<int64_t*>(ws + L.ds_base);
     sp.ds_capacity = ds_capacity;
@@ -399,7 +408,14 @@ jgdpa_status run_sched(const int32_t* q_off, const int32_t* kv_off, int32_t batc
     sp.list[2].n_units = hdr + 3;
     sp.list[2].units = reinterpret_cast<jg::Unit*>(ws + L.units2);
   }
-  if (dq_direct) {  // the key-major units of the direct-dQ segments, last list
+  if (one_tile && !bwd) {  // the key/value-resident forward units
+    jg::SchedList& ol = sp.list[sp.n_lists++];
+    ol.kind = jg::kUnitsFwdKvRes;
+    ol.max_units = L.max1;
+    ol.n_units = hdr + 2;
+    ol.units = reinterpret_cast<jg::Unit*>(ws + L.units1);
+  }
+  if (one_tile && bwd) {  // the key-major units of the direct-dQ segments, last list
     jg::SchedList& dl = sp.list[sp.n_lists++];
     dl.kind = jg::kUnitsKvDirect;
     dl.max_units = L.max0;
@@ -466,7 +482,14 @@ jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t
     if (lse) JG_CUDA(fill_f32(lse, total_q * heads, -INFINITY, stream));
     return JGDPA_OK;
   }
-  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, false, stream);
+  // shared queries of at most 64 rows (GELU / SiLU): keys on the MMA's 128
+  // rows and the queries as N, so the activation touches only live elements
+  const bool shortq = q_shared > 0 && q_shared <= kShortQMax && act != JGDPA_ACT_SOFTMAX;
+  // otherwise the segments whose keys fit one tile and that have two or more
+  // query tiles run in the key/value-resident forward
+  const bool one_tile = !shortq && window == 0;
+  st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, false, stream, -1,
+                 false, one_tile);
   if (st != JGDPA_OK) return st;
 
   jg::FwdParams p{};
@@ -491,12 +514,16 @@ jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t
   p.scale = act == JGDPA_ACT_SOFTMAX ? scale * jg::kLog2e : scale;
   p.wait_limit_ns = wait_limit_ns();
   const int grid = static_cast<int>(std::min<int64_t>(L.grid, std::max(1, L.max0)));
-  // shared queries of at most 64 rows (GELU / SiLU): keys on the MMA's 128
-  // rows and the queries as N, so the activation touches only live elements
-  if (q_shared > 0 && q_shared <= kShortQMax && act != JGDPA_ACT_SOFTMAX)
+  if (shortq) {
     JG_CUDA(jg::launch_fwd_shortq(p, head_dim, act, q_shared, grid, stream));
-  else
+  } else {
     JG_CUDA(jg::launch_fwd(p, head_dim, act, grid, stream));
+    if (one_tile) {
+      p.units = reinterpret_cast<const jg::Unit*>(ws + L.units1);
+      p.n_units = hdr + 2;
+      JG_CUDA(jg::launch_fwd_kvres(p, head_dim, act, grid, stream));
+    }
+  }
   return JGDPA_OK;
 }
 
@@ -592,7 +619,7 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
   // (a scratch smaller than one tile is no scratch: every dQ is recomputed)
   // every backward but the fused-dQ ones forms the dQ of single-key-tile
   // segments in its key-major pass
-  const bool dq_direct = !L.fused_dq;
+  const bool dq_direct = !L.fused_dq && window == 0;
   st = run_sched(q_offsets, kv_offsets, batch, heads, total_q, total_kv, causal, window, ws, L, true, stream,
                  stored_ds ? ds_tiles : -1, shortq, dq_direct);
   if (st != JGDPA_OK) return st;

@@ -31,6 +31,9 @@ enum UnitKind : int {
   // Key-major units of the segments whose dQ the key-major pass forms
   // directly (dq_direct_segment); kUnitsKv then holds the others.
   kUnitsKvDirect = 6,
+  // Forward units (segment, head, chunk of up to kChunkTiles query tiles) of
+  // the segments with kv_resident_segment; kUnitsFwd then holds the others.
+  kUnitsFwdKvRes = 7,
 };
 constexpr int kChunkTiles = 16;
 
@@ -62,7 +65,11 @@ struct SchedParams {
   // nullptr without a scratch
   int64_t* ds_base;
   int64_t ds_capacity;  // dS tiles the caller's scratch holds
-  int32_t dq_direct;    // backward: segments with dq_direct_segment get no query-major units and no dS
+  // Segments whose keys fit one tile get their own lists: in the forward
+  // those with kv_resident_segment go to kUnitsFwdKvRes; in the backward
+  // those with dq_direct_segment go to kUnitsKvDirect and get no query-major
+  // units and no stored dS.
+  int32_t one_tile;
 };
 
 // Lengths and tile counts of one segment.
@@ -118,6 +125,14 @@ __device__ __forceinline__ TileSpan q_span_for_kv_tile(int kt, int lq, int causa
 // every query tile.)
 __host__ __device__ __forceinline__ bool dq_direct_segment(int lq, int lkv, int window) {
   return window <= 0 && lq > 0 && lkv > 0 && lkv <= kTile;
+}
+
+// Forward: a segment whose keys fit one tile and that has at least two
+// query tiles runs in the key/value-resident forward (K and V loaded once
+// for up to kChunkTiles query tiles; a single query tile has nothing to
+// share them with).
+__host__ __device__ __forceinline__ bool kv_resident_segment(int lq, int lkv, int window) {
+  return dq_direct_segment(lq, lkv, window) && lq > kTile;
 }
 
 // Index of the i-th unit processed by CTA c of G (serpentine over rounds, so

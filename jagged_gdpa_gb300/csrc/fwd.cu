@@ -695,6 +695,337 @@ __global__ void __launch_bounds__(384, 1) gdpa_fwd_kernel(const __grid_constant_
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// ======================================= forward, key/value tile resident
+// For segments whose keys fit one tile (short key/value streams, e.g.
+// cross-attention to a few memory tokens): every query tile meets the same
+// single key/value tile.  The general kernel pairs two query tiles per unit
+// and reloads that tile for each pair, and its next unit's loads wait for the
+// current unit's products, so on such segments the load latency sets the
+// pace.  Here a unit is (segment, head, chunk of up to kChunkTiles query
+// tiles): K and V are loaded once per unit (two sets, so the next unit's pair
+// loads while this one runs) and the query tiles stream through a ring,
+// released as soon as their S product has read them.  The CTA's n-th query
+// tile goes to activation warpgroup n % 2 (TMEM S_w, O_w), so one
+// warpgroup's epilogue overlaps the other's activation.  P V is complete
+// after one product, and softmax needs no running rescale.
+// (The outer-loop pipelining of short inner loops: "Meta redesigns AI
+// training infrastructure ...", section "Custom Kernels and 5D Parallelism
+// ...".)
+template <int D>
+struct KvrCfg {
+  using F = FwdCfg<D>;
+  static constexpr int kQStages = D == 128 ? 2 : 4;
+  static constexpr int kKvOff = 0;  // (K, V) set s: K at s 2 tiles, V one tile after
+  static constexpr int kQOff = kKvOff + 4 * F::kTileBytes;
+  static constexpr int kEpiOff = kQOff + kQStages * F::kTileBytes;
+};
+template <int D, int ACT>
+struct KvrSmem {
+  static constexpr bool kStage = D >= 64 && ACT != 2;
+  static constexpr int kBarOff = KvrCfg<D>::kEpiOff + (kStage ? 8 * 4096 : 0);
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+struct KvrBars {
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t q_full[4], q_empty[4];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Query tiles [t0, t0 + nt) of segment b, head h.
+struct KvrUnit {
+  int b, h;
+  Seg seg;
+  int t0, nt;
+};
+
+__device__ __forceinline__ KvrUnit kvr_unit(const FwdParams& p, int idx) {
+  KvrUnit u;
+  const Unit w = p.units[idx];
+  u.b = w.x;
+  u.h = w.y;
+  u.seg = load_seg(p.q_off, p.kv_off, u.b);
+  u.t0 = w.z * kChunkTiles;
+  u.nt = max(0, min(ceil_div(u.seg.lq, kTile) - u.t0, kChunkTiles));
+  return u;
+}
+
+template <int D>
+__device__ void kvr_producer(const FwdParams& p, uint8_t* smem, KvrBars* bars, int n_units, Fail fail) {
+  using F = FwdCfg<D>;
+  using C = KvrCfg<D>;
+  uint32_t u_it = 0, q_it = 0;
+  const bool leader = elect_one();
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = unit_index(r, blockIdx.x, gridDim.x);
+    if (idx >= n_units) break;
+    const KvrUnit u = kvr_unit(p, idx);
+    if (u.nt == 0) continue;
+    const int ks = u_it & 1;
+    if (!(ok = mbar_wait_warp(&bars->kv_empty[ks], ((u_it >> 1) & 1) ^ 1, fail))) break;
+    if (leader) {
+      mbar_arrive_tx(&bars->kv_full[ks], 2 * F::kTileBytes);
+      uint8_t* kd = smem + C::kKvOff + ks * 2 * F::kTileBytes;
+#pragma unroll
+      for (int cb = 0; cb < F::kNumBlocks; ++cb) {
+        tma_load_3d(kd + cb * F::kBlockBytes, &p.tm_k, &bars->kv_full[ks], cb * F::kBlockCols, u.h, u.seg.k0);
+        tma_load_3d(kd + F::kTileBytes + cb * F::kBlockBytes, &p.tm_v, &bars->kv_full[ks], cb * F::kBlockCols, u.h,
+                    u.seg.k0);
+      }
+    }
+    ++u_it;
+    // shared queries: the Q map holds the shared rows once
+    const int qrow0 = p.q_shared ? 0 : u.seg.q0;
+    for (int t = 0; t < u.nt && ok; ++t) {
+      const int st = q_it % C::kQStages;
+      if (!(ok = mbar_wait_warp(&bars->q_empty[st], ((q_it / C::kQStages) & 1) ^ 1, fail))) break;
+      if (leader) {
+        mbar_arrive_tx(&bars->q_full[st], F::kTileBytes);
+        uint8_t* qd = smem + C::kQOff + st * F::kTileBytes;
+#pragma unroll
+        for (int cb = 0; cb < F::kNumBlocks; ++cb)
+          tma_load_3d(qd + cb * F::kBlockBytes, &p.tm_q, &bars->q_full[st], cb * F::kBlockCols, u.h,
+                      qrow0 + (u.t0 + t) * kTile);
+      }
+      ++q_it;
+    }
+  }
+  if (!ok) {  // let the copies already issued land before the CTA exits
+    for (uint32_t i = u_it > 2 ? u_it - 2 : 0; i < u_it; ++i) mbar_wait_drain(&bars->kv_full[i & 1], (i >> 1) & 1);
+    for (uint32_t i = q_it > C::kQStages ? q_it - C::kQStages : 0; i < q_it; ++i)
+      mbar_wait_drain(&bars->q_full[i % C::kQStages], (i / C::kQStages) & 1);
+  }
+}
+
+template <int D>
+__device__ void kvr_mma(const FwdParams& p, uint8_t* smem, KvrBars* bars, uint32_t tmem, int n_units, Fail fail) {
+  using F = FwdCfg<D>;
+  using C = KvrCfg<D>;
+  uint32_t u_it = 0, n = 0;
+  const bool leader = elect_one();
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = unit_index(r, blockIdx.x, gridDim.x);
+    if (idx >= n_units) break;
+    const KvrUnit u = kvr_unit(p, idx);
+    if (u.nt == 0) continue;
+    const int ks = u_it & 1;
+    if (!(ok = mbar_wait_warp(&bars->kv_full[ks], (u_it >> 1) & 1, fail))) break;
+    ++u_it;
+    const uint32_t k_addr = smem_u32(smem + C::kKvOff + ks * 2 * F::kTileBytes);
+    const uint32_t v_addr = k_addr + F::kTileBytes;
+    // S of tile m into S_(m % 2): the columns that P V of tile m - 2 read,
+    // issued before it (MMAs execute in issue order)
+    auto issue_s = [&](uint32_t m) -> bool {
+      const int st = m % C::kQStages, w = m & 1;
+      if (!mbar_wait_warp(&bars->q_full[st], (m / C::kQStages) & 1, fail)) return false;
+      tc_fence_after();
+      issue_qk<D>(tmem + 128 * w, smem_u32(smem + C::kQOff + st * F::kTileBytes), k_addr, leader);
+      if (leader) mma_commit(&bars->s_full[w]);
+      if (leader) mma_commit(&bars->q_empty[st]);  // the query tile is read by S only
+      return true;
+    };
+    if (!(ok = issue_s(n))) break;
+    for (int t = 0; t < u.nt && ok; ++t) {
+      const uint32_t m = n + t;
+      const int w = m & 1;
+      if (t + 1 < u.nt && !(ok = issue_s(m + 1))) break;
+      if (!(ok = mbar_wait_warp(&bars->o_empty[w], ((m >> 1) & 1) ^ 1, fail))) break;
+      if (!(ok = mbar_wait_warp(&bars->p_full[w], (m >> 1) & 1, fail))) break;
+      tc_fence_after();
+      issue_pv<D>(tmem + 256 + D * w, tmem + 128 * w, v_addr, false, leader);
+      if (leader) mma_commit(&bars->o_full[w]);
+    }
+    if (!ok) break;
+    n += u.nt;
+    if (leader) mma_commit(&bars->kv_empty[ks]);  // every product of this unit issued
+  }
+  if (leader) mma_commit(&bars->drain);
+  mbar_wait_drain(&bars->drain, 0);
+}
+
+template <int D, int ACT>
+__device__ void kvr_act(const FwdParams& p, uint8_t* smem, KvrBars* bars, uint32_t tmem, int w, int n_units,
+                        Fail fail) {
+  using C = KvrCfg<D>;
+  constexpr bool kSoftmax = ACT == 2;
+  const int warp = threadIdx.x >> 5;
+  const int quad = warp & 3;
+  const int r = quad * 32 + (threadIdx.x & 31);  // query row of the tile owned by this thread
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t t_s = tmem + lane_off + 128 * w;
+  const uint32_t t_o = tmem + lane_off + 256 + D * w;
+  const int H = p.heads;
+  uint32_t n = 0;
+  for (int rr = 0;; ++rr) {
+    const int idx = unit_index(rr, blockIdx.x, gridDim.x);
+    if (idx >= n_units) break;
+    const KvrUnit u = kvr_unit(p, idx);
+    if (u.nt == 0) continue;
+    float bc_lo = 0.f, bc_hi = 0.f;
+    if (p.bias_len) {
+      const float* brow = p.bias + static_cast<int64_t>(u.h) * p.bias_len;
+      bc_lo = __ldg(brow);
+      bc_hi = __ldg(brow + p.bias_len - 1);
+    }
+    const int nchunks = (min(kTile, u.seg.lkv) + 31) / 32;
+    bool ok = true;
+    for (int t = 0; t < u.nt; ++t) {
+      const uint32_t m = n + t;
+      if (static_cast<int>(m & 1) != w) continue;
+      const int qt = u.t0 + t;
+      const int rows = u.seg.lq - qt * kTile;
+      if (!(ok = mbar_wait(&bars->s_full[w], (m >> 1) & 1, fail))) break;
+      tc_fence_after();
+      const int i_row = qt * kTile + r;  // segment-local query row
+      int nvalid = min(kTile, u.seg.lkv);
+      if (p.causal) nvalid = min(nvalid, i_row + 1);
+      const bool tile_masked = u.seg.lkv < kTile || (p.causal && qt == 0);
+      const TileBias tb = tile_bias(p, u.h, qt * kTile, r, 0, bc_lo, bc_hi);
+      float m_run = -INFINITY, l_run = 0.f;  // softmax state (base 2)
+      if constexpr (!kSoftmax) {
+        const float hs = 0.5f * p.scale;
+        if (tb.band) {
+          if (tile_masked) tile_act<ACT, kFwdAluChunks, true, true>(t_s, hs, tb, 0, nvalid, nchunks);
+          else tile_act<ACT, kFwdAluChunks, true, false>(t_s, hs, tb, 0, nvalid, nchunks);
+        } else {
+          if (tile_masked) tile_act<ACT, kFwdAluChunks, false, true>(t_s, hs, tb, 0, nvalid, nchunks);
+          else tile_act<ACT, kFwdAluChunks, false, false>(t_s, hs, tb, 0, nvalid, nchunks);
+        }
+      } else {
+        if (tb.band) {
+          if (tile_masked) tile_softmax<D, true, true>(t_s, t_o, p.scale, tb, 0, nvalid, true, m_run, l_run);
+          else tile_softmax<D, true, false>(t_s, t_o, p.scale, tb, 0, nvalid, true, m_run, l_run);
+        } else {
+          if (tile_masked) tile_softmax<D, false, true>(t_s, t_o, p.scale, tb, 0, nvalid, true, m_run, l_run);
+          else tile_softmax<D, false, false>(t_s, t_o, p.scale, tb, 0, nvalid, true, m_run, l_run);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive_warp(&bars->p_full[w]);
+      // epilogue: O (TMEM) -> bf16 -> global, rows < Lq only
+      if (!(ok = mbar_wait(&bars->o_full[w], (m >> 1) & 1, fail))) break;
+      tc_fence_after();
+      const int64_t grow = static_cast<int64_t>(u.seg.q0) + qt * kTile + r;
+      const float inv_l = kSoftmax ? (l_run > 0.f ? 1.0f / l_run : 0.f) : 1.0f;
+      if constexpr (KvrSmem<D, ACT>::kStage) {
+        // each 64-column half of the warp's 32 rows staged in the warp's own
+        // 4 KB, then stored four whole 128-byte rows per instruction
+        const int lr = threadIdx.x & 31;
+        const uint32_t stg = smem_u32(smem + C::kEpiOff) + (warp - 4) * 4096;
+        const int64_t row0 = grow - lr;
+#pragma unroll
+        for (int hb = 0; hb < D / 64; ++hb) {
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + 64 * hb + c0, o);
+            tmem_ld_wait(o);
+            if (hb == D / 64 - 1 && c0 == 32) {  // every column of O is in registers
+              tc_fence_before();
+              mbar_arrive_warp(&bars->o_empty[w]);
+            }
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint32_t wd[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                wd[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * inv_l, __uint_as_float(o[c + 2 * e + 1]) * inv_l);
+              const int j = (c0 + c) >> 3;
+              st_shared_v4(stg + lr * 128 + ((j ^ (lr & 7)) << 4), wd[0], wd[1], wd[2], wd[3]);
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rw = 4 * k + (lr >> 3), j = lr & 7;
+            uint32_t a, b2, c2, d2;
+            ld_shared_v4(stg + rw * 128 + ((j ^ (rw & 7)) << 4), a, b2, c2, d2);
+            if (quad * 32 + rw < rows)
+              st_global_v4(p.out + ((row0 + rw) * H + u.h) * D + 64 * hb + 8 * j, a, b2, c2, d2);
+          }
+          __syncwarp();
+        }
+      } else {
+        __nv_bfloat16* out_row = p.out + (grow * H + u.h) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c0, o);
+          tmem_ld_wait(o);
+          if (c0 + 32 == D) {
+            tc_fence_before();
+            mbar_arrive_warp(&bars->o_empty[w]);
+          }
+          if (r < rows) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint32_t wd[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                wd[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * inv_l, __uint_as_float(o[c + 2 * e + 1]) * inv_l);
+              st_global_v4(out_row + c0 + c, wd[0], wd[1], wd[2], wd[3]);
+            }
+          }
+        }
+      }
+      if (kSoftmax && r < rows && p.lse)
+        p.lse[static_cast<int64_t>(u.h) * p.total_q + grow] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+    }
+    if (!ok) break;
+    n += u.nt;
+  }
+}
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(384, 1) gdpa_fwd_kvres_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  KvrBars* bars = reinterpret_cast<KvrBars*>(smem + KvrSmem<D, ACT>::kBarOff);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 4);
+      mbar_init(&bars->o_full[s], 1);
+      mbar_init(&bars->o_empty[s], 4);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int n_units = *p.n_units;
+  if (*reinterpret_cast<volatile int*>(p.status) != kOk) n_units = 0;
+  Fail fail{&bars->abort, p.status, p.wait_limit_ns};
+  if (warp == 0) kvr_producer<D>(p, smem, bars, n_units, fail);
+  else if (warp == 1) kvr_mma<D>(p, smem, bars, tmem, n_units, fail);
+  else if (warp >= 4) kvr_act<D, ACT>(p, smem, bars, tmem, (warp - 4) >> 2, n_units, fail);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
 // ------------------------------------------------------------------ launch
 // Each object file holds the kernels of one head dimension (JGDPA_HEAD_DIM),
 // so that the build compiles the head dimensions in parallel.
@@ -720,5 +1051,27 @@ cudaError_t launch_fwd_d(const FwdParams& p, int act, int grid, cudaStream_t str
   return launch_fwd_t<D, 2>(p, grid, stream);
 }
 template cudaError_t launch_fwd_d<JGDPA_HEAD_DIM>(const FwdParams&, int, int, cudaStream_t);
+
+// The key/value-resident forward (segments whose keys fit one tile; no window).
+template <int ACT>
+static cudaError_t launch_kvres_t(const FwdParams& p, int grid, cudaStream_t stream) {
+  constexpr int D = JGDPA_HEAD_DIM;
+  auto kern = gdpa_fwd_kvres_kernel<D, ACT>;
+  // at least half the SM's shared memory: one CTA per SM, so that a second
+  // CTA never waits in its TMEM allocation for the first to finish
+  constexpr int kSmem = KvrSmem<D, ACT>::kSmemBytes > 120 * 1024 ? KvrSmem<D, ACT>::kSmemBytes : 120 * 1024;
+  static DeviceFlags attr_set = {};
+  cudaError_t e = smem_attr_once(kern, kSmem, attr_set);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 384, kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+template <int D>
+cudaError_t launch_fwd_kvres_d(const FwdParams& p, int act, int grid, cudaStream_t stream) {
+  if (act == 0) return launch_kvres_t<0>(p, grid, stream);
+  if (act == 1) return launch_kvres_t<1>(p, grid, stream);
+  return launch_kvres_t<2>(p, grid, stream);
+}
+template cudaError_t launch_fwd_kvres_d<JGDPA_HEAD_DIM>(const FwdParams&, int, int, cudaStream_t);
 
 }  // namespace jg

@@ -21,14 +21,18 @@ constexpr int kSchedThreads = 1024;
 constexpr int kSmemBase = 6144;  // segments whose item prefix is searched in shared memory
 
 __device__ __forceinline__ bool direct_dq(const SchedParams& p, const Seg& s) {
-  return p.dq_direct && dq_direct_segment(s.lq, s.lkv, p.window);
+  return p.one_tile && dq_direct_segment(s.lq, s.lkv, p.window);
+}
+__device__ __forceinline__ bool kv_resident(const SchedParams& p, const Seg& s) {
+  return p.one_tile && kv_resident_segment(s.lq, s.lkv, p.window);
 }
 
 // Items of segment s in a list of this kind; `stored` tells whether the
 // segment's dS tiles fit the scratch (used by the two split query lists).
 // Segments whose dQ the key-major pass forms directly have no query items.
 __device__ int items_of_segment(const SchedParams& p, int kind, const Seg& s, bool stored) {
-  if (kind == kUnitsFwd) return ceil_div(s.lq, 2 * kTile);
+  if (kind == kUnitsFwd) return kv_resident(p, s) ? 0 : ceil_div(s.lq, 2 * kTile);
+  if (kind == kUnitsFwdKvRes) return kv_resident(p, s) ? ceil_div(ceil_div(s.lq, kTile), kChunkTiles) : 0;
   if (kind == kUnitsKvChunk) return ceil_div(ceil_div(s.lkv, kTile), kChunkTiles);
   if (kind == kUnitsKvDirect) return direct_dq(p, s) ? 1 : 0;
   if (kind == kUnitsKv) return direct_dq(p, s) ? 0 : ceil_div(s.lkv, kTile);
@@ -54,6 +58,7 @@ __device__ int cost_of_item(int kind, const Seg& s, int tile, int causal, int wi
   }
   if (kind == kUnitsKv || kind == kUnitsKvDirect) return q_span_for_kv_tile(tile, s.lq, causal, window).count + 1;
   if (kind == kUnitsKvChunk) return min(kChunkTiles, ceil_div(s.lkv, kTile) - tile * kChunkTiles) + 1;
+  if (kind == kUnitsFwdKvRes) return min(kChunkTiles, ceil_div(s.lq, kTile) - tile * kChunkTiles) + 1;
   return kv_span_for_q_tile(tile, s.lkv, causal, window).count + 1;  // the query lists
 }
 
