@@ -161,6 +161,9 @@ struct FwdParams {
   float scale;            // s (GELU/SiLU) or s * log2(e) (softmax)
   unsigned long long wait_limit_ns;  // limit of one internal wait
   int32_t q_shared;       // 1: every segment reads the same query rows (Q map row 0 = its row 0)
+  // the key/value-resident forward's O stores: boxes of 32 rows x 1 head x
+  // min(d, 64) columns over out, 128-byte swizzle (d >= 64, GELU / SiLU)
+  CUtensorMap tm_o;
 };
 
 struct BwdParams {

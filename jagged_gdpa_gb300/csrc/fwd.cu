@@ -916,12 +916,19 @@ __device__ void kvr_act(const FwdParams& p, uint8_t* smem, KvrBars* bars, uint32
       const float inv_l = kSoftmax ? (l_run > 0.f ? 1.0f / l_run : 0.f) : 1.0f;
       if constexpr (KvrSmem<D, ACT>::kStage) {
         // each 64-column half of the warp's 32 rows staged in the warp's own
-        // 4 KB, then stored four whole 128-byte rows per instruction
+        // 4 KB (the 128-byte swizzle of the O tensor map); a block whose 32
+        // rows all lie in the segment leaves by one TMA store, the last
+        // block of a segment by stores of four whole 128-byte rows per
+        // instruction
         const int lr = threadIdx.x & 31;
-        const uint32_t stg = smem_u32(smem + C::kEpiOff) + (warp - 4) * 4096;
+        uint8_t* stg_p = smem + C::kEpiOff + (warp - 4) * 4096;
+        const uint32_t stg = smem_u32(stg_p);
         const int64_t row0 = grow - lr;
+        const bool whole = quad * 32 + 31 < rows;
 #pragma unroll
         for (int hb = 0; hb < D / 64; ++hb) {
+          if (lr == 0) bulk_wait_read_all();  // the block's previous TMA store has read it
+          __syncwarp();
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t o[32];
@@ -941,16 +948,25 @@ __device__ void kvr_act(const FwdParams& p, uint8_t* smem, KvrBars* bars, uint32
               st_shared_v4(stg + lr * 128 + ((j ^ (lr & 7)) << 4), wd[0], wd[1], wd[2], wd[3]);
             }
           }
-          __syncwarp();
+          if (whole) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lr == 0) {
+              tma_store_3d(&p.tm_o, stg_p, 64 * hb, u.h, static_cast<int>(row0));
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int rw = 4 * k + (lr >> 3), j = lr & 7;
-            uint32_t a, b2, c2, d2;
-            ld_shared_v4(stg + rw * 128 + ((j ^ (rw & 7)) << 4), a, b2, c2, d2);
-            if (quad * 32 + rw < rows)
-              st_global_v4(p.out + ((row0 + rw) * H + u.h) * D + 64 * hb + 8 * j, a, b2, c2, d2);
+            for (int k = 0; k < 8; ++k) {
+              const int rw = 4 * k + (lr >> 3), j = lr & 7;
+              uint32_t a, b2, c2, d2;
+              ld_shared_v4(stg + rw * 128 + ((j ^ (rw & 7)) << 4), a, b2, c2, d2);
+              if (quad * 32 + rw < rows)
+                st_global_v4(p.out + ((row0 + rw) * H + u.h) * D + 64 * hb + 8 * j, a, b2, c2, d2);
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       } else {
         __nv_bfloat16* out_row = p.out + (grow * H + u.h) * D;
@@ -980,6 +996,10 @@ __device__ void kvr_act(const FwdParams& p, uint8_t* smem, KvrBars* bars, uint32
     }
     if (!ok) break;
     n += u.nt;
+  }
+  if constexpr (KvrSmem<D, ACT>::kStage) {  // this warp's TMA stores are complete before the CTA exits
+    if ((threadIdx.x & 31) == 0) bulk_wait_all();
+    __syncwarp();
   }
 }
 
