@@ -517,11 +517,12 @@ jgdpa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t
   if (shortq) {
     JG_CUDA(jg::launch_fwd_shortq(p, head_dim, act, q_shared, grid, stream));
   } else {
+    // O stores by TMA (32-row boxes) from the staged epilogues
+    if (!make_map(&p.tm_o, out, total_q, heads, head_dim, 32)) return JGDPA_ERR_CUDA;
     JG_CUDA(jg::launch_fwd(p, head_dim, act, grid, stream));
     if (one_tile) {
       p.units = reinterpret_cast<const jg::Unit*>(ws + L.units1);
       p.n_units = hdr + 2;
-      if (!make_map(&p.tm_o, out, total_q, heads, head_dim, 32)) return JGDPA_ERR_CUDA;
       JG_CUDA(jg::launch_fwd_kvres(p, head_dim, act, grid, stream));
     }
   }

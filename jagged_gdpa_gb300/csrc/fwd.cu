@@ -586,16 +586,27 @@ __device__ void fwd_act(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
       // warp's 32 rows is staged in the warp's own 4 KB of shared memory
       // (XOR-swizzled 16-byte chunks), then stored four whole 128-byte rows
       // per instruction.
+      // A block whose 32 rows all lie in the segment leaves by one TMA
+      // store (the O map's 32-row box and 128-byte swizzle match the
+      // staging); O is released once its last columns are in registers.
       const int lr = threadIdx.x & 31;
-      const uint32_t stg = smem_u32(smem + C::kEpiOff) + (warp - 4) * 4096;
+      uint8_t* stg_p = smem + C::kEpiOff + (warp - 4) * 4096;
+      const uint32_t stg = smem_u32(stg_p);
       const int64_t row0 = grow - lr;  // global row of the warp's first row
+      const bool whole = quad * 32 + 31 < rows;
 #pragma unroll
       for (int hb = 0; hb < D / 64; ++hb) {
+        if (lr == 0) bulk_wait_read_all();  // the staging's previous TMA store has read it
+        __syncwarp();
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(t_o + 64 * hb + c0, o);
           tmem_ld_wait(o);
+          if (hb == D / 64 - 1 && c0 == 32) {
+            tc_fence_before();
+            mbar_arrive_warp(&bars->o_empty[slot]);
+          }
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint32_t w[4];
@@ -606,16 +617,25 @@ __device__ void fwd_act(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
             st_shared_v4(stg + lr * 128 + ((j ^ (lr & 7)) << 4), w[0], w[1], w[2], w[3]);
           }
         }
-        __syncwarp();
+        if (whole) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lr == 0) {
+            tma_store_3d(&p.tm_o, stg_p, 64 * hb, u.h, static_cast<int>(row0));
+            bulk_commit();
+          }
+        } else {
+          __syncwarp();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int rr = 4 * k + (lr >> 3), j = lr & 7;
-          uint32_t a, b2, c2, d2;
-          ld_shared_v4(stg + rr * 128 + ((j ^ (rr & 7)) << 4), a, b2, c2, d2);
-          if (quad * 32 + rr < rows)
-            st_global_v4(p.out + ((row0 + rr) * H + u.h) * D + 64 * hb + 8 * j, a, b2, c2, d2);
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lr >> 3), j = lr & 7;
+            uint32_t a, b2, c2, d2;
+            ld_shared_v4(stg + rr * 128 + ((j ^ (rr & 7)) << 4), a, b2, c2, d2);
+            if (quad * 32 + rr < rows)
+              st_global_v4(p.out + ((row0 + rr) * H + u.h) * D + 64 * hb + 8 * j, a, b2, c2, d2);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     } else {
 #pragma unroll
@@ -635,10 +655,16 @@ __device__ void fwd_act(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
         }
       }
     }
-    tc_fence_before();
-    mbar_arrive_warp(&bars->o_empty[slot]);
+    if constexpr (!FwdSmem<D, ACT>::kStage) {
+      tc_fence_before();
+      mbar_arrive_warp(&bars->o_empty[slot]);
+    }
     if (kSoftmax && row_ok && p.lse)
       p.lse[static_cast<int64_t>(u.h) * p.total_q + grow] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+  }
+  if constexpr (FwdSmem<D, ACT>::kStage) {  // this warp's TMA stores are complete before the CTA exits
+    if ((threadIdx.x & 31) == 0) bulk_wait_all();
+    __syncwarp();
   }
 }
 
