@@ -641,6 +641,8 @@ jgdpa_status bwd_impl(const void* q, const void* k, const void* v, const void* o
     p.kv_item_base = reinterpret_cast<const int32_t*>(ws + L.item_base);  // list 0: the key tiles
     p.q_rows = q_shared;
   }
+  // direct dQ at d = 128 (into dq): TMA stores of 32-row blocks
+  if (dq_direct && q_shared == 0 && !make_map(&p.tm_dq, dq, total_q, heads, head_dim, 32)) return JGDPA_ERR_CUDA;
   if (stored_ds) {
     if (!make_ds_map(&p.tm_ds, ds_scratch, ds_tiles)) return JGDPA_ERR_CUDA;
     p.ds_base = reinterpret_cast<const int64_t*>(ws + L.ds_base);

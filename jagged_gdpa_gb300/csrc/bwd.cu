@@ -724,11 +724,68 @@ __device__ __forceinline__ void phase_b_chunk(const uint32_t (&dv)[32], const fl
 // DIRECT: dQ of query tile qt (key-major pass): TMEM lane r is query row r
 // of the tile; warpgroup `half` owns columns [half D/2, (half+1) D/2).
 // Scaled by s into dq (bf16), or into dq_part (fp32) with shared queries.
+// At d = 128 into dq the warp stages its 32 rows x 64 columns in its own 4 KB
+// of the X tile (free here: dK and this dQ have read it, and phase B writes
+// it only after this), which leaves by one TMA store when the 32 rows lie in
+// the segment and by stores of four whole 128-byte rows per instruction
+// otherwise: a thread's own row pieces lie H D 2 bytes apart, and storing
+// them directly touched 32 lines per instruction (~2 K cycles of the
+// load/store unit per tile in the traces).
 template <int D>
 __device__ __forceinline__ bool read_dq(const BwdParams& p, BwdBars* bars, uint32_t t_dq, int half, int r, int q0,
-                                        int lq, int h, int qt, uint32_t parity, Fail fail) {
+                                        int lq, int h, int qt, uint32_t parity, Fail fail, uint8_t* stage) {
   if (!mbar_wait(&bars->dq_full, parity, fail)) return false;
   tc_fence_after();
+  if constexpr (D == 128) {
+    if (p.dq_part == nullptr) {
+      const int lr = threadIdx.x & 31, quad = r >> 5;
+      const uint32_t stg = smem_u32(stage);
+      if (lr == 0) bulk_wait_read_all();  // this warp's previous TMA store has read the block
+      __syncwarp();
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_dq + c0, o);
+        tmem_ld_wait(o);
+        if (c0 == 32) {  // every column of this tile's dQ is in registers
+          tc_fence_before();
+          mbar_arrive_warp(&bars->dq_empty);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * p.scale, __uint_as_float(o[c + 2 * e + 1]) * p.scale);
+          const int j = (c0 + c) >> 3;
+          st_shared_v4(stg + lr * 128 + ((j ^ (lr & 7)) << 4), w[0], w[1], w[2], w[3]);
+        }
+      }
+      const int rows = lq - qt * kTile;
+      const int row0 = q0 + qt * kTile + quad * 32;  // the warp's first row
+      if (quad * 32 + 31 < rows) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lr == 0) {
+          tma_store_3d(&p.tm_dq, stage, 64 * half, h, row0);
+          bulk_commit();
+        }
+      } else {
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rw = 4 * k + (lr >> 3), j = lr & 7;
+          uint32_t a, b2, c2, d2;
+          ld_shared_v4(stg + rw * 128 + ((j ^ (rw & 7)) << 4), a, b2, c2, d2);
+          if (quad * 32 + rw < rows)
+            st_global_v4(p.dq + ((static_cast<int64_t>(row0) + rw) * p.heads + h) * D + 64 * half + 8 * j, a, b2,
+                         c2, d2);
+        }
+        __syncwarp();
+      }
+      return true;
+    }
+  }
   const bool q_ok = qt * kTile + r < lq;
   const int64_t qrow = (static_cast<int64_t>(q0) + qt * kTile + r) * p.heads + h;
   constexpr int kChunk = D / 2 < 32 ? D / 2 : 32;
@@ -788,6 +845,9 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
   const int R = (p.bias_len - 1) / 2;
   uint32_t s_it = 0, dp_it = 0, acc_it = 0;
   [[maybe_unused]] uint32_t dq_it = 0;
+  // DIRECT at d = 128: this warp's 4 KB of the X tile (its rows, its
+  // warpgroup's column block) stages dQ for its TMA store
+  [[maybe_unused]] uint8_t* dq_stage = smem + C::kXOff + half * (kTile * 128) + quad * 32 * 128;
   XRing x;
   const float hs = 0.5f * p.scale;                 // x / 2 = hs S + bias / 2
   const float s2 = p.scale * kLog2e;               // softmax: x log2 e
@@ -928,7 +988,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       if constexpr (DIRECT) {  // the previous query tile's dQ, before this tile's dP^T (d = 128: its columns)
         if (i > 0) {
           if (!(ok = read_dq<D>(p, bars, tmem + lane_off + kDqCol<D> + (D / 2) * half, half, r, u.seg.q0,
-                                u.seg.lq, u.h, pt - 1, dq_it & 1, fail)))
+                                u.seg.lq, u.h, pt - 1, dq_it & 1, fail, dq_stage)))
             break;
           ++dq_it;
         }
@@ -979,6 +1039,12 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         }
         if (chunk == 0 && !(ok = mbar_wait(&bars->x_empty[x.slot<C::kNumX>()], x.empty_parity<C::kNumX>(), fail)))
           break;
+        if constexpr (DIRECT && D == 128) {  // the dQ staged in X has been read by its TMA store
+          if (chunk == 0) {
+            if ((threadIdx.x & 31) == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+        }
         store_x_chunk(x_base + x.slot<C::kNumX>() * C::kXBytes, half, chunk, r, pk);
       }
       if (!ok) break;
@@ -1003,7 +1069,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     if (!ok) break;
     if constexpr (DIRECT) {
       if (!read_dq<D>(p, bars, tmem + lane_off + kDqCol<D> + (D / 2) * half, half, r, u.seg.q0, u.seg.lq, u.h,
-                      u.first + u.count - 1, dq_it & 1, fail))
+                      u.first + u.count - 1, dq_it & 1, fail, dq_stage))
         break;
       ++dq_it;
     }
@@ -1024,6 +1090,10 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       const int xs = x.slot<C::kNumX>();
       if (!mbar_wait(&bars->x_empty[xs], x.empty_parity<C::kNumX>(), fail)) break;
       const int lr = threadIdx.x & 31;
+      if constexpr (DIRECT && D == 128) {  // the dQ staged in X has been read by its TMA store
+        if (lr == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
       const uint32_t blk = x_base + xs * C::kXBytes + half * (kTile * 128) + quad * 32 * 128;
       __nv_bfloat16* base = half == 0 ? p.dv : p.dk;
       const int64_t row0 = grow - lr;  // global row of the warp's first row
@@ -1147,6 +1217,10 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
         atomicAdd(part + 2 * R, dbias_fixed(acc_hi));
       }
     }
+  }
+  if constexpr (DIRECT && D == 128) {  // this warp's dQ stores are complete before the CTA exits
+    if ((threadIdx.x & 31) == 0) bulk_wait_all();
+    __syncwarp();
   }
 }
 

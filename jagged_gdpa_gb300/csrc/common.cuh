@@ -205,6 +205,9 @@ struct BwdParams {
   float* dq_fused;
   const int32_t* kv_item_base;  // the scheduler's key-tile prefix per segment
   int32_t q_rows;               // rows of each dq_fused block (the shared query count)
+  // direct dQ at d = 128: boxes of 32 rows x 1 head x 64 columns over dq,
+  // 128-byte swizzle (the X tile's layout), for the TMA stores of dQ
+  CUtensorMap tm_dq;
 };
 
 constexpr int kDsTileBytes = kTile * kTile * 2;
