@@ -848,6 +848,7 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
   // DIRECT at d = 128: this warp's 4 KB of the X tile (its rows, its
   // warpgroup's column block) stages dQ for its TMA store
   [[maybe_unused]] uint8_t* dq_stage = smem + C::kXOff + half * (kTile * 128) + quad * 32 * 128;
+  [[maybe_unused]] const uint32_t t_dq = tmem + lane_off + kDqCol<D> + (D / 2) * half;  // DIRECT: dQ columns
   XRing x;
   const float hs = 0.5f * p.scale;                 // x / 2 = hs S + bias / 2
   const float s2 = p.scale * kLog2e;               // softmax: x log2 e
@@ -944,6 +945,17 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
       float keep0[32], keep1[32];  // act'(x) (GELU/SiLU) or P (softmax) per owned column
 #pragma unroll
       for (int chunk = 0; chunk < 2; ++chunk) {
+        if constexpr (DIRECT && D == 128) {
+          // the previous query tile's dQ, between the two halves of phase A:
+          // it is complete by then, and this tile's dP^T (into the same
+          // columns) then runs during the second half
+          if (chunk == 1 && i > 0) {
+            if (!(ok = read_dq<D>(p, bars, t_dq, half, r, u.seg.q0, u.seg.lq, u.h, pt - 1, dq_it & 1, fail,
+                                  dq_stage)))
+              break;
+            ++dq_it;
+          }
+        }
         if constexpr (D <= 64) {  // (at d = 128 this branch makes ptxas spill in the hot loop)
           if (chunk >= live) {    // no partner row in these columns: P^T (and later dS) zero
             if constexpr (KV_MAJOR) {
@@ -980,15 +992,16 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
 #undef JG_PHASE_A
         if constexpr (KV_MAJOR) tmem_st16(t_s + 16 * chunk, pk);  // P^T over S^T columns already read
       }
+      if (!ok) break;
       if constexpr (KV_MAJOR) {
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive_warp(&bars->p_full);
       }
-      if constexpr (DIRECT) {  // the previous query tile's dQ, before this tile's dP^T (d = 128: its columns)
+      if constexpr (DIRECT && D <= 64) {  // the previous query tile's dQ (its own columns)
         if (i > 0) {
-          if (!(ok = read_dq<D>(p, bars, tmem + lane_off + kDqCol<D> + (D / 2) * half, half, r, u.seg.q0,
-                                u.seg.lq, u.h, pt - 1, dq_it & 1, fail, dq_stage)))
+          if (!(ok = read_dq<D>(p, bars, t_dq, half, r, u.seg.q0, u.seg.lq, u.h, pt - 1, dq_it & 1, fail,
+                                dq_stage)))
             break;
           ++dq_it;
         }
@@ -1068,8 +1081,8 @@ __device__ void bwd_act(const BwdParams& p, uint8_t* smem, BwdBars* bars, uint32
     }
     if (!ok) break;
     if constexpr (DIRECT) {
-      if (!read_dq<D>(p, bars, tmem + lane_off + kDqCol<D> + (D / 2) * half, half, r, u.seg.q0, u.seg.lq, u.h,
-                      u.first + u.count - 1, dq_it & 1, fail, dq_stage))
+      if (!read_dq<D>(p, bars, t_dq, half, r, u.seg.q0, u.seg.lq, u.h, u.first + u.count - 1, dq_it & 1, fail,
+                      dq_stage))
         break;
       ++dq_it;
     }
