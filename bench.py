@@ -529,7 +529,7 @@ def run_native(args, world, rank, local):
     dom = max(kernels, key=lambda k: kernels[k][0])
     dom_ms, dom_fl, dom_by = kernels[dom]
     traffic = TRAFFIC.get(dom) if full_size else None
-    if hbm_bound:  # bound by HBM (the survey's roofline for this workload): algorithmic GB/s
+    if hbm_bound:  # a workload whose roofline is HBM: algorithmic GB/s
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(dom_by / (dom_ms * 1e-3) / 1e9, 1),
                     "peak": hbm, "unit": "GB/s", "frac": round(dom_by / (dom_ms * 1e-3) / 1e9 / hbm, 4),
                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic}
