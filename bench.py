@@ -107,9 +107,9 @@ HBM_BOUND = (2, 3, 4)
 # long-tail workload, from a one-pass ncu capture of the current kernels at
 # that size; emptied whenever a kernel changes after the capture.
 TRAFFIC = {
-    "gdpa_fwd_kernel": 1.468381e9 + 0.328024e9,
-    "gdpa_bwd_kernel (dK/dV pass)": 2.360132e9 + 13.150991e9,
-    "gdpa_dq_ds_kernel (dQ pass)": 12.909607e9 + 0.262244e9,
+    "gdpa_fwd_kernel": 1.478823e9 + 0.330478e9,
+    "gdpa_bwd_kernel (dK/dV pass)": 2.411085e9 + 13.152799e9,
+    "gdpa_dq_ds_kernel (dQ pass)": 12.910225e9 + 0.264045e9,
 }
 
 
