@@ -21,17 +21,16 @@
 //     dQ *= s; store
 //
 // The bf16 dS^T / dS that the activation warps produce go to a shared "X"
-// tile and dK / dQ read both operands from shared memory: on this GPU the
-// tensor core stalls for ~300 cycles each time it switches between MMAs whose
-// A operand comes from shared memory and from TMEM, while its shared-memory
-// operand reads do not compete with the warps' own shared-memory traffic.
-// The dq pass is therefore all shared-operand.  In dkdv only one X tile fits
-// at d = 128, and P^T and dS^T sharing it serialised phase B behind dV; P^T
-// goes back into TMEM over S^T instead (dV reads it from there) and the
-// switch this costs stays hidden because that pass is bound by the
-// activation warps.  The activation warps load a whole S (dP) tile into
-// registers before computing, so the next tile's S (dP) is computed while
-// they work.
+// tile, where the dK / dQ products, the TMA store of the dS tiles and the
+// direct dQ product read them.  In dkdv only one X tile fits at d = 128, and
+// P^T and dS^T sharing it serialised phase B behind dV; P^T goes back into
+// TMEM over S^T instead, and dV reads it from there -- which is also the
+// faster form: on this GPU an MMA whose A operand is in TMEM reads only B
+// from shared memory, and a 128 x 128 x 16 product takes ~80 cycles that way
+// against ~110 with both operands in shared memory (the shared-memory
+// operand stream, ~73 bytes a clock, is the limit).  The activation warps
+// load a whole S (dP) tile into registers before computing, so the next
+// tile's S (dP) is computed while they work.
 //
 // TMEM (512 columns): dkdv uses S^T [0,128), dP^T [128,256), dV [256,256+D),
 // dK [256+D, 256+2D); dq uses S [0,128), dP [128,256), dQ [256,256+D).  Two
@@ -312,8 +311,7 @@ struct XRing {
 //   [dP^T(i) loaded] dP^T(i+1) = V dO(i+1)^T
 // P^T stays in TMEM (A operand from TMEM) and only dS^T goes through the
 // shared X tile, so the two products of a tile never wait on each other for
-// X; the pass is bound by the activation warps, which hides the pipeline
-// switch between the TMEM-operand dV and the shared-operand MMAs.
+// X.
 // DIRECT (units of segments with dq_direct_segment only): after dK(i),
 // dQ(i) = dS(i) K of the unit's only key tile, complete, into kDqCol -- the
 // free columns past dK at d <= 64, dP^T's columns at d = 128 (once the
