@@ -356,7 +356,7 @@ def run_native(args, world, rank, local):
     stored = ds_scratch.numel() >= 128 * 128 * 2
     n_dq = 2 if fused_dq else (2 if stored else 1)
     # the forward's second launch: the key/value-resident units (keys within one
-    # tile, two or more query tiles), unless the short-query kernel runs
+    # tile), unless the short-query kernel runs
     fwd_kvres = not shortq and x.window == 0
     launches_per_step = (2 + int(shared) + int(fwd_kvres)) + \
         (2 + int(shared) + int(softmax) + int(dq_direct) + n_dq + int(bias_len > 0) + int(shared and not fused_dq))
@@ -480,7 +480,7 @@ def run_native(args, world, rank, local):
     # Algorithmic bytes per launch: the forward's b_fwd; the backward's b_bwd
     # split into dQ (written by the second pass) and the rest (the first).
     k_fwd = "gdpa_fwd_shortq_kernel" if shortq else "gdpa_fwd_kernel"
-    if fwd_kvres and np.any((np.asarray(x.lkv) >= 1) & (np.asarray(x.lkv) <= 128) & (np.asarray(x.lq) > 128)):
+    if fwd_kvres and np.any((np.asarray(x.lkv) >= 1) & (np.asarray(x.lkv) <= 128) & (np.asarray(x.lq) >= 1)):
         k_fwd = "gdpa_fwd_kernel + gdpa_fwd_kvres_kernel"
     if shortq:
         k_kv, k_q = "gdpa_bwd_shortq_kernel (dK, dV, dQ contributions)", "dq_fused_stage1/2 (dQ sum)"

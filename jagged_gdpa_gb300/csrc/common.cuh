@@ -127,12 +127,13 @@ __host__ __device__ __forceinline__ bool dq_direct_segment(int lq, int lkv, int 
   return window <= 0 && lq > 0 && lkv > 0 && lkv <= kTile;
 }
 
-// Forward: a segment whose keys fit one tile and that has at least two
-// query tiles runs in the key/value-resident forward (K and V loaded once
-// for up to kChunkTiles query tiles; a single query tile has nothing to
-// share them with).
+// Forward: a segment whose keys fit one tile runs in the key/value-resident
+// forward (K and V loaded once for up to kChunkTiles query tiles).  Segments
+// of a single query tile share nothing there, but taking them too leaves the
+// general forward fewer units, often none, when keys are short: measured
+// -1.4% on the short-K/V forward, no change on causal softmax.
 __host__ __device__ __forceinline__ bool kv_resident_segment(int lq, int lkv, int window) {
-  return dq_direct_segment(lq, lkv, window) && lq > kTile;
+  return dq_direct_segment(lq, lkv, window);
 }
 
 // Index of the i-th unit processed by CTA c of G (serpentine over rounds, so

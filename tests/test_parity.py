@@ -120,12 +120,12 @@ def test_edge_lengths(jg, act):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("act,causal,bias_len", [("gelu", False, 257), ("softmax", True, 0), ("silu", True, 7)])
 def test_key_value_resident_forward(jg, d, act, causal, bias_len):
-    """Segments whose keys fit one tile and that have two or more query tiles
-    (the key/value-resident forward and the direct-dQ backward): one to 128
-    keys, query counts across one and two chunks of 16 query tiles (2048 /
-    2049 rows), next to segments that take the general kernels."""
-    lq = [129, 256, 2048, 2049, 300, 4096, 1, 5000, 200]
-    lkv = [1, 64, 127, 128, 128, 33, 100, 300, 0]
+    """Segments whose keys fit one tile (the key/value-resident forward and
+    the direct-dQ backward): one to 128 keys, query counts from one row to
+    across one and two chunks of 16 query tiles (2048 / 2049 rows), next to
+    segments that take the general kernels."""
+    lq = [129, 256, 2048, 2049, 300, 4096, 1, 5000, 200, 128, 77]
+    lkv = [1, 64, 127, 128, 128, 33, 100, 300, 0, 128, 5]
     rng = np.random.default_rng(11 + d)
     x = workloads.make_inputs(lq, lkv, 2, d, act, causal=causal, bias_len=bias_len, rng=rng)
     check_fwd_full(jg, x, f"kv-resident fwd d={d} {act} causal={causal}")
