@@ -638,6 +638,10 @@ __device__ void fwd_act(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
         }
       }
     } else {
+      // 32-byte stores where out allows them: half the store instructions,
+      // whole 32-byte sectors (a thread owns one row, so each instruction
+      // still touches 32 rows)
+      const bool v8 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
@@ -645,12 +649,17 @@ __device__ void fwd_act(const FwdParams& p, uint8_t* smem, FwdBars* bars, uint32
         tmem_ld_wait(o);
         if (row_ok) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint32_t w[4];
+          for (int c = 0; c < 32; c += 16) {
+            uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
+            for (int e = 0; e < 8; ++e)
               w[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * inv_l, __uint_as_float(o[c + 2 * e + 1]) * inv_l);
-            st_global_v4(out_row + c0 + c, w[0], w[1], w[2], w[3]);
+            if (v8) {
+              st_global_v8(out_row + c0 + c, w);
+            } else {
+              st_global_v4(out_row + c0 + c, w[0], w[1], w[2], w[3]);
+              st_global_v4(out_row + c0 + c + 8, w[4], w[5], w[6], w[7]);
+            }
           }
         }
       }
@@ -996,6 +1005,7 @@ __device__ void kvr_act(const FwdParams& p, uint8_t* smem, KvrBars* bars, uint32
         }
       } else {
         __nv_bfloat16* out_row = p.out + (grow * H + u.h) * D;
+        const bool v8 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -1005,14 +1015,19 @@ __device__ void kvr_act(const FwdParams& p, uint8_t* smem, KvrBars* bars, uint32
             tc_fence_before();
             mbar_arrive_warp(&bars->o_empty[w]);
           }
-          if (r < rows) {
+          if (r < rows) {  // 32-byte stores where out allows them (as in the general kernel)
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              uint32_t wd[4];
+            for (int c = 0; c < 32; c += 16) {
+              uint32_t wd[8];
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
+              for (int e = 0; e < 8; ++e)
                 wd[e] = pack_bf16(__uint_as_float(o[c + 2 * e]) * inv_l, __uint_as_float(o[c + 2 * e + 1]) * inv_l);
-              st_global_v4(out_row + c0 + c, wd[0], wd[1], wd[2], wd[3]);
+              if (v8) {
+                st_global_v8(out_row + c0 + c, wd);
+              } else {
+                st_global_v4(out_row + c0 + c, wd[0], wd[1], wd[2], wd[3]);
+                st_global_v4(out_row + c0 + c + 8, wd[4], wd[5], wd[6], wd[7]);
+              }
             }
           }
         }
