@@ -132,6 +132,29 @@ def test_key_value_resident_forward(jg, d, act, causal, bias_len):
     check_bwd_full(jg, x, f"kv-resident bwd d={d} {act} causal={causal}")
 
 
+@pytest.mark.parametrize("d,act", [(128, "softmax"), (64, "softmax"), (32, "gelu")])
+def test_forward_output_16_byte_aligned(jg, d, act):
+    """O written through a pointer that is 16- but not 32-byte aligned: the
+    epilogues that store 32 bytes at a time where they can (softmax, d = 32)
+    fall back to 16-byte stores, in the general and the key/value-resident
+    kernels."""
+    lq = [300, 77, 1, 2049, 128]
+    lkv = [300, 5, 100, 64, 513]
+    rng = np.random.default_rng(21 + d)
+    x = workloads.make_inputs(lq, lkv, 2, d, act, causal=act == "softmax", bias_len=7, rng=rng)
+    dev = x.to("cuda")
+    n = x.q.shape[0] * x.heads * d
+    buf = torch.zeros(n + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(x.q.shape[0], x.heads, d)
+    assert out.data_ptr() % 32 == 16
+    o, _ = jg.jgdpa_fwd(dev.q, dev.k, dev.v, dev.q_offsets, dev.kv_offsets, x.act, x.scale, bias_table=dev.bias,
+                        causal=x.causal, out=out)
+    torch.cuda.synchronize()
+    ref, _ = oracle_fwd(x)
+    assert_close(f"O, 16-byte aligned out, d={d} {act}", o.cpu(), ref)
+    assert torch.count_nonzero(buf[:8]).item() == 0, "bytes before out written"
+
+
 # ------------------------------------------------------------ sliding window
 WINDOW_FWD = [(d, act, causal, w) for d in (64, 128) for act in ("gelu", "silu", "softmax")
               for causal in (False, True) for w in (1, 129, 300)]
