@@ -35,10 +35,11 @@ namespace jg {
 // Routes of the four 32-column chunks of every S tile: the last
 // JGDPA_FWD_ALU_CHUNKS take the ALU polynomial route, the
 // JGDPA_FWD_EX2_CHUNKS before them the ex2 route, the rest the hardware tanh.
-// Measured on GB300 (long-tail workload, 24 heads, d = 128, GELU): every chunk
-// moved off the tanh route made the forward slower (0/1/3/4 ex2 chunks:
-// 2.83/3.06/3.49/3.85 ms; ALU chunks likewise), so both default to 0 and
-// the other routes stay available as compile-time options.
+// Measured on GB300 (long-tail workload, d = 128, GELU): every chunk moved
+// off the tanh route made the forward slower (0/1/3/4 ex2 chunks:
+// 2.83/3.06/3.49/3.85 ms on an earlier build; 0/1/2 ALU chunks: 2.63/3.01/
+// 3.63 ms), so both default to 0 and the other routes stay available as
+// compile-time options.
 #ifndef JGDPA_FWD_ALU_CHUNKS
 #define JGDPA_FWD_ALU_CHUNKS 0
 #endif
